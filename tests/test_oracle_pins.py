@@ -1,0 +1,318 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these tests retypes the oracle's formulas to compare it with itself:
+they check printed values of the pages' worked example, closed forms,
+invariants the pages state, and exact (rational) brute force on tiny layers
+(the latter lives in test_oracle_bruteforce.py).
+"""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import awq_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            k, v = line.split("=", 1)
+            vals[k.strip()] = [float(x) for x in v.split()]
+    return vals
+
+
+def _tol(printed):
+    """Half a unit in the last digit the page printed."""
+    s = repr(printed)
+    if "." not in s:
+        return 0.5
+    return 0.5 * 10.0 ** -(len(s.split(".")[1]))
+
+
+WE = _read_golden("worked_example_two_channel.txt")
+
+
+def _close_printed(actual, printed_list):
+    for a, p in zip(np.ravel(actual), printed_list):
+        assert abs(a - p) <= _tol(p) + 1e-12, (a, p)
+
+
+# --------------------------------------------------------------------------
+# Worked example ("AWQ > Worked Example: Tracing AWQ Through a Two-Channel Layer")
+# --------------------------------------------------------------------------
+
+def test_worked_example_quantizer_with_page_scales():
+    """The page's own normalisation s = (abar / max abar) ** alpha."""
+    w = np.array([WE["w"]], dtype=np.float32)
+    s = np.array(WE["s_page"], dtype=np.float32)
+    bits = int(WE["bits"][0])
+    Wq, gq = O.fake_quant(w, s, bits, group=2, sym=True)
+    _close_printed(w * s, WE["w_scaled"])
+    _close_printed(gq.scale, WE["step_awq"])
+    assert list(gq.q.ravel()) == WE["codes_awq"]
+    _close_printed(Wq, WE["w_eff_awq"])
+    abar = np.array(WE["abar"])
+    _close_printed(np.abs(w[0] - Wq[0]) * abar, WE["err_awq"])
+
+
+def test_worked_example_rtn():
+    w = np.array([WE["w"]], dtype=np.float32)
+    bits = int(WE["bits"][0])
+    gq = O.quantize_groups(w, bits, group=2, sym=True)
+    _close_printed(gq.scale, WE["step_rtn"])
+    assert list(gq.q.ravel()) == WE["codes_rtn"]
+    _close_printed(gq.w_hat, WE["w_rtn"])
+    abar = np.array(WE["abar"])
+    _close_printed(np.abs(w[0] - gq.w_hat[0]) * abar, WE["err_rtn"])
+
+
+def test_worked_example_through_search():
+    """Full search path with one calibration token X = abar (so mean|X| = abar).
+
+    The search centres s by sqrt(max*min) instead of the page's max: both are
+    alpha-independent factors, so codes, effective weights and the output
+    error are the page's.  grid = 2 puts alpha = 0.5 on the grid.
+    """
+    w = np.array([WE["w"]], dtype=np.float32)
+    X = np.array([WE["abar"]], dtype=np.float64)
+    res = O.awq_search(w, X, bits=3, group=2, grid=2, sym=True)
+    assert res.alphas[1] == WE["alpha"][0]
+    # output error |X (Wq - W)^T| = sum over channels of the page's weighted errors
+    _close_printed(np.sqrt(res.errs[1]), [sum(WE["err_awq"])])
+    _close_printed(np.sqrt(res.errs[0]), [sum(WE["err_rtn"])])
+    Wq, gq = O.fake_quant(w, res.s32[1], 3, 2, True)
+    assert list(gq.q.ravel()) == WE["codes_awq"]
+    _close_printed(Wq, WE["w_eff_awq"])
+    # the search keeps the smallest error; AWQ at alpha=0.5 beats RTN here
+    assert res.errs[res.best] <= res.errs[1] < res.errs[0]
+
+
+# --------------------------------------------------------------------------
+# Closed forms and invariants stated on the pages
+# --------------------------------------------------------------------------
+
+def test_salience_closed_form():
+    X = np.array([[1.0, -2.0, 0.0], [3.0, 4.0, 0.0]])
+    sx = O.channel_salience(X)
+    assert sx[0] == 2.0 + 1e-8 and sx[1] == 3.0 + 1e-8
+    assert sx[2] == 1e-8          # always-zero channel keeps a nonzero scale
+
+
+def test_alpha_grid():
+    a = O.alpha_grid(20)
+    assert a.size == 21 and a[0] == 0.0 and a[-1] == 1.0
+    assert np.allclose(np.diff(a), 0.05, atol=1e-15)
+    a41 = O.alpha_grid(40)
+    assert a41.size == 41 and np.allclose(np.diff(a41), 0.025, atol=1e-15)
+
+
+def test_centring_is_geometric():
+    rng = np.random.default_rng(1)
+    sx = rng.uniform(0.3, 80.0, size=257)
+    for a in (0.0, 0.25, 0.5, 1.0):
+        s, s32 = O.centred_scales(sx, a)
+        assert abs(s.max() * s.min() - 1.0) < 1e-14
+        # monotone in s_X: larger salience never gets a smaller scale
+        order = np.argsort(sx)
+        assert np.all(np.diff(s[order]) >= 0)
+        assert s32.dtype == np.float32
+
+
+def test_alpha_zero_is_plain_rtn():
+    """alpha = 0 gives s = 1 exactly, so the search starts from plain RTN."""
+    rng = np.random.default_rng(2)
+    W = (rng.standard_normal((16, 64)) * 0.02).astype(np.float32)
+    X = rng.standard_normal((8, 64))
+    sx = O.channel_salience(X)
+    s, s32 = O.centred_scales(sx, 0.0)
+    assert np.all(s == 1.0) and np.all(s32 == np.float32(1.0))
+    for sym in (True, False):
+        Wq, _ = O.fake_quant(W, s32, 4, 32, sym)
+        assert np.array_equal(Wq, O.rtn_fake_quant(W, 4, 32, sym))
+        res = O.awq_search(W, X, bits=4, group=32, grid=20, sym=sym)
+        ref = X @ W.astype(np.float64).T
+        assert res.errs[0] == O.output_mse(X, O.rtn_fake_quant(W, 4, 32, sym), ref)
+        assert res.errs[res.best] <= res.errs[0]
+
+
+def test_flat_salience_reduces_to_rtn():
+    """Equal mean |X| in every channel: s = 1 for every alpha, all errors tie,
+    and the strict comparison keeps the first alpha (plain RTN)."""
+    rng = np.random.default_rng(3)
+    W = (rng.standard_normal((8, 32)) * 0.02).astype(np.float32)
+    X = np.where(rng.random((5, 32)) < 0.5, -1.0, 1.0) * 0.37
+    res = O.awq_search(W, X, bits=3, group=16, grid=20, sym=False)
+    assert np.all(res.s32 == np.float32(1.0))
+    assert np.all(res.errs == res.errs[0])
+    assert res.best == 0
+
+
+def test_scaling_identity_before_rounding():
+    """(W diag(s)) (diag(s)^-1 X) = W X, and the oracle's Wq is the deployed
+    computation: X @ Wq^T = (X / s) @ Q(W s)^T."""
+    rng = np.random.default_rng(4)
+    W = rng.standard_normal((12, 48)) * 0.02
+    X = rng.standard_normal((7, 48)) * rng.uniform(0.5, 50, size=48)
+    s = rng.uniform(0.1, 10.0, size=48)
+    lhs = (X / s) @ (W * s).T
+    rhs = X @ W.T
+    assert np.max(np.abs(lhs - rhs)) <= 1e-12 * np.max(np.abs(rhs))
+    s32 = s.astype(np.float32)
+    Wq, gq = O.fake_quant(W.astype(np.float32), s32, 4, 16, True)
+    deployed = (X / s32.astype(np.float64)) @ gq.w_hat.astype(np.float64).T
+    assert np.max(np.abs(X @ Wq.T - deployed)) <= 1e-12 * np.max(np.abs(deployed))
+    # the error is linear in the weight change: X Wq^T - X W^T = X (Wq - W)^T
+    W32 = W.astype(np.float32).astype(np.float64)
+    d1 = X @ Wq.T - X @ W32.T
+    d2 = X @ (Wq - W32).T
+    assert np.max(np.abs(d1 - d2)) <= 1e-12 * np.max(np.abs(X @ W32.T))
+
+
+def test_power_of_two_homogeneity():
+    """Scaling t by 2^k leaves codes and zero points unchanged and scales
+    every group step by exactly 2^k (both quantizers are positively
+    homogeneous, and multiplying by 2^k is exact)."""
+    rng = np.random.default_rng(5)
+    t = (rng.standard_normal((9, 64)) * 0.05).astype(np.float32)
+    for sym in (True, False):
+        base = O.quantize_groups(t, 4, 16, sym)
+        for k in (-3, 1, 5):
+            f = np.float32(2.0 ** k)
+            g = O.quantize_groups(t * f, 4, 16, sym)
+            assert np.array_equal(g.q, base.q)
+            assert np.array_equal(g.zero, base.zero)
+            assert np.array_equal(g.scale, base.scale * f)
+
+
+@pytest.mark.parametrize("sym", [True, False])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_quantizer_bounds(sym, bits):
+    rng = np.random.default_rng(6 + bits)
+    t = (rng.standard_normal((20, 128)) * 0.03).astype(np.float32)
+    t[0, :32] = np.abs(t[0, :32])       # an all-positive group
+    t[1, :32] = -np.abs(t[1, :32])      # an all-negative group
+    t[2, :32] = 0.0                     # an all-zero group
+    g = O.quantize_groups(t, bits, 32, sym)
+    if sym:
+        L = 2 ** (bits - 1) - 1
+        assert g.q.min() >= -L - 1 and g.q.max() <= L
+        # scale = max/L means the clamp never fires: codes stay in [-L, L]
+        assert g.q.min() >= -L
+    else:
+        maxq = 2 ** bits - 1
+        assert g.q.min() >= 0 and g.q.max() <= maxq
+        assert g.zero.min() >= 0 and g.zero.max() <= maxq
+        assert np.all(g.zero[0, 0] == 0)            # all-positive: lo = 0
+        assert g.zero[1, 0] == maxq                 # all-negative: hi = 0
+    # rounding error at most half a step (relative slack for float32 rounding)
+    step = np.repeat(g.scale, 32, axis=1)
+    err = np.abs(g.w_hat.astype(np.float64) - t)
+    assert np.all(err <= 0.5 * step * (1 + 1e-5) + 1e-30)
+    assert np.all(g.w_hat[2, :32] == 0)
+    assert np.all(g.scale[2, 0] == np.float32(1e-8))
+
+
+def test_fp64_quantizer_differs_only_at_near_ties():
+    rng = np.random.default_rng(7)
+    t = (rng.standard_normal((64, 512)) * 0.02).astype(np.float32)
+    for sym in (True, False):
+        a = O.quantize_groups(t, 4, 128, sym)
+        b = O.quantize_groups_f64(t, 4, 128, sym)
+        diff = a.q != b.q
+        assert diff.sum() <= 3
+        if diff.any():
+            r = t.astype(np.float64) / np.repeat(b.scale, 128, axis=1)
+            frac = np.abs(np.abs(r - np.floor(r)) - 0.5)
+            assert np.all(frac[diff] < 1e-5)
+
+
+def test_awq_beats_rtn_on_outlier_layer():
+    """The notebook's check: with a few high-activation channels the searched
+    scales give a lower output MSE than RTN ("GPTQ and AWQ weight
+    quantisation", awq_beats_rtn_on_output_mse), and the error is finite and
+    positive (awq_outputs_finite)."""
+    rng = np.random.default_rng(8)
+    W = (rng.standard_normal((256, 512)) * 0.02).astype(np.float16).astype(np.float32)
+    X = rng.standard_normal((64, 512))
+    X[:, rng.permutation(512)[:8]] *= 6.0
+    res = O.awq_search(W, X, bits=4, group=128, grid=20, sym=True)
+    assert res.best > 0
+    assert res.errs[res.best] < res.errs[0]
+    assert np.isfinite(res.errs).all() and res.errs[res.best] > 0
+
+
+def test_nonfinite_input_has_no_answer():
+    W = np.ones((2, 4), dtype=np.float32)
+    X = np.ones((3, 4))
+    X[0, 0] = np.nan
+    res = O.awq_search(W, X, bits=4, group=4, grid=4, sym=True)
+    assert res.best == -1 and np.all(np.isnan(res.errs))
+
+
+# --------------------------------------------------------------------------
+# Storage and packing
+# --------------------------------------------------------------------------
+
+def test_pack_layout_by_hand():
+    u = np.array([[1, 2, 3, 4, 5, 6, 7, 8, 9]], dtype=np.uint32)
+    w = O.pack_bits(u, 4)
+    assert w.shape == (1, 2)
+    assert w[0, 0] == 0x87654321 and w[0, 1] == 0x9
+    u3 = np.full((1, 11), 7, dtype=np.uint32)
+    w3 = O.pack_bits(u3, 3)
+    assert w3.shape == (1, 2) and w3[0, 0] == 0xFFFFFFFF and w3[0, 1] == 0x1
+    u3b = np.array([[1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 6]], dtype=np.uint32)
+    w3b = O.pack_bits(u3b, 3)
+    # code 10 (value 0b110) sits at bits 30..32: bit 31 of word 0 and bit 0 of word 1
+    assert w3b[0, 0] == 0x80000001 and w3b[0, 1] == 0x1
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 8])
+def test_pack_roundtrip(bits):
+    rng = np.random.default_rng(bits)
+    u = rng.integers(0, 2 ** bits, size=(5, 77)).astype(np.uint32)
+    assert np.array_equal(O.unpack_bits(O.pack_bits(u, bits), bits, 77), u)
+
+
+def test_storage_ratio_notebook_layer():
+    """4096 x 4096 layer at 4 bits: 8 MiB of codes; with one fp16 scale per
+    group of 128 the notebook gets 8.25 MiB, "4x" within 5 %
+    ("GPTQ and AWQ weight quantisation", "Storage math")."""
+    out = n_in = 4096
+    rng = np.random.default_rng(9)
+    W = (rng.standard_normal((out, n_in)) * 0.02).astype(np.float32)
+    s32 = np.ones(n_in, dtype=np.float32)
+    qweight, scales, zeros = O.quantize_pack(W, s32, 4, 128, True)
+    assert qweight.dtype == np.uint32 and qweight.nbytes == 8 * 2 ** 20
+    assert scales.shape == (out, n_in // 128) and zeros.shape == scales.shape
+    assert np.all(zeros == 8)
+    bytes_int4 = qweight.nbytes + scales.size * 2
+    assert bytes_int4 == int(8.25 * 2 ** 20)
+    ratio = (out * n_in * 2) / bytes_int4
+    assert abs(ratio - 4.0) <= 0.05 * 4.0
+    # decoding the packed words gives back the symmetric codes
+    codes = O.unpack_bits(qweight[:4], 4, n_in).astype(np.int64) - 8
+    assert np.array_equal(codes, O.quantize_groups(W[:4], 4, 128, True).q.astype(np.int64))
+
+
+def test_asym_code_formula_at_exact_ties():
+    """The code is round(w / scale) + zero, as the page writes it ("AWQ vs GPTQ
+    ...", "The shared problem"), not round(w / scale + zero): the two differ
+    when w / scale is exactly k + 1/2 and the zero point is odd.  A group with
+    lo = -3, hi = 12 has scale (12 + 3) / 15 = 1 and zero 3 exactly."""
+    t = np.array([[-3.0, 12.0, 0.5, 1.5, -2.5, 2.0, 0.0, 4.5]], dtype=np.float32)
+    g = O.quantize_groups(t, 4, 8, sym=False)
+    assert g.scale[0, 0] == 1.0 and g.zero[0, 0] == 3.0
+    # half-to-even of the quotient first: 0.5 -> 0, 1.5 -> 2, -2.5 -> -2, 4.5 -> 4
+    assert list(g.q[0]) == [0.0, 15.0, 3.0, 5.0, 1.0, 5.0, 3.0, 7.0]
+    # symmetric ties: scale = 3.5 / 7 = 0.5, so 0.25 / 0.5 = 0.5 -> 0 and 0.75 -> 2
+    ts = np.array([[3.5, 0.25, 0.75, -0.25, -0.75, 1.25, 0.0, -3.5]], dtype=np.float32)
+    gs = O.quantize_groups(ts, 4, 8, sym=True)
+    assert gs.scale[0, 0] == 0.5
+    assert list(gs.q[0]) == [7.0, 0.0, 2.0, -0.0, -2.0, 2.0, 0.0, -7.0]
