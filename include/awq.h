@@ -1,0 +1,182 @@
+/*
+ * awq.h - C ABI of libawq: AWQ's per-layer activation-aware scale search on
+ * one NVIDIA B300 (sm_103a).
+ *
+ * The method (stated in "AWQ (activation-aware weight quantization)",
+ * sections "How it works" and "The code, line by line"): for one linear
+ * layer W (out x in) with calibration inputs X (N x in),
+ *
+ *   s_X[j]  = mean_n |X[n, j]| + 1e-8
+ *   for alpha in linspace(0, 1, grid + 1):
+ *       s   = s_X ** alpha,  s /= sqrt(max(s) * min(s))
+ *       Wq  = Q(W * s) / s            Q = group round-to-nearest
+ *       err = mean((X Wq^T - X W^T)^2)
+ *   keep the alpha with the smallest err (strict <, first wins)
+ *
+ * then the weights are quantized once more at the kept scales and packed
+ * ("AWQ vs GPTQ Quantization Architectures Compared", "What lands on disk").
+ *
+ * Conventions for every entry point:
+ *  - All array pointers are DEVICE pointers owned by the caller, contiguous
+ *    and row-major.  The library never allocates device memory; scratch
+ *    comes from the caller's workspace.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously.  Nothing synchronises the host.
+ *  - The return value reports host-side argument checks and launch errors
+ *    (awq_status).  Errors found on the device are written to *dev_status
+ *    (an int32 in device memory, may be NULL): a call sets it to its error
+ *    code only if it is still 0, and never clears it.  Read it after
+ *    synchronising the stream.
+ *  - dtype applies to both W and X: AWQ_F32, AWQ_F16 or AWQ_BF16.
+ */
+#ifndef AWQ_H
+#define AWQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same types as cudaStream_t / cudaEvent_t; declared here so that the
+ * header needs no CUDA include. */
+typedef struct CUstream_st* awq_stream_t;
+typedef struct CUevent_st* awq_event_t;
+
+typedef enum {
+    AWQ_F32 = 0,
+    AWQ_F16 = 1,
+    AWQ_BF16 = 2
+} awq_dtype;
+
+typedef enum {
+    AWQ_OK = 0,
+    AWQ_ERR_INVALID_ARG = 1,  /* a size, pointer or parameter is out of range */
+    AWQ_ERR_UNSUPPORTED = 2,  /* valid for the method, not handled by this build */
+    AWQ_ERR_NONFINITE = 3,    /* every alpha's error was NaN/inf, or a NaN product in pack */
+    AWQ_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out; outputs are invalid */
+    AWQ_ERR_CUDA = 5          /* a CUDA runtime call failed */
+} awq_status;
+
+/* Text for a status code (static storage). */
+const char* awq_status_string(int status);
+
+/*
+ * awq_channel_stats - per-input-channel activation size.
+ *   sx[j] = (1/N) * sum_n |X[n, j]| + 1e-8, accumulated in float64.
+ * ["AWQ (activation-aware weight quantization)", "How it works" step 1 and
+ *  "The code, line by line", first bullet.]
+ *
+ *   X   [N][in] of `dtype`          (read)
+ *   sx  [in] double                 (written)
+ * N >= 1, in >= 1.  For 16-bit X the float64 sums are exact, so sx does
+ * not depend on the summation order.
+ */
+int awq_channel_stats(const void* X, int dtype, int64_t N, int64_t in,
+                      double* sx, int32_t* dev_status, awq_stream_t stream);
+
+/*
+ * Bytes of device workspace awq_search needs for these sizes (0 on invalid
+ * sizes).  The workspace must be 256-byte aligned.
+ */
+size_t awq_search_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N,
+                                  int group, int grid);
+
+/*
+ * awq_search - the alpha-grid scale search.
+ * ["AWQ (activation-aware weight quantization)", "Source code";
+ *  "AWQ vs GPTQ ...", "AWQ: move the error away from what matters"]
+ *
+ *   W      [out][in] of `dtype`   layer weights (read)
+ *   X      [N][in]   of `dtype`   calibration inputs (read)
+ *   sx     [in] double or NULL    channel sizes; NULL = computed here as
+ *                                 awq_channel_stats does
+ *   bits   2..8                   code width
+ *   group  columns per quantization group; divides `in`.  group == in is the
+ *          pages' "one group per row".  This build's search handles group
+ *          in {32, 64, 128}; others return AWQ_ERR_UNSUPPORTED.
+ *   sym    1: symmetric, scale = max|w| / (2^(b-1) - 1), codes in
+ *             [-2^(b-1), 2^(b-1) - 1]
+ *             ["GPTQ and AWQ weight quantisation", "Output MSE vs bit width"]
+ *          0: asymmetric, scale = (max(hi,0) - min(lo,0)) / (2^b - 1),
+ *             zero = round(-min/scale), codes in [0, 2^b - 1]
+ *             ["AWQ vs GPTQ ...", "The shared problem: one layer, sixteen levels"]
+ *   grid   1..4096; the search tries the grid + 1 alphas k/grid, k = 0..grid
+ *   workspace, workspace_bytes  >= awq_search_workspace_bytes(...)
+ *   err    [grid + 1] double      (written) mean((X (Wq - W)^T)^2) per alpha
+ *   best   [1] int32              (written) index of the kept alpha; -1 and
+ *                                 AWQ_ERR_NONFINITE in *dev_status if every
+ *                                 error is NaN or infinite
+ *   s_best [in] float             (written) the kept centred scale vector,
+ *                                 rounded to float32
+ *
+ * The error is formed as X (Wq - W)^T, which equals the pages' X Wq^T - X W^T;
+ * the GEMM runs on the tensor cores with fp16 operands (X and the weight
+ * change each scaled by an exact power of two chosen from max|X| and max|W|)
+ * and fp32 accumulation, the per-alpha sum in float64.  Rows, tokens and
+ * alphas are summed in a fixed order: repeated calls give bit-identical
+ * results.  Shared-input layer groups (q/k/v) are searched by passing their
+ * weights concatenated along `out` with the common X: one s, one error.
+ * Requirements beyond the method's: W and X 16-byte aligned, out, in, N
+ * <= 2^24.
+ */
+int awq_search(const void* W, const void* X, int dtype,
+               int64_t out, int64_t in, int64_t N,
+               const double* sx, int bits, int group, int sym, int grid,
+               void* workspace, size_t workspace_bytes,
+               double* err, int32_t* best, float* s_best,
+               int32_t* dev_status, awq_stream_t stream);
+
+/* Options for awq_search_ex; zero-initialise, then set what you need. */
+typedef struct {
+    awq_event_t ev_search_start;  /* recorded on `stream` right before the fused search kernel */
+    awq_event_t ev_search_stop;   /* recorded right after it (both or neither) */
+    int64_t wait_limit_ns;        /* bound of each device-side wait; 0 = 2 s */
+    int test_timeout;             /* nonzero: the search kernel also waits on a barrier that
+                                     nothing arrives at, so the bounded wait runs out and the
+                                     call reports AWQ_ERR_TIMEOUT (tests of the error path) */
+    uint32_t* diag;               /* NULL, or 4 device words, cleared by the call: when a wait
+                                     runs out they receive {site, block, sequence, parity} of
+                                     the first wait that gave up (site 0 = none) */
+} awq_search_opts;
+
+/* awq_search with options (opts may be NULL). */
+int awq_search_ex(const void* W, const void* X, int dtype,
+                  int64_t out, int64_t in, int64_t N,
+                  const double* sx, int bits, int group, int sym, int grid,
+                  void* workspace, size_t workspace_bytes,
+                  double* err, int32_t* best, float* s_best,
+                  int32_t* dev_status, awq_stream_t stream,
+                  const awq_search_opts* opts);
+
+/*
+ * awq_quantize_pack - quantize W * s once and pack the codes.
+ * ["AWQ vs GPTQ ...", "What lands on disk"; "GPTQ and AWQ weight
+ *  quantisation", "Storage math"]
+ *
+ *   W        [out][in] of `dtype`       (read)
+ *   s        [in] float                 column scales (e.g. s_best)
+ *   qweight  [out][ceil(in*bits/32)] uint32 (written)  code i of a row sits
+ *            at bit i*bits of the row's little-endian bit stream; high bits
+ *            of the last word are zero
+ *   scales   [out][in/group] float      (written) group step
+ *   zeros    [out][in/group] uint8      (written) zero point
+ * Codes are unsigned: symmetric codes are stored as q + 2^(b-1) with zero
+ * 2^(b-1), so that every code decodes as scale * (u - zero).
+ * Arithmetic is IEEE float32 with round-to-nearest on every operation and
+ * round-half-to-even for the codes: t = w*s, scale = max(m/L, 1e-8) or
+ * max((hi-lo)/maxq, 1e-8), code = round(t/scale) (+ zero, clamped).
+ * Any group size dividing `in` is accepted.  A NaN product w*s sets
+ * AWQ_ERR_NONFINITE.
+ */
+int awq_quantize_pack(const void* W, int dtype, int64_t out, int64_t in,
+                      const float* s, int bits, int group, int sym,
+                      uint32_t* qweight, float* scales, uint8_t* zeros,
+                      int32_t* dev_status, awq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AWQ_H */

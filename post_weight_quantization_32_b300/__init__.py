@@ -1,0 +1,191 @@
+"""AWQ per-layer activation-aware scale search on one B300 (sm_103a).
+
+A thin ctypes binding over ``libawq.so`` (C ABI in include/awq.h).  Every
+step of the computation runs in the library's CUDA kernels; this module only
+checks tensor shapes and dtypes, allocates outputs and workspace with
+PyTorch, and passes pointers and the current CUDA stream.  Importing it
+fails loudly if the library has not been built.
+
+Entry points (same names as the C ABI):
+
+* ``awq_channel_stats(X)`` -> s_X (float64, [in])
+* ``awq_search(W, X, bits, group, sym, grid)`` -> (err float64 [grid+1],
+  best int32 [1], s_best float32 [in])
+* ``awq_quantize_pack(W, s, bits, group, sym)`` -> (qweight, scales, zeros):
+  qweight int32 [out, ceil(in*bits/32)] holding the uint32 words (view it
+  as unsigned), scales float32 [out, in/group], zeros uint8 [out, in/group]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = [
+    "AWQError", "SearchOpts", "lib", "awq_channel_stats", "awq_search",
+    "awq_search_workspace_bytes", "awq_quantize_pack", "new_status", "check_status", "STATUS",
+    "DTYPE",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libawq.so")
+
+DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+STATUS = {0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARG", 2: "AWQ_ERR_UNSUPPORTED", 3: "AWQ_ERR_NONFINITE",
+          4: "AWQ_ERR_TIMEOUT", 5: "AWQ_ERR_CUDA"}
+
+EXPORTS = ("awq_status_string", "awq_channel_stats", "awq_search_workspace_bytes", "awq_search",
+           "awq_search_ex", "awq_quantize_pack")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libawq.so is not built (run `python post_weight_quantization_32_b300/build.py`)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    L.awq_status_string.restype = ctypes.c_char_p
+    L.awq_status_string.argtypes = [i32]
+    L.awq_channel_stats.restype = i32
+    L.awq_channel_stats.argtypes = [vp, i32, i64, i64, vp, vp, vp]
+    L.awq_search_workspace_bytes.restype = sz
+    L.awq_search_workspace_bytes.argtypes = [i32, i64, i64, i64, i32, i32]
+    L.awq_search.restype = i32
+    L.awq_search.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, i32, vp, sz, vp, vp, vp,
+                             vp, vp]
+    L.awq_search_ex.restype = i32
+    L.awq_search_ex.argtypes = L.awq_search.argtypes + [vp]
+    L.awq_quantize_pack.restype = i32
+    L.awq_quantize_pack.argtypes = [vp, i32, i64, i64, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+    return L
+
+
+lib = _load()
+
+
+class AWQError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s (%s)" % (where, STATUS.get(code, code),
+                                          lib.awq_status_string(int(code)).decode()))
+
+
+class SearchOpts(ctypes.Structure):
+    """awq_search_opts of the C ABI."""
+    _fields_ = [("ev_search_start", ctypes.c_void_p), ("ev_search_stop", ctypes.c_void_p),
+                ("wait_limit_ns", ctypes.c_int64), ("test_timeout", ctypes.c_int),
+                ("diag", ctypes.c_void_p)]
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise AWQError(code, where)
+
+
+def _need(t: torch.Tensor, name: str, ndim: int) -> None:
+    if not t.is_cuda or not t.is_contiguous() or t.dim() != ndim:
+        raise ValueError("%s must be a contiguous %d-D CUDA tensor" % (name, ndim))
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status word."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def check_status(dev_status: torch.Tensor, where: str = "device") -> None:
+    """Synchronise and raise if a kernel reported an error."""
+    code = int(dev_status.item())
+    if code != 0:
+        raise AWQError(code, where)
+
+
+def awq_channel_stats(X: torch.Tensor, sx: Optional[torch.Tensor] = None, stream=None,
+                      dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    _need(X, "X", 2)
+    N, n_in = X.shape
+    if sx is None:
+        sx = torch.empty(n_in, dtype=torch.float64, device=X.device)
+    _check(lib.awq_channel_stats(_ptr(X), DTYPE[X.dtype], N, n_in, _ptr(sx), _ptr(dev_status),
+                                 _stream(stream)), "awq_channel_stats")
+    return sx
+
+
+def awq_search_workspace_bytes(dtype: torch.dtype, out: int, n_in: int, N: int, group: int,
+                               grid: int) -> int:
+    return int(lib.awq_search_workspace_bytes(DTYPE[dtype], out, n_in, N, group, grid))
+
+
+def awq_search(W: torch.Tensor, X: torch.Tensor, bits: int = 4, group: Optional[int] = None,
+               sym: bool = True, grid: int = 20, sx: Optional[torch.Tensor] = None,
+               workspace: Optional[torch.Tensor] = None, out_tensors=None, stream=None,
+               dev_status: Optional[torch.Tensor] = None, opts: Optional[SearchOpts] = None,
+               check: bool = True) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Alpha-grid search; returns (err [grid+1] f64, best [1] i32, s_best [in] f32).
+
+    ``group=None`` means one group per row (group = in).  With ``check``
+    the call synchronises and raises on a device-reported error.
+    """
+    _need(W, "W", 2)
+    _need(X, "X", 2)
+    if W.dtype != X.dtype or W.shape[1] != X.shape[1]:
+        raise ValueError("W and X must share dtype and the input dimension")
+    out, n_in = W.shape
+    N = X.shape[0]
+    g = n_in if group is None else int(group)
+    if workspace is None:
+        need = awq_search_workspace_bytes(W.dtype, out, n_in, N, g, grid)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=W.device)
+    if out_tensors is None:
+        err = torch.empty(grid + 1, dtype=torch.float64, device=W.device)
+        best = torch.empty(1, dtype=torch.int32, device=W.device)
+        s_best = torch.empty(n_in, dtype=torch.float32, device=W.device)
+    else:
+        err, best, s_best = out_tensors
+    st = dev_status if dev_status is not None else new_status(W.device)
+    args = (_ptr(W), _ptr(X), DTYPE[W.dtype], out, n_in, N, _ptr(sx), bits, g, 1 if sym else 0,
+            grid, _ptr(workspace), workspace.numel(), _ptr(err), _ptr(best), _ptr(s_best), _ptr(st),
+            _stream(stream))
+    if opts is None:
+        code = lib.awq_search(*args)
+    else:
+        code = lib.awq_search_ex(*args, ctypes.byref(opts))
+    _check(code, "awq_search")
+    if check:
+        check_status(st, "awq_search")
+    return err, best, s_best
+
+
+def awq_quantize_pack(W: torch.Tensor, s: torch.Tensor, bits: int = 4, group: Optional[int] = None,
+                      sym: bool = True, out_tensors=None, stream=None,
+                      dev_status: Optional[torch.Tensor] = None, check: bool = True):
+    """Quantize W * s per group and pack; returns (qweight, scales, zeros)."""
+    _need(W, "W", 2)
+    _need(s, "s", 1)
+    if s.dtype != torch.float32 or s.numel() != W.shape[1]:
+        raise ValueError("s must be float32 with one entry per input column")
+    out, n_in = W.shape
+    g = n_in if group is None else int(group)
+    if out_tensors is None:
+        nwords = (n_in * bits + 31) // 32
+        qweight = torch.empty((out, nwords), dtype=torch.int32, device=W.device)
+        scales = torch.empty((out, max(n_in // g, 1)), dtype=torch.float32, device=W.device)
+        zeros = torch.empty((out, max(n_in // g, 1)), dtype=torch.uint8, device=W.device)
+    else:
+        qweight, scales, zeros = out_tensors
+    st = dev_status if dev_status is not None else new_status(W.device)
+    _check(lib.awq_quantize_pack(_ptr(W), DTYPE[W.dtype], out, n_in, _ptr(s), bits, g,
+                                 1 if sym else 0, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(st),
+                                 _stream(stream)), "awq_quantize_pack")
+    if check:
+        check_status(st, "awq_quantize_pack")
+    return qweight, scales, zeros

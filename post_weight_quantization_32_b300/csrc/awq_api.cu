@@ -1,0 +1,174 @@
+// The C ABI of libawq (declared in include/awq.h): argument checks,
+// workspace layout, and the order of launches on the caller's stream.
+#include "../../include/awq.h"
+#include "awq_internal.h"
+
+namespace awq {
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = v > 0 ? v : 1;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+constexpr int kMaxGrid = 4096;
+
+// Byte offsets of the workspace regions of awq_search (each 256-aligned).
+struct WsLayout {
+  size_t ctl, pow2, unscale, sx64, s64, minmax, s32, inv_s32, xf16, partials, total;
+};
+
+WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int grid) {
+  WsLayout w{};
+  const int64_t n_alpha = grid + 1;
+  const int64_t n_tiles = ((out + 127) / 128) * ((N + 255) / 256);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  w.ctl = take(8 * sizeof(uint32_t));  // max|W| and max|X| bits; 4 words of wait diagnostics
+  w.pow2 = take((size_t)n_alpha * 4);
+  w.unscale = take((size_t)n_alpha * 8);
+  w.sx64 = take((size_t)in * 8);
+  w.s64 = take((size_t)n_alpha * in * 8);
+  w.minmax = take((size_t)n_alpha * prep_chunks(in) * 16);
+  w.s32 = take((size_t)n_alpha * in * 4);
+  w.inv_s32 = take((size_t)n_alpha * in * 4);
+  w.xf16 = take(dt == kDtF16 ? 0 : (size_t)N * in * 2);
+  w.partials = take((size_t)n_alpha * n_tiles * 8);
+  w.total = o;
+  return w;
+}
+
+bool dtype_ok(int dt) { return dt == kDtF32 || dt == kDtF16 || dt == kDtBF16; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA; }
+
+}  // namespace
+}  // namespace awq
+
+using namespace awq;
+
+extern "C" {
+
+const char* awq_status_string(int status) {
+  switch (status) {
+    case AWQ_OK: return "ok";
+    case AWQ_ERR_INVALID_ARG: return "invalid argument";
+    case AWQ_ERR_UNSUPPORTED: return "unsupported by this build";
+    case AWQ_ERR_NONFINITE: return "non-finite values: no alpha has a finite error";
+    case AWQ_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case AWQ_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+int awq_channel_stats(const void* X, int dtype, int64_t N, int64_t in, double* sx,
+                      int32_t* dev_status, awq_stream_t stream) {
+  (void)dev_status;  // no device-side errors in this kernel
+  if (!X || !sx || !dtype_ok(dtype) || N < 1 || in < 1) return AWQ_ERR_INVALID_ARG;
+  return cuda_status(launch_channel_stats(X, dtype, N, in, sx, (cudaStream_t)stream));
+}
+
+size_t awq_search_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N, int group,
+                                  int grid) {
+  if (!dtype_ok(dtype) || out < 1 || in < 1 || N < 1 || grid < 1 || grid > kMaxGrid ||
+      group < 1 || in % group != 0)
+    return 0;
+  return ws_layout(dtype, out, in, N, grid).total;
+}
+
+int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
+                  const double* sx, int bits, int group, int sym, int grid, void* workspace,
+                  size_t workspace_bytes, double* err, int32_t* best, float* s_best,
+                  int32_t* dev_status, awq_stream_t stream, const awq_search_opts* opts) {
+  if (!W || !X || !workspace || !err || !best || !s_best || !dtype_ok(dtype))
+    return AWQ_ERR_INVALID_ARG;
+  if (out < 1 || in < 1 || N < 1 || bits < 2 || bits > 8 || grid < 1 || grid > kMaxGrid ||
+      group < 1 || in % group != 0)
+    return AWQ_ERR_INVALID_ARG;
+  const WsLayout ws = ws_layout(dtype, out, in, N, grid);
+  if (workspace_bytes < ws.total || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return AWQ_ERR_INVALID_ARG;
+  if (!search_supported(dtype, out, in, N, bits, group, grid)) return AWQ_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(W) & 15) != 0 || (reinterpret_cast<uintptr_t>(X) & 15) != 0)
+    return AWQ_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  const int n_alpha = grid + 1;
+
+  // max|W| and max|X| set the exact power-of-two scalings of the fp16 GEMM operands
+  uint32_t* absmax = reinterpret_cast<uint32_t*>(wsb + ws.ctl);
+  uint32_t* diag = (opts && opts->diag) ? opts->diag : absmax + 4;
+  int32_t* pow2_s = reinterpret_cast<int32_t*>(wsb + ws.pow2);
+  cudaError_t e = cudaMemsetAsync(absmax, 0, 8 * sizeof(uint32_t), s);
+  if (e == cudaSuccess && opts && opts->diag)
+    e = cudaMemsetAsync(opts->diag, 0, 4 * sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(pow2_s, 0xFF, (size_t)n_alpha * 4, s);
+  if (e == cudaSuccess) e = launch_absmax(W, dtype, out * in, absmax, s);
+  const void* xh = X;
+  if (e == cudaSuccess && dtype != kDtF16) {
+    e = launch_absmax(X, dtype, N * in, absmax + 1, s);
+    if (e == cudaSuccess) e = launch_to_f16(X, dtype, N * in, absmax + 1, wsb + ws.xf16, s);
+    xh = wsb + ws.xf16;
+  }
+  if (e != cudaSuccess) return AWQ_ERR_CUDA;
+  const double* sxp = sx;
+  if (!sxp) {
+    e = launch_channel_stats(X, dtype, N, in, reinterpret_cast<double*>(wsb + ws.sx64), s);
+    if (e != cudaSuccess) return AWQ_ERR_CUDA;
+    sxp = reinterpret_cast<const double*>(wsb + ws.sx64);
+  }
+  float* s32 = reinterpret_cast<float*>(wsb + ws.s32);
+  float* inv_s32 = reinterpret_cast<float*>(wsb + ws.inv_s32);
+  double* unscale = reinterpret_cast<double*>(wsb + ws.unscale);
+  e = launch_alpha_prep(sxp, in, grid, absmax, dtype != kDtF16 ? 1 : 0,
+                        reinterpret_cast<double*>(wsb + ws.s64),
+                        reinterpret_cast<double*>(wsb + ws.minmax), s32, inv_s32, unscale, pow2_s,
+                        s);
+  if (e != cudaSuccess) return AWQ_ERR_CUDA;
+
+  const SearchPlan pl = plan_search(dtype, out, in, N, n_alpha, group, device_sm_count());
+  double* partials = reinterpret_cast<double*>(wsb + ws.partials);
+  e = launch_search(W, xh, dtype, out, in, N, bits, group, sym ? 1 : 0, n_alpha, s32, inv_s32,
+                    pow2_s, partials, pl, opts ? opts->wait_limit_ns : 0,
+                    opts ? opts->test_timeout : 0, dev_status, diag, s,
+                    opts ? (cudaEvent_t)opts->ev_search_start : nullptr,
+                    opts ? (cudaEvent_t)opts->ev_search_stop : nullptr);
+  if (e == cudaErrorInvalidValue) return AWQ_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return AWQ_ERR_CUDA;
+  e = launch_reduce_argmin(partials, unscale, n_alpha, pl.n_tiles, (double)N * (double)out, s32,
+                           in, err, best, s_best, dev_status, s);
+  return cuda_status(e);
+}
+
+int awq_search(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
+               const double* sx, int bits, int group, int sym, int grid, void* workspace,
+               size_t workspace_bytes, double* err, int32_t* best, float* s_best,
+               int32_t* dev_status, awq_stream_t stream) {
+  return awq_search_ex(W, X, dtype, out, in, N, sx, bits, group, sym, grid, workspace,
+                       workspace_bytes, err, best, s_best, dev_status, stream, nullptr);
+}
+
+int awq_quantize_pack(const void* W, int dtype, int64_t out, int64_t in, const float* s, int bits,
+                      int group, int sym, uint32_t* qweight, float* scales, uint8_t* zeros,
+                      int32_t* dev_status, awq_stream_t stream) {
+  if (!W || !s || !qweight || !scales || !zeros || !dtype_ok(dtype)) return AWQ_ERR_INVALID_ARG;
+  if (out < 1 || in < 1 || bits < 2 || bits > 8 || group < 1 || in % group != 0)
+    return AWQ_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_pack(W, dtype, out, in, s, bits, group, sym ? 1 : 0, qweight,
+                                          scales, zeros, dev_status, (cudaStream_t)stream));
+}
+
+}  // extern "C"

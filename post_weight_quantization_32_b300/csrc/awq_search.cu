@@ -1,0 +1,686 @@
+// The fused alpha-grid search: for every alpha of the grid it forms
+//     dW_alpha = Q(W * s_alpha) / s_alpha - W
+// tile by tile and scores sum((X dW_alpha^T)^2) on the tensor cores, never
+// materialising X W^T or the dequantized weights.  By linearity this is the
+// pages' ((X @ Wq.T - X @ W.T) ** 2).sum() ("AWQ (activation-aware weight
+// quantization)", "Source code"; "AWQ vs GPTQ ...", awq_scales).
+//
+// Work unit = (128-row tile of W, a group of up to 8 alphas, a token tile of
+// T <= 256 tokens).  One persistent CTA per SM walks a static list of units.
+// Warp roles inside a CTA (384 threads):
+//   warp 0      TMA loads of W blocks (128 rows x 64 columns) into a ring
+//   warp 1      TMA loads of X blocks (T tokens x 64 columns, fp16) into a ring
+//   warp 2      tensor memory owner and the single tcgen05.mma issuer
+//   warp 3      idle
+//   warps 4-11  two warpgroups of producers: thread = one W row.  Each reads
+//               its row's weights, scales by s_alpha, finds the group
+//               max/min, rounds to the grid, and writes dW (fp16) straight
+//               into tensor memory, where the MMA reads it as operand A;
+//               after the last K block they read the fp32 accumulators
+//               (128 rows x T tokens per alpha), square and sum them.
+//               Warpgroup 0 takes the even K groups of a unit, warpgroup 1
+//               the odd ones.
+// Tensor memory (512 columns): columns [0, 256) hold a_per accumulators of
+// T columns; columns [256, 512) are eight 32-column slots of dW (64 fp16
+// values per row each), four per producer warpgroup.  X is the MMA's B
+// operand from shared memory in the 128-byte-swizzle K-major layout that
+// TMA writes.  The W ring is likewise split into one bank per warpgroup.
+// With one bank per consumer, every barrier's phases are consumed in order
+// by a single party, so a parity wait can never be a full phase ahead.
+//
+// The GEMM runs on fp16 operands (11-bit significands) with fp32
+// accumulation.  X arrives as fp16 scaled by a power of two, and dW is
+// scaled by a per-alpha power of two folded into the 1/s table, both chosen
+// from max|X| and max|W| so every value lies in fp16's normal range; the
+// float64 reduction divides the exact powers of two out again.
+//
+// The producer rounds t * (1/scale) with one fused multiply-add against
+// 1.5 * 2^23 (round to nearest even); next to an exact half-integer this can
+// differ from rounding the correctly rounded quotient, which changes the
+// error far less than the fp16 rounding of dW.  Where every scale of an alpha
+// is a power of two (alpha = 0, flat salience) t / scale falls on exact
+// half-integers of the 16-bit weight lattice often, so those alphas use the
+// correctly rounded quotient.  The group step itself is the exact float32
+// max(m / L, 1e-8) (asymmetric: (hi - lo) / maxq and the zero point
+// round(-lo / scale)), as in the final quantizer.
+//
+// Every wait on an mbarrier is bounded (wall clock).  A wait that runs out
+// raises a shared abort flag; all roles then stop issuing work, drain what
+// they have in flight, free tensor memory and return, and the host sees
+// AWQ_ERR_TIMEOUT in the status word.
+#include <algorithm>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "awq_device.cuh"
+#include "awq_internal.h"
+
+namespace awq {
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kRows = 128;       // MMA M: weight rows per tile
+constexpr int kKB = 64;          // K columns per block: one 128-byte fp16 swizzle row
+constexpr int kBankSlots = 4;    // dW slots in tensor memory per producer warpgroup
+constexpr int kSlots = 2 * kBankSlots;
+constexpr int kMaxSW = 8, kMaxSX = 8, kMaxAPer = 8;
+constexpr uint32_t kSlotCol0 = 256;
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: fma(x, r, M) - M = rint(x * r)
+constexpr uint32_t kCtrlBytes = 1024;
+
+struct SearchArgs {
+  const float* s32;       // [n_alpha][in]
+  const float* inv_s32;   // [n_alpha][in], times 2^e_k
+  const int32_t* pow2_s;  // [n_alpha]: nonzero when every scale of that alpha is a power of two
+  double* partials;       // [n_alpha][n_tiles]
+  int32_t* status;
+  uint32_t* diag;         // 4 words: where a wait gave up
+  int out, in, N;
+  int n_alpha, a_per, n_ag, n_rt, n_tt, T, n_kb, n_units, n_tiles;
+  int sw, sx;
+  float Lf, maxqf;
+  uint64_t wait_limit_ns;
+  int test_timeout;
+};
+
+struct Ctrl {
+  uint64_t w_full[kMaxSW], w_empty[kMaxSW];
+  uint64_t x_full[kMaxSX], x_empty[kMaxSX];
+  uint64_t d_full[kSlots], d_empty[kSlots];
+  uint64_t acc_full, acc_empty, epi_full, never, drain;
+  uint32_t tmem_base;
+  int abort;
+  float epi[2][kMaxAPer][8];
+};
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
+
+// Eight weights (columns 8*cc .. 8*cc+7 of the 64-column block) of `row`
+// from a TMA stage in the 128-byte swizzle layout: the 16-byte chunk j of a
+// 128-byte row r sits at chunk j ^ (r & 7).
+template <typename WT>
+__device__ __forceinline__ void load_w8(const uint8_t* stage, int row, int cc, float (&v)[8]);
+
+template <>
+__device__ __forceinline__ void load_w8<__nv_bfloat16>(const uint8_t* stage, int row, int cc,
+                                                       float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(stage + row * 128 + ((cc ^ (row & 7)) << 4));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+template <>
+__device__ __forceinline__ void load_w8<__half>(const uint8_t* stage, int row, int cc,
+                                                float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(stage + row * 128 + ((cc ^ (row & 7)) << 4));
+  const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+template <>
+__device__ __forceinline__ void load_w8<float>(const uint8_t* stage, int row, int cc,
+                                               float (&v)[8]) {
+  // fp32 stages hold two 32-column boxes of 128 rows x 128 bytes
+  const uint8_t* box = stage + (cc >> 2) * (kRows * 128);
+  const int j0 = (cc & 3) * 2;
+  const float4 a = *reinterpret_cast<const float4*>(box + row * 128 + ((j0 ^ (row & 7)) << 4));
+  const float4 b =
+      *reinterpret_cast<const float4*>(box + row * 128 + (((j0 + 1) ^ (row & 7)) << 4));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void load_f8(const float* p, bool valid, float (&v)[8]) {
+  if (valid) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// dW for the 64 columns of K block kbi of a producer job, as 32 fp16 pairs.
+// q = round(t / scale): the fast form rounds t * (1/scale) with one fused
+// multiply-add against 1.5 * 2^23; the EXACT form first forms the correctly
+// rounded quotient q1 = q0 + (t - q0 * scale) * (1/scale), q0 = t * (1/scale)
+// (one residual correction of the reciprocal quotient), then rounds it.
+template <bool SYM, bool EXACT, int G, int JC>
+__device__ __forceinline__ void make_dw(const float (&t)[JC], int kbi, const float* ip, int col0,
+                                        int in, const float (&scl)[JC / G],
+                                        const float (&rcp)[JC / G], const float (&alo)[JC / G],
+                                        const float (&ahi)[JC / G], uint32_t (&pk)[32]) {
+  const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
+  const float2 nm2 = make_float2(-kRoundMagic, -kRoundMagic);
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) {
+    const int cgi = kbi * 8 + cc;
+    const int g = (cgi * 8) / G;
+    float i8[8];
+    load_f8(ip + cgi * 8, col0 + cgi * 8 < in, i8);
+    const float2 rc2 = make_float2(rcp[g], rcp[g]);
+    const float2 sc2 = make_float2(scl[g], scl[g]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float t0 = t[cgi * 8 + 2 * e], t1 = t[cgi * 8 + 2 * e + 1];
+      const float2 tv = make_float2(t0, t1);
+      float2 av;
+      if (EXACT) {
+        const float2 q0 = __fmul2_rn(tv, rc2);
+        const float2 r = __ffma2_rn(make_float2(-q0.x, -q0.y), sc2, tv);
+        av = __fadd2_rn(__ffma2_rn(r, rc2, q0), mg2);
+      } else {
+        av = __ffma2_rn(tv, rc2, mg2);
+      }
+      if (!SYM) {
+        av.x = fminf(fmaxf(av.x, alo[g]), ahi[g]);
+        av.y = fminf(fmaxf(av.y, alo[g]), ahi[g]);
+      }
+      const float2 qv = __fadd2_rn(av, nm2);
+      const float2 ev = __ffma2_rn(qv, sc2, make_float2(-t0, -t1));
+      const float2 dv = __fmul2_rn(ev, make_float2(i8[2 * e], i8[2 * e + 1]));
+      pk[cc * 4 + e] = pack_f16x2(dv.x, dv.y);
+    }
+  }
+}
+
+template <typename WT, int G, bool SYM>
+__global__ void __launch_bounds__(kThreads, 1)
+    awq_search_kernel(const __grid_constant__ CUtensorMap tmW,
+                      const __grid_constant__ CUtensorMap tmX, const SearchArgs p) {
+  constexpr int KBJ = (G == 128) ? 2 : 1;  // K blocks per producer job
+  constexpr int JC = KBJ * kKB;            // columns per producer job
+  constexpr int NG = JC / G;               // groups per job
+  constexpr uint32_t W_STAGE = kRows * kKB * sizeof(WT);
+  constexpr uint32_t FULL = 0xffffffffu;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  Ctrl& c = *reinterpret_cast<Ctrl*>(gbase);
+  const uint32_t w_ring = base + kCtrlBytes;
+  const uint8_t* w_ring_ptr = gbase + kCtrlBytes;
+  const uint32_t X_STAGE = (uint32_t)p.T * 128u;
+  const uint32_t x_ring = w_ring + (uint32_t)p.sw * W_STAGE;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.sw; ++i) {
+      mbar_init(smem_addr(&c.w_full[i]), 1);
+      mbar_init(smem_addr(&c.w_empty[i]), 4);
+    }
+    for (int i = 0; i < p.sx; ++i) {
+      mbar_init(smem_addr(&c.x_full[i]), 1);
+      mbar_init(smem_addr(&c.x_empty[i]), 1);
+    }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_addr(&c.d_full[i]), 4);
+      mbar_init(smem_addr(&c.d_empty[i]), 1);
+    }
+    mbar_init(smem_addr(&c.acc_full), 1);
+    mbar_init(smem_addr(&c.acc_empty), 8);
+    mbar_init(smem_addr(&c.epi_full), 8);
+    mbar_init(smem_addr(&c.never), 1);
+    mbar_init(smem_addr(&c.drain), 1);
+    c.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_addr(&c.tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmW);
+    tma_prefetch_map(&tmX);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c.tmem_base;
+  volatile int* abort = &c.abort;
+  const uint64_t lim = p.wait_limit_ns;
+  const int units_per_rt = p.n_ag * p.n_tt;
+  const int n_kg = p.n_kb / KBJ;
+  const uint32_t hw = (uint32_t)p.sw / 2;  // W stages per warpgroup bank
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- W loader
+    if (lane == 0) {
+      uint32_t wcnt[2] = {0, 0};  // W blocks loaded into each warpgroup's bank
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        const int rt = u / units_per_rt;
+        for (int kb = 0; kb < p.n_kb; ++kb) {
+          const int b = (kb / KBJ) & 1;
+          const uint32_t m = wcnt[b];
+          const uint32_t st = b * hw + m % hw, ph = (m / hw) & 1;
+          if (!mbar_wait(smem_addr(&c.w_empty[st]), ph ^ 1, abort, lim, p.diag, 1, m | (b << 30))) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_addr(&c.w_full[st]);
+          mbar_arrive_expect_tx(bar, W_STAGE);
+          const uint32_t dst = w_ring + st * W_STAGE;
+          if (sizeof(WT) == 4) {
+            tma_load_2d(dst, &tmW, bar, kb * kKB, rt * kRows);
+            tma_load_2d(dst + W_STAGE / 2, &tmW, bar, kb * kKB + 32, rt * kRows);
+          } else {
+            tma_load_2d(dst, &tmW, bar, kb * kKB, rt * kRows);
+          }
+          ++wcnt[b];
+        }
+      }
+      int never_set = 0;  // drain: wait for the loads still in flight
+      for (int b = 0; b < 2; ++b)
+        for (uint32_t m = wcnt[b] > hw ? wcnt[b] - hw : 0; m < wcnt[b]; ++m)
+          mbar_wait(smem_addr(&c.w_full[b * hw + m % hw]), (m / hw) & 1, &never_set, lim);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- X loader
+    if (lane == 0) {
+      uint32_t seq = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        const int tt = (u % units_per_rt) % p.n_tt;
+        for (int kb = 0; kb < p.n_kb; ++kb) {
+          const uint32_t st = seq % p.sx, ph = (seq / p.sx) & 1;
+          if (!mbar_wait(smem_addr(&c.x_empty[st]), ph ^ 1, abort, lim, p.diag, 3, seq)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_addr(&c.x_full[st]);
+          mbar_arrive_expect_tx(bar, X_STAGE);
+          tma_load_2d(x_ring + st * X_STAGE, &tmX, bar, kb * kKB, tt * p.T);
+          ++seq;
+        }
+      }
+      int never_set = 0;
+      for (uint32_t i = seq > (uint32_t)p.sx ? seq - p.sx : 0; i < seq; ++i)
+        mbar_wait(smem_addr(&c.x_full[i % p.sx]), (i / p.sx) & 1, &never_set, lim);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(kRows, (uint32_t)p.T);
+      uint32_t xseq = 0, useq = 0;
+      uint32_t dcnt[2] = {0, 0};  // dW slots consumed from each warpgroup's bank
+      bool ok = true;
+      if (p.test_timeout) ok = mbar_wait(smem_addr(&c.never), 0, abort, lim, p.diag, 5, 0);
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        const int ag = (u % units_per_rt) / p.n_tt;
+        const int na = min(p.a_per, p.n_alpha - ag * p.a_per);
+        if (useq > 0) {
+          if (!mbar_wait(smem_addr(&c.acc_empty), (useq - 1) & 1, abort, lim, p.diag, 6, useq)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        for (int kg = 0; ok && kg < n_kg; ++kg) {
+          const int b = kg & 1;
+          for (int a = 0; ok && a < na; ++a) {
+            for (int kbi = 0; kbi < KBJ; ++kbi) {
+              const uint32_t xq = xseq + kg * KBJ + kbi;
+              const uint32_t xs = xq % p.sx;
+              if (a == 0 &&
+                  !mbar_wait(smem_addr(&c.x_full[xs]), (xq / p.sx) & 1, abort, lim, p.diag, 7, xq)) {
+                ok = false;
+                break;
+              }
+              const uint32_t n = dcnt[b];
+              const uint32_t ds = b * kBankSlots + n % kBankSlots;
+              if (!mbar_wait(smem_addr(&c.d_full[ds]), (n / kBankSlots) & 1, abort, lim, p.diag, 8,
+                             n | (b << 30))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t d_t = tmem + (uint32_t)(a * p.T);
+              const uint32_t a_t = tmem + kSlotCol0 + ds * 32u;
+              const uint64_t bdesc = smem_desc_sw128(x_ring + xs * X_STAGE);
+#pragma unroll
+              for (int k = 0; k < kKB / 16; ++k)
+                umma_ts(d_t, a_t + 8u * k, bdesc + (uint64_t)(2 * k), idesc,
+                        (kg | kbi | k) != 0 ? 1u : 0u);
+              umma_commit(smem_addr(&c.d_empty[ds]));
+              if (a == na - 1) umma_commit(smem_addr(&c.x_empty[xs]));
+              ++dcnt[b];
+            }
+          }
+        }
+        if (!ok) break;
+        xseq += p.n_kb;
+        umma_commit(smem_addr(&c.acc_full));
+        ++useq;
+      }
+      umma_commit(smem_addr(&c.drain));
+      int never_set = 0;
+      mbar_wait(smem_addr(&c.drain), 0, &never_set, lim);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------- producers + epilogue
+    const int wg = (warp - 4) >> 2;
+    const int q = warp & 3;  // tensor memory lanes 32q .. 32q+31
+    const int row = q * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    uint32_t wm = 0, dn = 0, useq = 0;  // this warpgroup's W-block and dW-slot counters
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      const int rem = u % units_per_rt;
+      const int rt = u / units_per_rt, ag = rem / p.n_tt, tt = rem % p.n_tt;
+      const int na = min(p.a_per, p.n_alpha - ag * p.a_per);
+      for (int kg = 0; ok && kg < n_kg; ++kg) {
+        if ((kg & 1) != wg) continue;
+        for (int kbi = 0; kbi < KBJ; ++kbi) {
+          const uint32_t m = wm + kbi;
+          ok = mbar_wait(smem_addr(&c.w_full[wg * hw + m % hw]), (m / hw) & 1, abort, lim, p.diag,
+                         10, m | (wg << 30));
+          ok = __all_sync(FULL, ok);
+          if (!ok) break;
+        }
+        if (!ok) break;
+        const int col0 = kg * JC;
+        for (int a = 0; ok && a < na; ++a) {
+          const int k = ag * p.a_per + a;
+          const float* sp = p.s32 + (size_t)k * p.in + col0;
+          const float* ip = p.inv_s32 + (size_t)k * p.in + col0;
+          const bool exact = p.pow2_s[k] != 0;
+          // pass 1: t = fl32(w * s)
+          float t[JC];
+#pragma unroll
+          for (int cgi = 0; cgi < JC / 8; ++cgi) {
+            const int kbi = cgi >> 3, cc = cgi & 7;
+            const uint32_t st = wg * hw + (wm + kbi) % hw;
+            float w8[8], s8[8];
+            load_w8<WT>(w_ring_ptr + st * W_STAGE, row, cc, w8);
+            load_f8(sp + cgi * 8, col0 + cgi * 8 < p.in, s8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t[cgi * 8 + e] = __fmul_rn(w8[e], s8[e]);
+          }
+          if (a == na - 1) {
+            // the weights are in registers now: hand the W stages back
+            __syncwarp();
+            if (lane == 0)
+              for (int kbi = 0; kbi < KBJ; ++kbi)
+                mbar_arrive(smem_addr(&c.w_empty[wg * hw + (wm + kbi) % hw]));
+          }
+          // group steps (and zero points)
+          float scl[NG], rcp[NG], alo[NG], ahi[NG];
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            if (SYM) {
+              float m = 0.0f;
+#pragma unroll
+              for (int e = 0; e < G; ++e) m = fmaxf(m, fabsf(t[g * G + e]));
+              scl[g] = fmaxf(__fdiv_rn(m, p.Lf), 1e-8f);
+              alo[g] = ahi[g] = 0.0f;
+            } else {
+              float lo = 0.0f, hi = 0.0f;
+#pragma unroll
+              for (int e = 0; e < G; ++e) {
+                lo = fminf(lo, t[g * G + e]);
+                hi = fmaxf(hi, t[g * G + e]);
+              }
+              scl[g] = fmaxf(__fdiv_rn(__fsub_rn(hi, lo), p.maxqf), 1e-8f);
+              const float z = rintf(__fdiv_rn(-lo, scl[g]));
+              alo[g] = kRoundMagic - z;
+              ahi[g] = kRoundMagic + p.maxqf - z;
+            }
+            rcp[g] = __frcp_rn(scl[g]);
+          }
+          // pass 2: dW = (q * scale - t) / s (times 2^e_k), fp16 pairs into a tensor memory slot
+#pragma unroll
+          for (int kbi = 0; kbi < KBJ; ++kbi) {
+            const uint32_t ds = wg * kBankSlots + dn % kBankSlots;
+            ok = mbar_wait(smem_addr(&c.d_empty[ds]), ((dn / kBankSlots) & 1) ^ 1, abort, lim,
+                           p.diag, 11, dn | (wg << 30));
+            ok = __all_sync(FULL, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t pk[32];
+            if (exact)
+              make_dw<SYM, true, G, JC>(t, kbi, ip, col0, p.in, scl, rcp, alo, ahi, pk);
+            else
+              make_dw<SYM, false, G, JC>(t, kbi, ip, col0, p.in, scl, rcp, alo, ahi, pk);
+            tmem_st32(tmem + lane_addr + kSlotCol0 + ds * 32u, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&c.d_full[ds]));
+            ++dn;
+          }
+        }
+        wm += KBJ;
+      }
+      if (!ok) break;
+      // epilogue: sum of squares of this unit's accumulators
+      ok = mbar_wait(smem_addr(&c.acc_full), useq & 1, abort, lim, p.diag, 12, useq);
+      ok = __all_sync(FULL, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int half = p.T >> 1;
+      for (int a = 0; a < na; ++a) {
+        float acc = 0.0f;
+        const uint32_t cb = tmem + lane_addr + (uint32_t)(a * p.T + wg * half);
+        for (int cc = 0; cc < half; cc += 16) {
+          uint32_t v[16];
+          tmem_ld16(cb + (uint32_t)cc, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float f = __uint_as_float(v[i]);
+            acc = fmaf(f, f, acc);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(FULL, acc, o);
+        if (lane == 0) c.epi[useq & 1][a][warp - 4] = acc;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&c.acc_empty));
+        mbar_arrive(smem_addr(&c.epi_full));
+      }
+      if (warp == 4) {
+        bool ok2 = true;
+        if (lane == 0) ok2 = mbar_wait(smem_addr(&c.epi_full), useq & 1, abort, lim, p.diag, 13, useq);
+        __syncwarp();
+        ok2 = __shfl_sync(FULL, ok2, 0);
+        if (!ok2) {
+          ok = false;
+          break;
+        }
+        if (lane < na) {
+          double s = 0.0;
+          for (int w = 0; w < 8; ++w) s += (double)c.epi[useq & 1][lane][w];
+          p.partials[(size_t)(ag * p.a_per + lane) * p.n_tiles + rt * p.n_tt + tt] = s;
+        }
+      }
+      ++useq;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && c.abort) set_status(p.status, ST_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, CUtensorMapDataType t, const void* ptr, uint64_t cols, uint64_t rows,
+              uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, t, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const SearchArgs);
+
+template <typename WT>
+KernelFn pick_g(int group, int sym) {
+  switch (group) {
+    case 32: return sym ? &awq_search_kernel<WT, 32, true> : &awq_search_kernel<WT, 32, false>;
+    case 64: return sym ? &awq_search_kernel<WT, 64, true> : &awq_search_kernel<WT, 64, false>;
+    case 128: return sym ? &awq_search_kernel<WT, 128, true> : &awq_search_kernel<WT, 128, false>;
+    default: return nullptr;
+  }
+}
+
+int max_dyn_smem() {
+  int dev = 0, v = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  return v;
+}
+
+}  // namespace
+
+bool search_supported(int dt, int64_t out, int64_t in, int64_t N, int bits, int group, int grid) {
+  (void)dt; (void)bits; (void)grid;
+  if (group != 32 && group != 64 && group != 128) return false;
+  if (in % group != 0) return false;
+  if (out > (1 << 24) || N > (1 << 24) || in > (1 << 24)) return false;
+  return true;
+}
+
+SearchPlan plan_search(int dt, int64_t out, int64_t in, int64_t N, int n_alpha, int group,
+                       int sms) {
+  SearchPlan pl{};
+  pl.n_tt = (int)((N + 255) / 256);
+  const int64_t per = (N + pl.n_tt - 1) / pl.n_tt;
+  pl.T = (int)((per + 31) / 32 * 32);
+  pl.a_per = std::max(1, std::min({n_alpha, 256 / pl.T, kMaxAPer}));
+  pl.n_ag = (n_alpha + pl.a_per - 1) / pl.a_per;
+  pl.n_rt = (int)((out + kRows - 1) / kRows);
+  pl.n_kb = (int)((in + kKB - 1) / kKB);
+  pl.n_units = pl.n_rt * pl.n_ag * pl.n_tt;
+  pl.n_tiles = pl.n_rt * pl.n_tt;
+  const int kbj = group == 128 ? 2 : 1;
+  const size_t w_stage = (size_t)kRows * kKB * dtype_size(dt);
+  const size_t x_stage = (size_t)pl.T * 128;
+  const size_t budget = (size_t)max_dyn_smem() - kCtrlBytes - 1024;
+  // deepest W ring (two equal banks of whole jobs) that leaves at least three X stages
+  pl.sw = 0;
+  pl.sx = 0;
+  for (int sw = kMaxSW; sw >= 2 * kbj && pl.sw == 0; sw -= 2 * kbj) {
+    for (int sx = 4; sx >= 3; --sx) {
+      if (sw * w_stage + sx * x_stage <= budget) {
+        pl.sw = sw;
+        pl.sx = sx;
+        break;
+      }
+    }
+  }
+  pl.smem = kCtrlBytes + 1024 + pl.sw * w_stage + pl.sx * x_stage;
+  pl.grid = std::max(1, std::min(pl.n_units, sms));
+  return pl;
+}
+
+cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, int64_t in,
+                          int64_t N, int bits, int group, int sym, int n_alpha,
+                          const float* s32, const float* inv_s32, const int32_t* pow2_s,
+                          double* partials, const SearchPlan& pl, int64_t wait_limit_ns,
+                          int test_timeout, int32_t* dev_status, uint32_t* diag, cudaStream_t s,
+                          cudaEvent_t ev0, cudaEvent_t ev1) {
+  KernelFn fn = nullptr;
+  CUtensorMapDataType wt;
+  uint32_t wbox;
+  switch (dt) {
+    case kDtF32:
+      fn = pick_g<float>(group, sym);
+      wt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+      wbox = 32;
+      break;
+    case kDtF16:
+      fn = pick_g<__half>(group, sym);
+      wt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      wbox = 64;
+      break;
+    default:
+      fn = pick_g<__nv_bfloat16>(group, sym);
+      wt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      wbox = 64;
+      break;
+  }
+  if (!fn || pl.sw < 2 || pl.sx < 3) return cudaErrorInvalidValue;
+  CUtensorMap mw, mx;
+  if (!make_map(&mw, wt, W, (uint64_t)in, (uint64_t)out, (uint64_t)in * dtype_size(dt), wbox, kRows))
+    return cudaErrorInvalidValue;
+  if (!make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xf16, (uint64_t)in, (uint64_t)N,
+                (uint64_t)in * 2, kKB, (uint32_t)pl.T))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  if (e != cudaSuccess) return e;
+  SearchArgs a;
+  a.s32 = s32;
+  a.inv_s32 = inv_s32;
+  a.pow2_s = pow2_s;
+  a.partials = partials;
+  a.status = dev_status;
+  a.diag = diag;
+  a.out = (int)out;
+  a.in = (int)in;
+  a.N = (int)N;
+  a.n_alpha = n_alpha;
+  a.a_per = pl.a_per;
+  a.n_ag = pl.n_ag;
+  a.n_rt = pl.n_rt;
+  a.n_tt = pl.n_tt;
+  a.T = pl.T;
+  a.n_kb = pl.n_kb;
+  a.n_units = pl.n_units;
+  a.n_tiles = pl.n_tiles;
+  a.sw = pl.sw;
+  a.sx = pl.sx;
+  a.Lf = (float)((1 << (bits - 1)) - 1);
+  a.maxqf = (float)((1 << bits) - 1);
+  a.wait_limit_ns = (uint64_t)(wait_limit_ns > 0 ? wait_limit_ns : 2000000000LL);
+  a.test_timeout = test_timeout;
+  if (ev0) cudaEventRecord(ev0, s);
+  fn<<<pl.grid, kThreads, pl.smem, s>>>(mw, mx, a);
+  e = cudaGetLastError();
+  if (ev1) cudaEventRecord(ev1, s);
+  return e;
+}
+
+}  // namespace awq

@@ -1,0 +1,171 @@
+// Channel statistics s_X[j] = mean_n |X[n, j]| + 1e-8 ("AWQ (activation-aware
+// weight quantization)", "How it works" step 1), the max |.| reductions that
+// set the power-of-two operand scalings, and the fp16 copy of X that the
+// tensor-core error GEMM reads.
+//
+// All three are HBM-bound passes.  The statistic is accumulated in float64
+// in a fixed order; for 16-bit inputs every partial sum is exact, so the
+// result does not depend on that order at all.
+#include <algorithm>
+
+#include "awq_device.cuh"
+#include "awq_internal.h"
+
+namespace awq {
+
+namespace {
+
+constexpr int kStatCols = 64;    // columns per CTA (8 lanes x 8 columns)
+constexpr int kStatSlices = 32;  // row slices per CTA
+
+// Vector path: in % 8 == 0 and 16-byte aligned rows.  Thread (c, r) sums the
+// 8 columns c*8..c*8+7 of the CTA's 64 over rows r, r+32, r+64, ...
+template <typename T>
+__global__ void __launch_bounds__(256) stats_vec_kernel(const T* __restrict__ X, int64_t N,
+                                                        int64_t in, double* __restrict__ sx) {
+  __shared__ double red[kStatSlices][kStatCols + 1];
+  const int c = threadIdx.x % 8, r = threadIdx.x / 8;
+  const int64_t col0 = (int64_t)blockIdx.x * kStatCols + c * 8;
+  double acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.0;
+  if (col0 < in) {
+    for (int64_t n = r; n < N; n += kStatSlices) {
+      float v[8];
+      load8_f32<T>(X + n * in + col0, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += (double)fabsf(v[e]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[r][c * 8 + e] = acc[e];
+  __syncthreads();
+  if (threadIdx.x < kStatCols) {
+    const int64_t j = (int64_t)blockIdx.x * kStatCols + threadIdx.x;
+    if (j < in) {
+      double s = 0.0;
+      for (int k = 0; k < kStatSlices; ++k) s += red[k][threadIdx.x];
+      sx[j] = s / (double)N + 1e-8;
+    }
+  }
+}
+
+// Scalar path for any shape: thread (c, r) sums column c over rows r, r+4, ...
+template <typename T>
+__global__ void __launch_bounds__(256) stats_scalar_kernel(const T* __restrict__ X, int64_t N,
+                                                           int64_t in, double* __restrict__ sx) {
+  __shared__ double red[4][kStatCols];
+  const int c = threadIdx.x % kStatCols, r = threadIdx.x / kStatCols;
+  const int64_t j = (int64_t)blockIdx.x * kStatCols + c;
+  double acc = 0.0;
+  if (j < in)
+    for (int64_t n = r; n < N; n += 4) acc += (double)fabsf(Elt<T>::to_f32(X[n * in + j]));
+  red[r][c] = acc;
+  __syncthreads();
+  if (r == 0 && j < in)
+    sx[j] = (((red[0][c] + red[1][c]) + red[2][c]) + red[3][c]) / (double)N + 1e-8;
+}
+
+// max |x| over n values as the bit pattern of a non-negative float (the
+// integer order of such patterns is the float order), combined across CTAs
+// with atomicMax: order-independent, so deterministic.  NaN is ignored.
+template <typename T>
+__global__ void __launch_bounds__(256) absmax_kernel(const T* __restrict__ p, int64_t n, bool vec,
+                                                     uint32_t* __restrict__ out) {
+  float m = 0.0f;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (vec) {
+    for (int64_t i = i0; i < n / 8; i += stride) {
+      float v[8];
+      load8_f32<T>(p + i * 8, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[e]));
+    }
+  } else {
+    for (int64_t i = i0; i < n; i += stride) m = fmaxf(m, fabsf(Elt<T>::to_f32(p[i])));
+  }
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(m));
+}
+
+// dst = fp16(X * 2^m), m from max|X| (pow2_exponent_for): an exact
+// power-of-two scaling, then one rounding to fp16.
+template <typename T>
+__global__ void __launch_bounds__(256) to_f16_kernel(const T* __restrict__ X, int64_t n8,
+                                                     const uint32_t* __restrict__ xmax_bits,
+                                                     uint4* __restrict__ dst) {
+  const float sc = ldexpf(1.0f, pow2_exponent_for((double)__uint_as_float(*xmax_bits)));
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float v[8];
+    load8_f32<T>(X + i * 8, v);
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      __half2 h = __floats2half2_rn(v[2 * k] * sc, v[2 * k + 1] * sc);
+      w[k] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <typename T>
+cudaError_t stats_dispatch(const void* X, int64_t N, int64_t in, double* sx, cudaStream_t s) {
+  const bool vec = (in % 8 == 0) && ((reinterpret_cast<uintptr_t>(X) & 15) == 0);
+  const unsigned grid = (unsigned)((in + kStatCols - 1) / kStatCols);
+  if (vec)
+    stats_vec_kernel<T><<<grid, 256, 0, s>>>(static_cast<const T*>(X), N, in, sx);
+  else
+    stats_scalar_kernel<T><<<grid, 256, 0, s>>>(static_cast<const T*>(X), N, in, sx);
+  return cudaGetLastError();
+}
+
+unsigned grid_for(int64_t work) {
+  const int64_t want = (work + 255) / 256;
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  return (unsigned)std::max<int64_t>(1, std::min(want, cap));
+}
+
+}  // namespace
+
+cudaError_t launch_channel_stats(const void* X, int dt, int64_t N, int64_t in, double* sx,
+                                 cudaStream_t s) {
+  switch (dt) {
+    case kDtF32: return stats_dispatch<float>(X, N, in, sx, s);
+    case kDtF16: return stats_dispatch<__half>(X, N, in, sx, s);
+    default: return stats_dispatch<__nv_bfloat16>(X, N, in, sx, s);
+  }
+}
+
+cudaError_t launch_absmax(const void* p, int dt, int64_t n, uint32_t* out, cudaStream_t s) {
+  const bool vec = (n % 8 == 0) && ((reinterpret_cast<uintptr_t>(p) & 15) == 0);
+  const unsigned grid = grid_for(vec ? n / 8 : n);
+  switch (dt) {
+    case kDtF32:
+      absmax_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(p), n, vec, out);
+      break;
+    case kDtF16:
+      absmax_kernel<__half><<<grid, 256, 0, s>>>(static_cast<const __half*>(p), n, vec, out);
+      break;
+    default:
+      absmax_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(p), n,
+                                                        vec, out);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_f16(const void* X, int dt, int64_t n, const uint32_t* xmax_bits, void* dst,
+                          cudaStream_t s) {
+  const int64_t n8 = n / 8;
+  const unsigned grid = grid_for(n8);
+  uint4* d = static_cast<uint4*>(dst);
+  if (dt == kDtF32)
+    to_f16_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(X), n8, xmax_bits, d);
+  else
+    to_f16_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(X), n8,
+                                                      xmax_bits, d);
+  return cudaGetLastError();
+}
+
+}  // namespace awq

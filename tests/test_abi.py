@@ -1,0 +1,124 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import importlib.util
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "awq.h")
+LIB = os.path.join(ROOT, "post_weight_quantization_32_b300", "libawq.so")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(awq_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        path = os.path.join(ROOT, "post_weight_quantization_32_b300", "build.py")
+        spec = importlib.util.spec_from_file_location("awq_build", path)
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        mod.build()
+    return ctypes.CDLL(LIB)
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("awq_channel_stats", "awq_search", "awq_search_ex", "awq_search_workspace_bytes",
+              "awq_quantize_pack", "awq_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+
+
+def test_binding_names_match_abi(lib):
+    import post_weight_quantization_32_b300 as pkg
+    for n in ("awq_channel_stats", "awq_search", "awq_quantize_pack", "awq_search_workspace_bytes"):
+        assert callable(getattr(pkg, n))
+    for n in pkg.EXPORTS:
+        assert n in _declared()
+
+
+def test_status_strings(lib):
+    lib.awq_status_string.restype = ctypes.c_char_p
+    for code in range(6):
+        assert lib.awq_status_string(code)
+    assert b"unknown" in lib.awq_status_string(99)
+
+
+def _ws(lib, *a):
+    lib.awq_search_workspace_bytes.restype = ctypes.c_size_t
+    lib.awq_search_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                               ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+    return lib.awq_search_workspace_bytes(*a)
+
+
+def test_workspace_query(lib):
+    # fp16 notebook-shaped layer: no copy of X, tables for 21 alphas
+    n = _ws(lib, 1, 4096, 4096, 256, 128, 20)
+    assert n >= 21 * 4096 * (8 + 4 + 4) and n % 256 == 0
+    # bf16 and fp32 add the fp16 copy of X
+    assert _ws(lib, 2, 4096, 4096, 256, 128, 20) >= n + 256 * 4096 * 2
+    assert _ws(lib, 2, 4096, 4096, 256, 100, 20) == 0      # group does not divide in
+    assert _ws(lib, 2, 0, 4096, 256, 128, 20) == 0
+    assert _ws(lib, 7, 16, 16, 16, 16, 20) == 0
+    assert _ws(lib, 2, 16, 16, 16, 16, 5000) == 0
+
+
+def test_search_rejects_bad_arguments_on_host(lib):
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    lib.awq_search.restype = i32
+    lib.awq_search.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, i32, vp, sz, vp, vp,
+                               vp, vp, vp]
+    fake = 1 << 20  # never dereferenced: the checks return before any launch
+    ok = dict(W=fake, X=fake, dt=2, out=256, n_in=512, N=64, sx=None, bits=4, group=128, sym=1,
+              grid=20, ws=fake, wsb=1 << 30, err=fake, best=fake, s_best=fake, st=fake, stream=None)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return lib.awq_search(a["W"], a["X"], a["dt"], a["out"], a["n_in"], a["N"], a["sx"],
+                              a["bits"], a["group"], a["sym"], a["grid"], a["ws"], a["wsb"],
+                              a["err"], a["best"], a["s_best"], a["st"], a["stream"])
+
+    assert call(W=None) == 1
+    assert call(N=0) == 1
+    assert call(bits=1) == 1 and call(bits=9) == 1
+    assert call(grid=0) == 1
+    assert call(group=100) == 1          # does not divide in
+    assert call(wsb=16) == 1             # workspace too small
+    assert call(ws=fake + 8) == 1        # workspace not 256-byte aligned
+    assert call(group=512) == 2          # valid for the method, not handled by the search kernels
+    assert call(group=16) == 2
+    assert call(W=fake + 4) == 2         # TMA needs 16-byte aligned rows
+
+
+def test_pack_rejects_bad_arguments_on_host(lib):
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.awq_quantize_pack.restype = i32
+    lib.awq_quantize_pack.argtypes = [vp, i32, i64, i64, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+    f = 1 << 20
+    assert lib.awq_quantize_pack(None, 2, 4, 8, f, 4, 8, 1, f, f, f, f, None) == 1
+    assert lib.awq_quantize_pack(f, 2, 4, 8, f, 4, 3, 1, f, f, f, f, None) == 1
+    assert lib.awq_quantize_pack(f, 2, 4, 8, f, 1, 8, 1, f, f, f, f, None) == 1
+    assert lib.awq_quantize_pack(f, 5, 4, 8, f, 4, 8, 1, f, f, f, f, None) == 1
+
+
+def test_stats_rejects_bad_arguments_on_host(lib):
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.awq_channel_stats.restype = i32
+    lib.awq_channel_stats.argtypes = [vp, i32, i64, i64, vp, vp, vp]
+    f = 1 << 20
+    assert lib.awq_channel_stats(None, 2, 4, 8, f, None, None) == 1
+    assert lib.awq_channel_stats(f, 2, 0, 8, f, None, None) == 1
+    assert lib.awq_channel_stats(f, 9, 4, 8, f, None, None) == 1

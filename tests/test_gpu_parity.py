@@ -1,0 +1,256 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Acceptance (per alpha error, chosen alpha, final codes):
+  * per-alpha errors within 2e-3 relative (fp16 tensor-core operands,
+    fp32 accumulation, float64 sums);
+  * the same alpha unless the two grid errors are within 1e-3 relative;
+  * given the oracle's scale vector, codes, group scales and zero points
+    bit-exact;
+  * s_X equal to the oracle's float64 statistic (exactly for 16-bit X).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import awq_oracle as O
+from synthetic import make_random_layer
+
+pytestmark = pytest.mark.gpu
+
+ERR_RTOL = 2e-3
+TIE_RTOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def awq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import post_weight_quantization_32_b300 as m
+    return m
+
+
+def _np_w(W):
+    return W.float().numpy()
+
+
+def _np_x(X):
+    return X.double().numpy()
+
+
+def _dev(*ts):
+    return [t.cuda() for t in ts]
+
+
+def check_search(awq, W, X, bits, group, sym, grid, label=""):
+    Wd, Xd = _dev(W, X)
+    diag = torch.zeros(4, dtype=torch.int32, device="cuda")
+    opts = awq.SearchOpts()
+    opts.diag = diag.data_ptr()
+    st = awq.new_status()
+    err, best, s_best = awq.awq_search(Wd, Xd, bits=bits, group=group, sym=sym, grid=grid,
+                                       dev_status=st, opts=opts, check=False)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "%s status %d, wait diagnostics %s" % (label, int(st.item()),
+                                                                      diag.cpu().tolist())
+    res = O.awq_search(_np_w(W), _np_x(X), bits=bits, group=group, grid=grid, sym=sym)
+    e = err.cpu().numpy()
+    b = int(best.item())
+    rel = np.abs(e - res.errs) / np.maximum(res.errs, 1e-300)
+    assert rel.max() <= ERR_RTOL, "%s per-alpha rel err %g (alpha %d)" % (label, rel.max(), rel.argmax())
+    if b != res.best:
+        assert abs(res.errs[b] - res.errs[res.best]) <= TIE_RTOL * res.errs[res.best], (label, b, res.best)
+    sb = s_best.cpu().numpy()
+    ref = res.s32[b]
+    ulps = np.abs(sb.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
+    assert ulps.max() <= 1 and (ulps > 0).sum() <= max(2, sb.size // 1000), label
+    return e, b, res
+
+
+def check_pack(awq, W, s32, bits, group, sym, rows=None):
+    Wd = W.cuda()
+    sd = torch.from_numpy(np.ascontiguousarray(s32, dtype=np.float32)).cuda()
+    qw, sc, z = awq.awq_quantize_pack(Wd, sd, bits=bits, group=group, sym=sym)
+    Wn = _np_w(W)
+    if rows is not None:
+        Wn = Wn[rows]
+        qw, sc, z = qw[rows], sc[rows], z[rows]
+    qo, so, zo = O.quantize_pack(Wn, s32, bits, group, sym)
+    assert np.array_equal(qw.cpu().numpy().view(np.uint32), qo)
+    assert np.array_equal(sc.cpu().numpy(), so)
+    assert np.array_equal(z.cpu().numpy(), zo)
+
+
+# ---------------------------------------------------------------- statistics
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("shape", [(64, 256), (1, 8), (300, 4104), (7, 3), (33, 77)])
+def test_channel_stats(awq, dtype, shape):
+    N, n_in = shape
+    _, X = make_random_layer(4, n_in, N, dtype=dtype, seed=N + n_in)
+    sx = awq.awq_channel_stats(X.cuda()).cpu().numpy()
+    ref = O.channel_salience(_np_x(X))
+    if dtype == "f32":
+        assert np.allclose(sx, ref, rtol=1e-14, atol=0)
+    else:
+        assert np.array_equal(sx, ref)   # float64 sums of 16-bit values are exact
+
+
+# ---------------------------------------------------------------- packing
+
+PACK_CASES = [
+    (4, 128, True), (4, 128, False), (3, 128, True), (3, 128, False), (2, 64, False),
+    (8, 32, True), (5, 16, False), (4, 8, True), (4, 256, False),
+    (4, 96, True), (3, 96, False), (4, 384, False), (4, None, True), (3, 24, True),
+]
+
+
+@pytest.mark.parametrize("bits,group,sym", PACK_CASES)
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_quantize_pack_bit_exact(awq, bits, group, sym, dtype):
+    W, X = make_random_layer(37, 768, 16, dtype=dtype, seed=bits * 100 + (group or 0))
+    g = 768 if group is None else group
+    rng = np.random.default_rng(5)
+    s32 = rng.uniform(0.05, 20.0, size=768).astype(np.float32)
+    check_pack(awq, W, s32, bits, g, sym)
+
+
+def test_quantize_pack_special_groups(awq):
+    W, _ = make_random_layer(8, 256, 4, dtype="bf16", seed=3)
+    W = W.clone()
+    W[0, :128] = W[0, :128].abs()        # all-positive group
+    W[1, :128] = -W[1, :128].abs()       # all-negative group
+    W[2, :128] = 0                       # all-zero group
+    W[3, 128:] = 1e-30                   # tiny: the 1e-8 floor of the step applies
+    s32 = np.ones(256, dtype=np.float32)
+    for sym in (True, False):
+        check_pack(awq, W, s32, 4, 128, sym)
+
+
+def test_quantize_pack_ragged_shapes(awq):
+    for out, n_in, g in ((1, 8, 8), (5, 40, 8), (3, 2, 2), (1, 2, 2), (9, 264, 8)):
+        W, _ = make_random_layer(out, n_in, 2, dtype="bf16", seed=out * n_in)
+        s32 = np.random.default_rng(out).uniform(0.5, 2.0, size=n_in).astype(np.float32)
+        for bits in (3, 4):
+            for sym in (True, False):
+                check_pack(awq, W, s32, bits, g, sym)
+
+
+def test_quantize_pack_nan_reports(awq):
+    W, _ = make_random_layer(4, 128, 2, dtype="bf16", seed=9)
+    W = W.clone()
+    W[2, 5] = float("nan")
+    st = awq.new_status()
+    awq.awq_quantize_pack(W.cuda(), torch.ones(128, device="cuda"), 4, 128, True, dev_status=st,
+                          check=False)
+    assert int(st.item()) == 3
+
+
+# ---------------------------------------------------------------- search
+
+SEARCH_CASES = [
+    # (out, in, N, dtype, bits, group, sym, grid)
+    (128, 256, 64, "f32", 4, 128, True, 20),       # the tiny configuration's shape
+    (300, 384, 100, "bf16", 4, 128, False, 20),    # ragged rows, 3 row tiles, odd K groups
+    (256, 512, 300, "f16", 4, 128, True, 10),      # two token tiles
+    (200, 256, 32, "bf16", 3, 64, True, 8),        # 3 bits, group 64, 8 alphas per unit
+    (130, 96, 17, "bf16", 4, 32, False, 5),        # group 32, partial K block
+    (64, 1024, 513, "bf16", 4, 128, False, 4),     # three token tiles, 16 K blocks
+    (1, 128, 1, "bf16", 4, 128, True, 20),         # one row, one token
+    (384, 640, 256, "f16", 2, 64, False, 20),
+    (128, 256, 16, "bf16", 4, 128, True, 20),      # 8 alphas per unit, both producer banks
+    (96, 1024, 20, "bf16", 4, 128, False, 20),     # 8 alphas per unit over 8 K groups
+    (256, 384, 48, "bf16", 4, 128, True, 20),      # odd number of K groups
+    (160, 512, 40, "f32", 4, 64, False, 12),
+]
+
+
+@pytest.mark.parametrize("case", SEARCH_CASES, ids=lambda c: "%dx%d_n%d_%s_b%d_g%d_%s_G%d" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], "sym" if c[6] else "asym", c[7]))
+def test_search_matches_oracle(awq, case):
+    out, n_in, N, dtype, bits, group, sym, grid = case
+    W, X = make_random_layer(out, n_in, N, dtype=dtype, seed=out + n_in + N,
+                             n_outlier=max(1, n_in // 64))
+    e, b, res = check_search(awq, W, X, bits, group, sym, grid, label=str(case))
+    # the kept scales reproduce the oracle's codes exactly
+    check_pack(awq, W, res.s32[b], bits, group, sym)
+
+
+def test_search_shared_input_group(awq):
+    """q/k/v share X and one s: the concatenated rows are searched at once."""
+    ws, X = [], None
+    for i in range(3):
+        w, x = make_random_layer(128, 256, 96, dtype="bf16", seed=40 + i, n_outlier=3)
+        ws.append(w)
+        X = x if X is None else X
+    W = torch.cat(ws, 0).contiguous()
+    check_search(awq, W, X, 4, 128, False, 20, "qkv")
+
+
+def test_search_flat_salience_keeps_alpha_zero(awq):
+    """Equal mean |X| per channel: every alpha has s = 1, the errors tie, the
+    first alpha is kept, and the errors still match the oracle."""
+    W, _ = make_random_layer(256, 256, 8, dtype="bf16", seed=1)
+    sign = torch.where(torch.rand(64, 256, generator=torch.Generator().manual_seed(2)) < 0.5, -1.0, 1.0)
+    X = (sign * 0.375).to(torch.bfloat16)
+    e, b, res = check_search(awq, W, X, 4, 128, True, 20, "flat")
+    assert b == 0 and res.best == 0
+    assert np.all(e == e[0])
+
+
+def test_search_is_deterministic(awq):
+    W, X = make_random_layer(512, 1024, 256, dtype="bf16", seed=77, n_outlier=10)
+    Wd, Xd = _dev(W, X)
+    r1 = [t.clone() for t in awq.awq_search(Wd, Xd, 4, 128, False, 20)]
+    r2 = awq.awq_search(Wd, Xd, 4, 128, False, 20)
+    for a, b in zip(r1, r2):
+        assert torch.equal(a, b)
+
+
+def test_search_given_sx(awq):
+    W, X = make_random_layer(256, 512, 64, dtype="bf16", seed=5, n_outlier=4)
+    Wd, Xd = _dev(W, X)
+    sx = awq.awq_channel_stats(Xd)
+    a = awq.awq_search(Wd, Xd, 4, 128, True, 20)
+    b = awq.awq_search(Wd, Xd, 4, 128, True, 20, sx=sx)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+def test_search_nonfinite_input(awq):
+    W, X = make_random_layer(128, 256, 16, dtype="bf16", seed=6)
+    X = X.clone()
+    X[3, 7] = float("nan")
+    st = awq.new_status()
+    err, best, _ = awq.awq_search(W.cuda(), X.cuda(), 4, 128, True, 20, dev_status=st, check=False)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 3
+    assert int(best.item()) == -1
+    # alpha = 0 has s = 1 in every column, so the NaN channel still reaches
+    # the error only through X; every alpha's error is NaN
+    assert torch.isnan(err).all()
+
+
+def test_search_wait_timeout_reports_and_recovers(awq):
+    """A wait on a barrier nothing arrives at runs out (50 ms); the kernel
+    returns with AWQ_ERR_TIMEOUT, says where it gave up, and the context
+    stays usable."""
+    W, X = make_random_layer(256, 512, 64, dtype="bf16", seed=8)
+    Wd, Xd = _dev(W, X)
+    diag = torch.zeros(4, dtype=torch.int32, device="cuda")
+    opts = awq.SearchOpts()
+    opts.wait_limit_ns = 50_000_000
+    opts.test_timeout = 1
+    opts.diag = diag.data_ptr()
+    st = awq.new_status()
+    awq.awq_search(Wd, Xd, 4, 128, True, 20, dev_status=st, opts=opts, check=False)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 4
+    assert diag[0].item() == 5          # the deliberately unset barrier
+    check_search(awq, W, X, 4, 128, True, 20, "after timeout")
+
+
+def test_search_rejects_unsupported_group(awq):
+    W, X = make_random_layer(64, 256, 16, dtype="bf16", seed=1)
+    with pytest.raises(awq.AWQError) as ei:
+        awq.awq_search(W.cuda(), X.cuda(), 4, 256, True, 20)
+    assert ei.value.code == 2
