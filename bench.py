@@ -1,0 +1,305 @@
+"""Benchmark of the AWQ per-layer scale search on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step is the whole hot path over one seeded synthetic layer: channel
+statistics, the alpha tables, the fused tcgen05 search over every alpha of
+the grid, the reduction and argmin, and the final quantize + pack at the
+kept scales, all through the C ABI.  The metric is layer-alpha-evals/s
+(alphas searched per second); GFLOP/s and the tensor-core roofline fraction
+of the search kernel are reported beside it.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream; between steps a 512 MiB buffer is written to flush
+the 126 MB L2 (outside the timed region).  With several GPUs (torchrun),
+every rank searches its own layer (different seed): weak scaling, no
+collective on the data path; the time is the max over ranks.
+
+--impl reference times the CPU oracle (float64 numpy, the pages' algorithm
+as written) on the same layer, each step a bounded sample of the grid.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synthetic import CONFIGS, config_by_name, make_layer  # noqa: E402
+
+DEFAULT_CONFIG = "nb-4096x4096-n256"
+METRIC = "AWQ search layer-alpha-evals/sec"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops", 1800.0), d.get("hbm_gbs", 6400.0), "measured"
+    return 1800.0, 6400.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        rank = int(os.environ.get("RANK", "0"))
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return dist, rank, ws
+    return None, 0, 1
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_ours(args, cfg, rank, world, dist):
+    import post_weight_quantization_32_b300 as awq
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    W, X = make_layer(cfg, seed=rank)
+    Wd, Xd = W.to(dev), X.to(dev)
+    out, n_in, N, na = cfg.out, cfg.in_, cfg.N, cfg.n_alpha
+    ws = torch.empty(awq.awq_search_workspace_bytes(Wd.dtype, out, n_in, N, cfg.group, cfg.grid),
+                     dtype=torch.uint8, device=dev)
+    err = torch.empty(na, dtype=torch.float64, device=dev)
+    best = torch.empty(1, dtype=torch.int32, device=dev)
+    s_best = torch.empty(n_in, dtype=torch.float32, device=dev)
+    nwords = (n_in * cfg.bits + 31) // 32
+    qw = torch.empty((out, nwords), dtype=torch.int32, device=dev)
+    sc = torch.empty((out, n_in // cfg.group), dtype=torch.float32, device=dev)
+    zz = torch.empty((out, n_in // cfg.group), dtype=torch.uint8, device=dev)
+    st = awq.new_status(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    ev_s0, ev_s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_s0.record(stream)   # torch creates the CUDA event at its first record
+    ev_s1.record(stream)
+    opts = awq.SearchOpts()
+    opts.ev_search_start = ev_s0.cuda_event
+    opts.ev_search_stop = ev_s1.cuda_event
+
+    def step(W_, X_):
+        # torch times only events it has recorded itself: record both here;
+        # the library records them again around the search kernel
+        ev_s0.record(stream)
+        ev_s1.record(stream)
+        awq.awq_search(W_, X_, cfg.bits, cfg.group, cfg.sym, cfg.grid, workspace=ws,
+                       out_tensors=(err, best, s_best), dev_status=st, opts=opts, check=False)
+        awq.awq_quantize_pack(W_, s_best, cfg.bits, cfg.group, cfg.sym, out_tensors=(qw, sc, zz),
+                              dev_status=st, check=False)
+
+    for _ in range(args.warmup):
+        step(Wd, Xd)
+    torch.cuda.synchronize()
+    awq.check_status(st, "bench warm-up")
+    if dist is not None:
+        dist.barrier()
+    step_ms, search_ms = [], []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            e0.record(stream)
+            step(Wd, Xd)
+            e1.record(stream)
+            e1.synchronize()
+            step_ms.append(e0.elapsed_time(e1))
+            search_ms.append(ev_s0.elapsed_time(ev_s1))
+    torch.cuda.synchronize()
+    awq.check_status(st, "bench")
+    if dist is not None:
+        dist.barrier()
+
+    # end to end through the public API with host buffers: H2D of W and X from
+    # pinned memory, the path, D2H of every result, every step
+    Wh, Xh = W.pin_memory(), X.pin_memory()
+    res_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (err, best, s_best, qw, sc, zz)]
+    Wb, Xb = torch.empty_like(Wd), torch.empty_like(Xd)
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        Wb.copy_(Wh, non_blocking=True)
+        Xb.copy_(Xh, non_blocking=True)
+        step(Wb, Xb)
+        for h, d in zip(res_h, (err, best, s_best, qw, sc, zz)):
+            h.copy_(d, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    h2d = W.numel() * W.element_size() + X.numel() * X.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in res_h)
+
+    def world_max(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    ms = world_max(sum(step_ms) / len(step_ms))
+    e2e = world_max(sum(e2e_ms) / len(e2e_ms))
+    t_search = world_max(sum(search_ms) / len(search_ms))
+    return dict(ms=ms, e2e_ms=e2e, search_ms=t_search, h2d=h2d, d2h=d2h, clocks=clk.summary())
+
+
+def run_oracle_sample(cfg, n_sample, seed=0):
+    """Oracle time for n_sample alphas of the grid (spread over it), seconds."""
+    from oracle import awq_oracle as O
+    W, X = make_layer(cfg, seed=seed)
+    Wn, Xn = W.float().numpy(), X.double().numpy()
+    idx = set(np.linspace(0, cfg.n_alpha - 1, n_sample).round().astype(int).tolist())
+    t0 = time.perf_counter()
+    O.awq_search(Wn, Xn, cfg.bits, cfg.group, cfg.grid, cfg.sym, alpha_index=idx)
+    return time.perf_counter() - t0, len(idx)
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=[c.name for c in CONFIGS])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample", type=int, default=2, help="alphas in the oracle's timed sample")
+    args = ap.parse_args()
+    cfg = config_by_name(args.config)
+    dist, rank, world = _dist()
+    tflops_peak, hbm_peak, peak_kind = _peaks()
+    flops = cfg.search_flops
+    conf = {"workload": cfg.name, "out": cfg.out, "in": cfg.in_, "N": cfg.N,
+            "dtype_in": cfg.dtype, "bits": cfg.bits, "group": cfg.group,
+            "quantizer": "sym" if cfg.sym else "asym", "n_alpha": cfg.n_alpha,
+            "l2": "flushed between steps (512 MiB write)", "parallelism": "independent layers per rank"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        times = []
+        n = 1
+        for i in range(args.warmup + args.steps):
+            t, n = run_oracle_sample(cfg, 1)
+            if i >= args.warmup:
+                times.append(t)
+        t = sum(times) / len(times)
+        v = n / t
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "layer-alpha-evals/s",
+                "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": conf,
+                "cpu_baseline": {"value": v, "unit": "layer-alpha-evals/s", "cores": _cores(),
+                                 "kind": "oracle",
+                                 "sample": "one alpha of the grid per step (incl. the reference GEMM X W^T)"},
+                "e2e": {"value": v, "unit": "layer-alpha-evals/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    r = run_ours(args, cfg, rank, world, dist)
+    if rank != 0:
+        return
+    n_alpha = cfg.n_alpha
+    value = n_alpha * world / (r["ms"] * 1e-3)
+    e2e_v = n_alpha * world / (r["e2e_ms"] * 1e-3)
+    achieved = flops / (r["search_ms"] * 1e-3) / 1e12
+    cpu_t, cpu_n = run_oracle_sample(cfg, args.cpu_sample)
+    launches_per_step = 7 + (0 if cfg.dtype == "f16" else 2)
+    line = {
+        "metric": METRIC, "value": value, "unit": "layer-alpha-evals/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic", "config": conf,
+        "gflops": flops / (r["ms"] * 1e-3) / 1e9,
+        "search_kernel_ms": r["search_ms"],
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tflops_peak, "traffic": None,
+                     "kernel": "awq_search_kernel", "peak_kind": peak_kind + " (bf16 dense = fp16 dense)"},
+        "cpu_baseline": {"value": cpu_n / cpu_t, "unit": "layer-alpha-evals/s", "cores": _cores(),
+                         "kind": "oracle",
+                         "sample": "%d alphas of the grid on the same layer (incl. the reference GEMM)" % cpu_n},
+        "e2e": {"value": e2e_v, "unit": "layer-alpha-evals/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": r["clocks"],
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -676,10 +676,10 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
   a.maxqf = (float)((1 << bits) - 1);
   a.wait_limit_ns = (uint64_t)(wait_limit_ns > 0 ? wait_limit_ns : 2000000000LL);
   a.test_timeout = test_timeout;
-  if (ev0) cudaEventRecord(ev0, s);
+  if (ev0 && (e = cudaEventRecord(ev0, s)) != cudaSuccess) return e;
   fn<<<pl.grid, kThreads, pl.smem, s>>>(mw, mx, a);
   e = cudaGetLastError();
-  if (ev1) cudaEventRecord(ev1, s);
+  if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
   return e;
 }
 
