@@ -175,6 +175,43 @@ int awq_quantize_pack(const void* W, int dtype, int64_t out, int64_t in,
                       uint32_t* qweight, float* scales, uint8_t* zeros,
                       int32_t* dev_status, awq_stream_t stream);
 
+/*
+ * awq_search_noalloc - awq_search for callers that cannot allocate device
+ * memory.  (The method itself has no counterpart of this: it is a calling
+ * convenience of this library.)
+ *
+ * Some callers have no way to obtain scratch memory: a plug-in whose host
+ * application owns every device allocation and offers no workspace hook,
+ * real-time code that forbids cudaMalloc because it can synchronise the
+ * device and take unbounded time, or code that must not grow its memory
+ * footprint after start-up.  This entry point needs no workspace argument:
+ * its scratch is a fixed device array inside the library of
+ * AWQ_NOALLOC_SCRATCH_BYTES (32 MiB), reserved on every GPU that loads this
+ * part of the library and held until the process exits.  The call makes no
+ * cudaMalloc, cudaFree or other allocating call.
+ *
+ * Arguments, outputs, numerics and errors are those of awq_search, except:
+ *  - the sizes must satisfy awq_search_workspace_bytes(dtype, out, in, N,
+ *    group, grid) <= AWQ_NOALLOC_SCRATCH_BYTES; larger problems return
+ *    AWQ_ERR_UNSUPPORTED before anything is enqueued (use awq_search with
+ *    your own workspace for those);
+ *  - the first call on each device looks up the device address of the
+ *    array (with that device current) and caches it; make that first call
+ *    before any stream capture begins;
+ *  - every call on a device shares the one array, which keeps the previous
+ *    call's contents (the call clears what must start at zero).  Calls whose
+ *    work overlaps on the GPU (for example on two streams without ordering
+ *    between them) race on the array and give wrong results: order them on
+ *    one stream or with events.
+ */
+#define AWQ_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+int awq_search_noalloc(const void* W, const void* X, int dtype,
+                       int64_t out, int64_t in, int64_t N,
+                       const double* sx, int bits, int group, int sym, int grid,
+                       double* err, int32_t* best, float* s_best,
+                       int32_t* dev_status, awq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

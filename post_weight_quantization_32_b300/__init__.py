@@ -14,6 +14,9 @@ Entry points (same names as the C ABI):
 * ``awq_quantize_pack(W, s, bits, group, sym)`` -> (qweight, scales, zeros):
   qweight int32 [out, ceil(in*bits/32)] holding the uint32 words (view it
   as unsigned), scales float32 [out, in/group], zeros uint8 [out, in/group]
+* ``awq_search_noalloc(W, X, bits, group, sym, grid)`` -> as ``awq_search``,
+  but the library's fixed scratch array (``NOALLOC_SCRATCH_BYTES``) stands
+  in for the workspace, for callers that cannot allocate device memory
 """
 from __future__ import annotations
 
@@ -26,7 +29,7 @@ import torch
 __all__ = [
     "AWQError", "SearchOpts", "lib", "awq_channel_stats", "awq_search",
     "awq_search_workspace_bytes", "awq_quantize_pack", "new_status", "check_status", "STATUS",
-    "DTYPE",
+    "DTYPE", "awq_search_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -37,7 +40,10 @@ STATUS = {0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARG", 2: "AWQ_ERR_UNSUPPORTED", 3: "A
           4: "AWQ_ERR_TIMEOUT", 5: "AWQ_ERR_CUDA"}
 
 EXPORTS = ("awq_status_string", "awq_channel_stats", "awq_search_workspace_bytes", "awq_search",
-           "awq_search_ex", "awq_quantize_pack")
+           "awq_search_ex", "awq_quantize_pack", "awq_search_noalloc")
+
+# Size of the library's fixed scratch array used by awq_search_noalloc.
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def _load() -> ctypes.CDLL:
@@ -58,6 +64,9 @@ def _load() -> ctypes.CDLL:
     L.awq_search_ex.argtypes = L.awq_search.argtypes + [vp]
     L.awq_quantize_pack.restype = i32
     L.awq_quantize_pack.argtypes = [vp, i32, i64, i64, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+    L.awq_search_noalloc.restype = i32
+    L.awq_search_noalloc.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, i32, vp, vp, vp,
+                                     vp, vp]
     return L
 
 
@@ -189,3 +198,34 @@ def awq_quantize_pack(W: torch.Tensor, s: torch.Tensor, bits: int = 4, group: Op
     if check:
         check_status(st, "awq_quantize_pack")
     return qweight, scales, zeros
+
+
+def awq_search_noalloc(W: torch.Tensor, X: torch.Tensor, bits: int = 4, group: Optional[int] = None,
+                       sym: bool = True, grid: int = 20, sx: Optional[torch.Tensor] = None,
+                       out_tensors=None, stream=None, dev_status: Optional[torch.Tensor] = None,
+                       check: bool = True) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """``awq_search`` without a workspace: the library's fixed scratch array
+    is used instead, so the C call allocates nothing.  Output tensors are
+    still the caller's (pass ``out_tensors`` to reuse preallocated ones).
+    Problems whose workspace would exceed ``NOALLOC_SCRATCH_BYTES`` raise
+    AWQError with AWQ_ERR_UNSUPPORTED."""
+    _need(W, "W", 2)
+    _need(X, "X", 2)
+    if W.dtype != X.dtype or W.shape[1] != X.shape[1]:
+        raise ValueError("W and X must share dtype and the input dimension")
+    out, n_in = W.shape
+    N = X.shape[0]
+    g = n_in if group is None else int(group)
+    if out_tensors is None:
+        err = torch.empty(grid + 1, dtype=torch.float64, device=W.device)
+        best = torch.empty(1, dtype=torch.int32, device=W.device)
+        s_best = torch.empty(n_in, dtype=torch.float32, device=W.device)
+    else:
+        err, best, s_best = out_tensors
+    st = dev_status if dev_status is not None else new_status(W.device)
+    _check(lib.awq_search_noalloc(_ptr(W), _ptr(X), DTYPE[W.dtype], out, n_in, N, _ptr(sx), bits, g,
+                                  1 if sym else 0, grid, _ptr(err), _ptr(best), _ptr(s_best),
+                                  _ptr(st), _stream(stream)), "awq_search_noalloc")
+    if check:
+        check_status(st, "awq_search_noalloc")
+    return err, best, s_best
