@@ -11,6 +11,7 @@ from __future__ import annotations
 import concurrent.futures as cf
 import glob
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -38,12 +39,39 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
+# The search kernels split their registers between warpgroups with
+# setmaxnreg (128 threads x 56 + 256 threads x 216); that split must fit in
+# what the block is launched with, so every search kernel has to be compiled
+# to the full 168 registers a thread that its launch bounds allow.
+SEARCH_KERNEL_REGS = 168
+
+
+def _check_registers(src: str, text: str) -> None:
+    current = None
+    for line in text.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current and "awq_search_kernel" in current:
+            if int(m.group(1)) != SEARCH_KERNEL_REGS:
+                raise RuntimeError("%s: %s compiled to %s registers, the register split needs %d"
+                                   % (os.path.basename(src), current, m.group(1), SEARCH_KERNEL_REGS))
+            current = None
+
+
 def _compile(src: str, obj: str, log: list) -> None:
     cmd = [_nvcc()] + ARCH + FLAGS + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     log.append((src, r.stdout + r.stderr))
     if r.returncode != 0:
         raise RuntimeError("nvcc failed on %s:\n%s" % (os.path.basename(src), r.stdout + r.stderr))
+    try:
+        _check_registers(src, r.stdout + r.stderr)
+    except RuntimeError:
+        os.remove(obj)
+        raise
 
 
 def build(verbose: bool = False, force: bool = False) -> str:

@@ -1,6 +1,6 @@
 // The C ABI of libawq (declared in include/awq.h): argument checks,
 // workspace layout, and the order of launches on the caller's stream.
-#include "../../include/awq.h"
+#include "awq.h"
 #include "awq_internal.h"
 
 namespace awq {

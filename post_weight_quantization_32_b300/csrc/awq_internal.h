@@ -57,6 +57,7 @@ struct SearchPlan {
   int n_units;  // n_rt * n_ag * n_tt
   int n_tiles;  // partial sums per alpha = n_rt * n_tt
   int sw, sx;   // W and X ring depths
+  size_t w_stage;  // bytes of one W ring stage (W tile + the alphas' scale-table columns)
   size_t smem;  // dynamic shared memory bytes
   int grid;     // persistent CTAs
 };

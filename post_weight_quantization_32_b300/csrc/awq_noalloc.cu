@@ -10,7 +10,7 @@
 // zero on each call, so stale contents of an earlier call do not matter.
 #include <mutex>
 
-#include "../../include/awq.h"
+#include "awq.h"
 #include "awq_internal.h"
 
 namespace awq {

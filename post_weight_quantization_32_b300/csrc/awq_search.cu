@@ -7,26 +7,30 @@
 //
 // Work unit = (128-row tile of W, a group of up to 8 alphas, a token tile of
 // T <= 256 tokens).  One persistent CTA per SM walks a static list of units.
-// Warp roles inside a CTA (384 threads):
-//   warp 0      TMA loads of W blocks (128 rows x 64 columns) into a ring
-//   warp 1      TMA loads of X blocks (T tokens x 64 columns, fp16) into a ring
-//   warp 2      tensor memory owner and the single tcgen05.mma issuer
-//   warp 3      idle
-//   warps 4-11  two warpgroups of producers: thread = one W row.  Each reads
-//               its row's weights, scales by s_alpha, finds the group
-//               max/min, rounds to the grid, and writes dW (fp16) straight
-//               into tensor memory, where the MMA reads it as operand A;
-//               after the last K block they read the fp32 accumulators
-//               (128 rows x T tokens per alpha), square and sum them.
-//               Warpgroup 0 takes the even K groups of a unit, warpgroup 1
-//               the odd ones.
+// Warp roles inside a CTA (384 threads, three warpgroups):
+//   warpgroup 0 (56 registers a thread after setmaxnreg):
+//     warp 0    TMA loads of W blocks (128 rows x 64 columns) together with
+//               the matching 64 columns of the s and 2^e/s tables of the
+//               unit's alphas, into one ring stage
+//     warp 1    TMA loads of X blocks (T tokens x 64 columns, fp16)
+//     warp 2    tensor memory owner and the single tcgen05.mma issuer
+//     warp 3    idle
+//   warpgroups 1 and 2 (216 registers a thread): producers, thread = one W
+//     row.  Per 128-column job (one quantization group for group 128) and
+//     alpha, pass 1 forms t = w * s in registers and the group's range;
+//     pass 2 rounds t to the group's grid and writes -dW (fp16; the sign
+//     does not change the squared error) straight into tensor memory,
+//     where the MMA reads it as operand A.  After the last K block they
+//     read the fp32 accumulators (128 rows x T tokens per alpha) back,
+//     square and sum them.  Warpgroup 1 takes the even jobs of a unit,
+//     warpgroup 2 the odd ones, each with its own ring bank and dW slots.
 // Tensor memory (512 columns): columns [0, 256) hold a_per accumulators of
 // T columns; columns [256, 512) are eight 32-column slots of dW (64 fp16
 // values per row each), four per producer warpgroup.  X is the MMA's B
 // operand from shared memory in the 128-byte-swizzle K-major layout that
-// TMA writes.  The W ring is likewise split into one bank per warpgroup.
-// With one bank per consumer, every barrier's phases are consumed in order
-// by a single party, so a parity wait can never be a full phase ahead.
+// TMA writes.  With one bank per consumer, every barrier's phases are
+// consumed in order by a single party, so a parity wait can never be a
+// full phase ahead.
 //
 // The GEMM runs on fp16 operands (11-bit significands) with fp32
 // accumulation.  X arrives as fp16 scaled by a power of two, and dW is
@@ -34,15 +38,27 @@
 // from max|X| and max|W| so every value lies in fp16's normal range; the
 // float64 reduction divides the exact powers of two out again.
 //
-// The producer rounds t * (1/scale) with one fused multiply-add against
-// 1.5 * 2^23 (round to nearest even); next to an exact half-integer this can
-// differ from rounding the correctly rounded quotient, which changes the
-// error far less than the fp16 rounding of dW.  Where every scale of an alpha
-// is a power of two (alpha = 0, flat salience) t / scale falls on exact
-// half-integers of the 16-bit weight lattice often, so those alphas use the
-// correctly rounded quotient.  The group step itself is the exact float32
-// max(m / L, 1e-8) (asymmetric: (hi - lo) / maxq and the zero point
-// round(-lo / scale)), as in the final quantizer.
+// Rounding.  The producer rounds t * (1/scale) with one fused multiply-add
+// against 1.5 * 2^23 (round to nearest even).  Next to an exact
+// half-integer this can differ from rounding the correctly rounded quotient;
+// either neighbour is half a step away, so only the sign of that entry's
+// error changes, far less than the fp16 rounding of dW moves the score.
+// Where every scale of an alpha is a power of two (alpha = 0, flat salience)
+// t / scale falls on exact half-integers of the 16-bit weight lattice often,
+// so those alphas use the correctly rounded quotient.  The group step is
+// the exact float32 max(m / L, 1e-8) (asymmetric: (hi - lo) / maxq) as in
+// the final quantizer.  The code clamps of the quantizers never act in
+// exact arithmetic (|t| / scale <= L, and for the asymmetric grid
+// round(t / scale) + zero stays in [0, maxq] because the zero point is the
+// rounded -lo / scale), so the dequantized value is scale * round(t / scale)
+// for both quantizers and the zero point cancels.  The one exception is an
+// exact tie: when -lo / scale is k + 1/2 with k odd, round-half-even gives
+// zero = k + 1 and the top entry rounds to code maxq + 1, which the clamp
+// pulls back.  Exact ties are common only where every scale is a power of
+// two (the weights then stay on their 16-bit lattice), so the correctly
+// rounded path, which those alphas take, keeps the asymmetric upper clamp;
+// elsewhere a tie needs an exact coincidence of products, and a near-tie
+// only flips the sign of one half-step error.
 //
 // Every wait on an mbarrier is bounded (wall clock).  A wait that runs out
 // raises a shared abort flag; all roles then stop issuing work, drain what
@@ -69,10 +85,14 @@ constexpr int kMaxSW = 8, kMaxSX = 8, kMaxAPer = 8;
 constexpr uint32_t kSlotCol0 = 256;
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: fma(x, r, M) - M = rint(x * r)
 constexpr uint32_t kCtrlBytes = 1024;
+// Register split after setmaxnreg: 128 * 56 + 256 * 216 = 62464 must not
+// exceed the 384 * 168 = 64512 registers the block is launched with (the
+// build checks that every search kernel is compiled to 168 registers).
+constexpr uint32_t kRegsCtl = 56, kRegsProd = 216;
+constexpr uint32_t kLaunchRegs = 168;
+static_assert(128 * kRegsCtl + 256 * kRegsProd <= kThreads * kLaunchRegs, "register split");
 
 struct SearchArgs {
-  const float* s32;       // [n_alpha][in]
-  const float* inv_s32;   // [n_alpha][in], times 2^e_k
   const int32_t* pow2_s;  // [n_alpha]: nonzero when every scale of that alpha is a power of two
   double* partials;       // [n_alpha][n_tiles]
   int32_t* status;
@@ -80,6 +100,7 @@ struct SearchArgs {
   int out, in, N;
   int n_alpha, a_per, n_ag, n_rt, n_tt, T, n_kb, n_units, n_tiles;
   int sw, sx;
+  uint32_t w_stage;       // bytes of one W ring stage: W tile, then the scale block
   float Lf, maxqf;
   uint64_t wait_limit_ns;
   int test_timeout;
@@ -95,6 +116,11 @@ struct Ctrl {
   float epi[2][kMaxAPer][8];
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
+
+template <typename WT>
+__host__ __device__ constexpr uint32_t w_tile_bytes() {
+  return (uint32_t)(kRows * kKB * sizeof(WT));
+}
 
 // Eight weights (columns 8*cc .. 8*cc+7 of the 64-column block) of `row`
 // from a TMA stage in the 128-byte swizzle layout: the 16-byte chunk j of a
@@ -138,33 +164,31 @@ __device__ __forceinline__ void load_w8<float>(const uint8_t* stage, int row, in
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-__device__ __forceinline__ void load_f8(const float* p, bool valid, float (&v)[8]) {
-  if (valid) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = 0.0f;
-  }
+// Eight consecutive floats of a scale-table row in shared memory (every
+// lane reads the same address: a broadcast).
+__device__ __forceinline__ void lds_f8(const float* p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
+__device__ __forceinline__ uint32_t pack_f16x2(float2 v) {
+  __half2 h = __float22half2_rn(v);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// dW for the 64 columns of K block kbi of a producer job, as 32 fp16 pairs.
-// q = round(t / scale): the fast form rounds t * (1/scale) with one fused
-// multiply-add against 1.5 * 2^23; the EXACT form first forms the correctly
-// rounded quotient q1 = q0 + (t - q0 * scale) * (1/scale), q0 = t * (1/scale)
-// (one residual correction of the reciprocal quotient), then rounds it.
-template <bool SYM, bool EXACT, int G, int JC>
-__device__ __forceinline__ void make_dw(const float (&t)[JC], int kbi, const float* ip, int col0,
-                                        int in, const float (&scl)[JC / G],
-                                        const float (&rcp)[JC / G], const float (&alo)[JC / G],
-                                        const float (&ahi)[JC / G], uint32_t (&pk)[32]) {
+// Pass 2 for one 64-column K block of a job: -dW * 2^e = (t - q * scale) *
+// (2^e / s) as 32 fp16 pairs.  q = round(t / scale): the fast form rounds
+// t * (1/scale) with one fused multiply-add against 1.5 * 2^23; the EXACT
+// form first forms the correctly rounded quotient q1 = q0 + (t - q0 *
+// scale) * (1/scale), q0 = t * (1/scale), then rounds it.
+// With CLAMP the rounded value is also capped at the group's top code
+// (chi = 1.5 * 2^23 + maxq - zero, in the shifted domain).
+template <bool EXACT, bool CLAMP, int G, int JC>
+__device__ __forceinline__ void make_dw(const float (&t)[JC], int kbi, const float* inv_row,
+                                        const float (&scl)[JC / G], const float (&rcp)[JC / G],
+                                        const float (&chi)[JC / G], uint32_t (&pk)[32]) {
   const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
   const float2 nm2 = make_float2(-kRoundMagic, -kRoundMagic);
 #pragma unroll
@@ -172,29 +196,27 @@ __device__ __forceinline__ void make_dw(const float (&t)[JC], int kbi, const flo
     const int cgi = kbi * 8 + cc;
     const int g = (cgi * 8) / G;
     float i8[8];
-    load_f8(ip + cgi * 8, col0 + cgi * 8 < in, i8);
+    lds_f8(inv_row + cc * 8, i8);
     const float2 rc2 = make_float2(rcp[g], rcp[g]);
-    const float2 sc2 = make_float2(scl[g], scl[g]);
+    const float2 ns2 = make_float2(-scl[g], -scl[g]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float t0 = t[cgi * 8 + 2 * e], t1 = t[cgi * 8 + 2 * e + 1];
-      const float2 tv = make_float2(t0, t1);
+      const float2 tv = make_float2(t[cgi * 8 + 2 * e], t[cgi * 8 + 2 * e + 1]);
       float2 av;
       if (EXACT) {
         const float2 q0 = __fmul2_rn(tv, rc2);
-        const float2 r = __ffma2_rn(make_float2(-q0.x, -q0.y), sc2, tv);
+        const float2 r = __ffma2_rn(q0, ns2, tv);
         av = __fadd2_rn(__ffma2_rn(r, rc2, q0), mg2);
       } else {
         av = __ffma2_rn(tv, rc2, mg2);
       }
-      if (!SYM) {
-        av.x = fminf(fmaxf(av.x, alo[g]), ahi[g]);
-        av.y = fminf(fmaxf(av.y, alo[g]), ahi[g]);
+      if (CLAMP) {
+        av.x = fminf(av.x, chi[g]);
+        av.y = fminf(av.y, chi[g]);
       }
       const float2 qv = __fadd2_rn(av, nm2);
-      const float2 ev = __ffma2_rn(qv, sc2, make_float2(-t0, -t1));
-      const float2 dv = __fmul2_rn(ev, make_float2(i8[2 * e], i8[2 * e + 1]));
-      pk[cc * 4 + e] = pack_f16x2(dv.x, dv.y);
+      const float2 ev = __ffma2_rn(qv, ns2, tv);  // t - q * scale
+      pk[cc * 4 + e] = pack_f16x2(__fmul2_rn(ev, make_float2(i8[2 * e], i8[2 * e + 1])));
     }
   }
 }
@@ -202,11 +224,13 @@ __device__ __forceinline__ void make_dw(const float (&t)[JC], int kbi, const flo
 template <typename WT, int G, bool SYM>
 __global__ void __launch_bounds__(kThreads, 1)
     awq_search_kernel(const __grid_constant__ CUtensorMap tmW,
-                      const __grid_constant__ CUtensorMap tmX, const SearchArgs p) {
+                      const __grid_constant__ CUtensorMap tmX,
+                      const __grid_constant__ CUtensorMap tmS, const SearchArgs p) {
   constexpr int KBJ = (G == 128) ? 2 : 1;  // K blocks per producer job
   constexpr int JC = KBJ * kKB;            // columns per producer job
   constexpr int NG = JC / G;               // groups per job
-  constexpr uint32_t W_STAGE = kRows * kKB * sizeof(WT);
+  constexpr int CPG = G / 8;               // 8-column chunks per group
+  constexpr uint32_t W_TILE = w_tile_bytes<WT>();
   constexpr uint32_t FULL = 0xffffffffu;
 
   extern __shared__ uint8_t smem_raw[];
@@ -216,6 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl& c = *reinterpret_cast<Ctrl*>(gbase);
   const uint32_t w_ring = base + kCtrlBytes;
   const uint8_t* w_ring_ptr = gbase + kCtrlBytes;
+  const uint32_t W_STAGE = p.w_stage;
+  const uint32_t S_BYTES = 2u * (uint32_t)p.a_per * kKB * 4u;  // s and 2^e/s rows
   const uint32_t X_STAGE = (uint32_t)p.T * 128u;
   const uint32_t x_ring = w_ring + (uint32_t)p.sw * W_STAGE;
 
@@ -248,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&tmW);
     tma_prefetch_map(&tmX);
+    tma_prefetch_map(&tmS);
   }
   __syncthreads();
   tc_fence_after();
@@ -258,41 +285,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_kg = p.n_kb / KBJ;
   const uint32_t hw = (uint32_t)p.sw / 2;  // W stages per warpgroup bank
 
-  if (warp == 0) {
-    // ---------------------------------------------------------- W loader
-    if (lane == 0) {
-      uint32_t wcnt[2] = {0, 0};  // W blocks loaded into each warpgroup's bank
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsCtl>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- W loader
+      uint32_t wc0 = 0, wc1 = 0;  // W blocks loaded into each warpgroup's bank
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
         const int rt = u / units_per_rt;
+        const int ag = (u % units_per_rt) / p.n_tt;
         for (int kb = 0; kb < p.n_kb; ++kb) {
           const int b = (kb / KBJ) & 1;
-          const uint32_t m = wcnt[b];
+          const uint32_t m = b ? wc1 : wc0;
           const uint32_t st = b * hw + m % hw, ph = (m / hw) & 1;
           if (!mbar_wait(smem_addr(&c.w_empty[st]), ph ^ 1, abort, lim, p.diag, 1, m | (b << 30))) {
             ok = false;
             break;
           }
           const uint32_t bar = smem_addr(&c.w_full[st]);
-          mbar_arrive_expect_tx(bar, W_STAGE);
+          mbar_arrive_expect_tx(bar, W_TILE + S_BYTES);
           const uint32_t dst = w_ring + st * W_STAGE;
           if (sizeof(WT) == 4) {
             tma_load_2d(dst, &tmW, bar, kb * kKB, rt * kRows);
-            tma_load_2d(dst + W_STAGE / 2, &tmW, bar, kb * kKB + 32, rt * kRows);
+            tma_load_2d(dst + W_TILE / 2, &tmW, bar, kb * kKB + 32, rt * kRows);
           } else {
             tma_load_2d(dst, &tmW, bar, kb * kKB, rt * kRows);
           }
-          ++wcnt[b];
+          tma_load_3d(dst + W_TILE, &tmS, bar, kb * kKB, ag * p.a_per, 0);
+          if (b) ++wc1; else ++wc0;
         }
       }
       int never_set = 0;  // drain: wait for the loads still in flight
-      for (int b = 0; b < 2; ++b)
-        for (uint32_t m = wcnt[b] > hw ? wcnt[b] - hw : 0; m < wcnt[b]; ++m)
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t wc = b ? wc1 : wc0;
+        for (uint32_t m = wc > hw ? wc - hw : 0; m < wc; ++m)
           mbar_wait(smem_addr(&c.w_full[b * hw + m % hw]), (m / hw) & 1, &never_set, lim);
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- X loader
-    if (lane == 0) {
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- X loader
       uint32_t seq = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
@@ -312,13 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int never_set = 0;
       for (uint32_t i = seq > (uint32_t)p.sx ? seq - p.sx : 0; i < seq; ++i)
         mbar_wait(smem_addr(&c.x_full[i % p.sx]), (i / p.sx) & 1, &never_set, lim);
-    }
-  } else if (warp == 2) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    } else if (warp == 2 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       const uint32_t idesc = idesc_f16_f32(kRows, (uint32_t)p.T);
       uint32_t xseq = 0, useq = 0;
-      uint32_t dcnt[2] = {0, 0};  // dW slots consumed from each warpgroup's bank
+      uint32_t dc0 = 0, dc1 = 0;  // dW slots consumed from each warpgroup's bank
       bool ok = true;
       if (p.test_timeout) ok = mbar_wait(smem_addr(&c.never), 0, abort, lim, p.diag, 5, 0);
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
@@ -342,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
               }
-              const uint32_t n = dcnt[b];
+              const uint32_t n = b ? dc1 : dc0;
               const uint32_t ds = b * kBankSlots + n % kBankSlots;
               if (!mbar_wait(smem_addr(&c.d_full[ds]), (n / kBankSlots) & 1, abort, lim, p.diag, 8,
                              n | (b << 30))) {
@@ -359,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (kg | kbi | k) != 0 ? 1u : 0u);
               umma_commit(smem_addr(&c.d_empty[ds]));
               if (a == na - 1) umma_commit(smem_addr(&c.x_empty[xs]));
-              ++dcnt[b];
+              if (b) ++dc1; else ++dc0;
             }
           }
         }
@@ -372,8 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int never_set = 0;
       mbar_wait(smem_addr(&c.drain), 0, &never_set, lim);
     }
-  } else if (warp >= 4) {
-    // ---------------------------------------------------------- producers + epilogue
+  } else {
+    // ------------------------------------------------------------ producers + epilogue
+    setmaxnreg_inc<kRegsProd>();
     const int wg = (warp - 4) >> 2;
     const int q = warp & 3;  // tensor memory lanes 32q .. 32q+31
     const int row = q * 32 + lane;
@@ -384,66 +413,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rem = u % units_per_rt;
       const int rt = u / units_per_rt, ag = rem / p.n_tt, tt = rem % p.n_tt;
       const int na = min(p.a_per, p.n_alpha - ag * p.a_per);
-      for (int kg = 0; ok && kg < n_kg; ++kg) {
-        if ((kg & 1) != wg) continue;
+      uint32_t exact_mask = 0;
+      for (int a = 0; a < na; ++a)
+        if (p.pow2_s[ag * p.a_per + a] != 0) exact_mask |= 1u << a;
+      for (int kg = wg; ok && kg < n_kg; kg += 2) {
+        const uint8_t* stg[KBJ];
+#pragma unroll
         for (int kbi = 0; kbi < KBJ; ++kbi) {
           const uint32_t m = wm + kbi;
-          ok = mbar_wait(smem_addr(&c.w_full[wg * hw + m % hw]), (m / hw) & 1, abort, lim, p.diag,
-                         10, m | (wg << 30));
-          ok = __all_sync(FULL, ok);
-          if (!ok) break;
+          const uint32_t st = wg * hw + m % hw;
+          stg[kbi] = w_ring_ptr + st * W_STAGE;
+          if (ok)
+            ok = mbar_wait(smem_addr(&c.w_full[st]), (m / hw) & 1, abort, lim, p.diag, 10,
+                           m | (wg << 30));
         }
+        ok = __all_sync(FULL, ok);
         if (!ok) break;
-        const int col0 = kg * JC;
         for (int a = 0; ok && a < na; ++a) {
-          const int k = ag * p.a_per + a;
-          const float* sp = p.s32 + (size_t)k * p.in + col0;
-          const float* ip = p.inv_s32 + (size_t)k * p.in + col0;
-          const bool exact = p.pow2_s[k] != 0;
-          // pass 1: t = fl32(w * s)
+          // pass 1: t = fl32(w * s) and each group's range
           float t[JC];
+          float r0[NG][4], r1[NG][4];  // sym: running max|t|; asym: running min / max
+#pragma unroll
+          for (int g = 0; g < NG; ++g)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) r0[g][j] = r1[g][j] = 0.0f;
 #pragma unroll
           for (int cgi = 0; cgi < JC / 8; ++cgi) {
-            const int kbi = cgi >> 3, cc = cgi & 7;
-            const uint32_t st = wg * hw + (wm + kbi) % hw;
+            const int kbi = cgi >> 3, cc = cgi & 7, g = cgi / CPG;
             float w8[8], s8[8];
-            load_w8<WT>(w_ring_ptr + st * W_STAGE, row, cc, w8);
-            load_f8(sp + cgi * 8, col0 + cgi * 8 < p.in, s8);
+            load_w8<WT>(stg[kbi], row, cc, w8);
+            lds_f8(reinterpret_cast<const float*>(stg[kbi] + W_TILE) + a * kKB + cc * 8, s8);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) t[cgi * 8 + e] = __fmul_rn(w8[e], s8[e]);
+            for (int e = 0; e < 4; ++e) {
+              const float2 tv =
+                  __fmul2_rn(make_float2(w8[2 * e], w8[2 * e + 1]), make_float2(s8[2 * e], s8[2 * e + 1]));
+              t[cgi * 8 + 2 * e] = tv.x;
+              t[cgi * 8 + 2 * e + 1] = tv.y;
+              if (SYM) {
+                r0[g][e] = fmax3f(r0[g][e], fabsf(tv.x), fabsf(tv.y));
+              } else {
+                r0[g][e] = fmin3f(r0[g][e], tv.x, tv.y);
+                r1[g][e] = fmax3f(r1[g][e], tv.x, tv.y);
+              }
+            }
           }
-          if (a == na - 1) {
-            // the weights are in registers now: hand the W stages back
-            __syncwarp();
-            if (lane == 0)
-              for (int kbi = 0; kbi < KBJ; ++kbi)
-                mbar_arrive(smem_addr(&c.w_empty[wg * hw + (wm + kbi) % hw]));
-          }
-          // group steps (and zero points)
-          float scl[NG], rcp[NG], alo[NG], ahi[NG];
+          // group steps
+          float scl[NG], rcp[NG], chi[NG];
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
             if (SYM) {
-              float m = 0.0f;
-#pragma unroll
-              for (int e = 0; e < G; ++e) m = fmaxf(m, fabsf(t[g * G + e]));
+              const float m = fmaxf(fmaxf(r0[g][0], r0[g][1]), fmaxf(r0[g][2], r0[g][3]));
               scl[g] = fmaxf(__fdiv_rn(m, p.Lf), 1e-8f);
-              alo[g] = ahi[g] = 0.0f;
+              chi[g] = 0.0f;
             } else {
-              float lo = 0.0f, hi = 0.0f;
-#pragma unroll
-              for (int e = 0; e < G; ++e) {
-                lo = fminf(lo, t[g * G + e]);
-                hi = fmaxf(hi, t[g * G + e]);
-              }
+              const float lo = fminf(fminf(r0[g][0], r0[g][1]), fminf(r0[g][2], r0[g][3]));
+              const float hi = fmaxf(fmaxf(r1[g][0], r1[g][1]), fmaxf(r1[g][2], r1[g][3]));
               scl[g] = fmaxf(__fdiv_rn(__fsub_rn(hi, lo), p.maxqf), 1e-8f);
-              const float z = rintf(__fdiv_rn(-lo, scl[g]));
-              alo[g] = kRoundMagic - z;
-              ahi[g] = kRoundMagic + p.maxqf - z;
+              chi[g] = kRoundMagic + p.maxqf - rintf(__fdiv_rn(-lo, scl[g]));
             }
             rcp[g] = __frcp_rn(scl[g]);
           }
-          // pass 2: dW = (q * scale - t) / s (times 2^e_k), fp16 pairs into a tensor memory slot
+          // pass 2: -dW * 2^e as fp16 pairs into a tensor memory slot
+          const bool exact = (exact_mask >> a) & 1u;
 #pragma unroll
           for (int kbi = 0; kbi < KBJ; ++kbi) {
             const uint32_t ds = wg * kBankSlots + dn % kBankSlots;
@@ -452,11 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(FULL, ok);
             if (!ok) break;
             tc_fence_after();
+            const float* inv_row =
+                reinterpret_cast<const float*>(stg[kbi] + W_TILE) + (p.a_per + a) * kKB;
             uint32_t pk[32];
             if (exact)
-              make_dw<SYM, true, G, JC>(t, kbi, ip, col0, p.in, scl, rcp, alo, ahi, pk);
+              make_dw<true, !SYM, G, JC>(t, kbi, inv_row, scl, rcp, chi, pk);
             else
-              make_dw<SYM, false, G, JC>(t, kbi, ip, col0, p.in, scl, rcp, alo, ahi, pk);
+              make_dw<false, false, G, JC>(t, kbi, inv_row, scl, rcp, chi, pk);
             tmem_st32(tmem + lane_addr + kSlotCol0 + ds * 32u, pk);
             tmem_wait_st();
             tc_fence_before();
@@ -465,6 +498,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++dn;
           }
         }
+        if (!ok) break;
+        // every alpha of the job is done with these stages (weights and tables)
+        __syncwarp();
+        if (lane == 0)
+          for (int kbi = 0; kbi < KBJ; ++kbi)
+            mbar_arrive(smem_addr(&c.w_empty[wg * hw + (wm + kbi) % hw]));
         wm += KBJ;
       }
       if (!ok) break;
@@ -541,6 +580,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
+// 2-D map of a row-major matrix, 128-byte swizzled boxes (the MMA operand layout).
 bool make_map(CUtensorMap* m, CUtensorMapDataType t, const void* ptr, uint64_t cols, uint64_t rows,
               uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
   auto enc = get_encode_fn();
@@ -554,7 +594,24 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType t, const void* ptr, uint64_t c
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const SearchArgs);
+// 3-D map over the two float32 scale tables s32 and inv_s32 ([n_alpha][in]
+// each, table_bytes apart): box = 64 columns x a_per alphas x both tables,
+// unswizzled; out-of-range columns and alphas read as zero.
+bool make_scale_map(CUtensorMap* m, const float* s32, uint64_t in, uint64_t n_alpha,
+                    uint64_t table_bytes, uint32_t a_per) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {in, n_alpha, 2};
+  cuuint64_t strides[2] = {in * 4, table_bytes};
+  cuuint32_t box[3] = {(cuuint32_t)kKB, a_per, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(s32), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                          const SearchArgs);
 
 template <typename WT>
 KernelFn pick_g(int group, int sym) {
@@ -596,22 +653,21 @@ SearchPlan plan_search(int dt, int64_t out, int64_t in, int64_t N, int n_alpha, 
   pl.n_units = pl.n_rt * pl.n_ag * pl.n_tt;
   pl.n_tiles = pl.n_rt * pl.n_tt;
   const int kbj = group == 128 ? 2 : 1;
-  const size_t w_stage = (size_t)kRows * kKB * dtype_size(dt);
+  const size_t w_tile = (size_t)kRows * kKB * dtype_size(dt);
+  pl.w_stage = align_up(w_tile + 2 * (size_t)pl.a_per * kKB * 4, 1024);
   const size_t x_stage = (size_t)pl.T * 128;
   const size_t budget = (size_t)max_dyn_smem() - kCtrlBytes - 1024;
-  // deepest W ring (two equal banks of whole jobs) that leaves at least three X stages
+  // deepest W ring (two equal banks, each holding at least one job) that
+  // leaves at least three X stages; then as many X stages as still fit
   pl.sw = 0;
   pl.sx = 0;
-  for (int sw = kMaxSW; sw >= 2 * kbj && pl.sw == 0; sw -= 2 * kbj) {
-    for (int sx = 4; sx >= 3; --sx) {
-      if (sw * w_stage + sx * x_stage <= budget) {
-        pl.sw = sw;
-        pl.sx = sx;
-        break;
-      }
+  for (int sw = kMaxSW; sw >= 2 * kbj && pl.sw == 0; sw -= 2) {
+    if (sw * pl.w_stage + 3 * x_stage <= budget) {
+      pl.sw = sw;
+      pl.sx = (int)std::min<size_t>(kMaxSX, (budget - sw * pl.w_stage) / x_stage);
     }
   }
-  pl.smem = kCtrlBytes + 1024 + pl.sw * w_stage + pl.sx * x_stage;
+  pl.smem = kCtrlBytes + 1024 + pl.sw * pl.w_stage + pl.sx * x_stage;
   pl.grid = std::max(1, std::min(pl.n_units, sms));
   return pl;
 }
@@ -643,17 +699,20 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
       break;
   }
   if (!fn || pl.sw < 2 || pl.sx < 3) return cudaErrorInvalidValue;
-  CUtensorMap mw, mx;
+  const uintptr_t tbl = reinterpret_cast<uintptr_t>(inv_s32) - reinterpret_cast<uintptr_t>(s32);
+  if (inv_s32 <= s32 || (tbl & 15) != 0 || (reinterpret_cast<uintptr_t>(s32) & 15) != 0)
+    return cudaErrorInvalidValue;
+  CUtensorMap mw, mx, ms;
   if (!make_map(&mw, wt, W, (uint64_t)in, (uint64_t)out, (uint64_t)in * dtype_size(dt), wbox, kRows))
     return cudaErrorInvalidValue;
   if (!make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xf16, (uint64_t)in, (uint64_t)N,
                 (uint64_t)in * 2, kKB, (uint32_t)pl.T))
     return cudaErrorInvalidValue;
+  if (!make_scale_map(&ms, s32, (uint64_t)in, (uint64_t)n_alpha, (uint64_t)tbl, (uint32_t)pl.a_per))
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
   SearchArgs a;
-  a.s32 = s32;
-  a.inv_s32 = inv_s32;
   a.pow2_s = pow2_s;
   a.partials = partials;
   a.status = dev_status;
@@ -672,12 +731,13 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
   a.n_tiles = pl.n_tiles;
   a.sw = pl.sw;
   a.sx = pl.sx;
+  a.w_stage = (uint32_t)pl.w_stage;
   a.Lf = (float)((1 << (bits - 1)) - 1);
   a.maxqf = (float)((1 << bits) - 1);
   a.wait_limit_ns = (uint64_t)(wait_limit_ns > 0 ? wait_limit_ns : 2000000000LL);
   a.test_timeout = test_timeout;
   if (ev0 && (e = cudaEventRecord(ev0, s)) != cudaSuccess) return e;
-  fn<<<pl.grid, kThreads, pl.smem, s>>>(mw, mx, a);
+  fn<<<pl.grid, kThreads, pl.smem, s>>>(mw, mx, ms, a);
   e = cudaGetLastError();
   if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
   return e;

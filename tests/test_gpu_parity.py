@@ -232,8 +232,10 @@ def test_search_nonfinite_input(awq):
 
 def test_search_wait_timeout_reports_and_recovers(awq):
     """A wait on a barrier nothing arrives at runs out (50 ms); the kernel
-    returns with AWQ_ERR_TIMEOUT, says where it gave up, and the context
-    stays usable."""
+    returns with AWQ_ERR_TIMEOUT, records a wait site, and the context stays
+    usable.  The unset barrier stalls the whole pipeline, so whichever
+    bounded wait runs out first (the MMA issuer's, or a producer's or
+    loader's waiting behind it) is the one recorded."""
     W, X = make_random_layer(256, 512, 64, dtype="bf16", seed=8)
     Wd, Xd = _dev(W, X)
     diag = torch.zeros(4, dtype=torch.int32, device="cuda")
@@ -245,7 +247,7 @@ def test_search_wait_timeout_reports_and_recovers(awq):
     awq.awq_search(Wd, Xd, 4, 128, True, 20, dev_status=st, opts=opts, check=False)
     torch.cuda.synchronize()
     assert int(st.item()) == 4
-    assert diag[0].item() == 5          # the deliberately unset barrier
+    assert diag[0].item() in (1, 3, 5, 6, 7, 8, 10, 11, 12, 13)   # a known wait site
     check_search(awq, W, X, 4, 128, True, 20, "after timeout")
 
 
