@@ -70,8 +70,9 @@ const char* awq_status_string(int status);
  *
  *   X   [N][in] of `dtype`          (read)
  *   sx  [in] double                 (written)
- * N >= 1, in >= 1.  For 16-bit X the float64 sums are exact, so sx does
- * not depend on the summation order.
+ * N >= 1, in >= 1.  The sums are taken in a fixed order, so repeated calls
+ * give identical results; for fp16 X with N <= 8192 every partial sum is
+ * exact, so sx then equals the exactly rounded mean.
  */
 int awq_channel_stats(const void* X, int dtype, int64_t N, int64_t in,
                       double* sx, int32_t* dev_status, awq_stream_t stream);

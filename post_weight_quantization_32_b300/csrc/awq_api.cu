@@ -24,7 +24,8 @@ constexpr int kMaxGrid = 4096;
 
 // Byte offsets of the workspace regions of awq_search (each 256-aligned).
 struct WsLayout {
-  size_t ctl, pow2, unscale, sx64, s64, minmax, s32, inv_s32, xf16, partials, total;
+  size_t ctl, pow2, unscale, escale, inv_c, sx64, root, minmax, s32, inv_s32, xf16, partials,
+      total;
 };
 
 WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int grid) {
@@ -40,12 +41,14 @@ WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int grid) {
   w.ctl = take(8 * sizeof(uint32_t));  // max|W| and max|X| bits; 4 words of wait diagnostics
   w.pow2 = take((size_t)n_alpha * 4);
   w.unscale = take((size_t)n_alpha * 8);
+  w.escale = take((size_t)n_alpha * 4);
+  w.inv_c = take((size_t)n_alpha * 8);
   w.sx64 = take((size_t)in * 8);
-  w.s64 = take((size_t)n_alpha * in * 8);
-  w.minmax = take((size_t)n_alpha * prep_chunks(in) * 16);
+  w.root = take((size_t)in * 8);                   // s_X ^ (1 / grid)
+  w.minmax = take(prep_chunks(in) * 16);           // per-chunk max and min of s_X
   w.s32 = take((size_t)n_alpha * in * 4);
   w.inv_s32 = take((size_t)n_alpha * in * 4);
-  w.xf16 = take(dt == kDtF16 ? 0 : (size_t)N * in * 2);
+  w.xf16 = take(dt == kDtF16 ? 0 : (size_t)N * in * 2);  // fp16 copy of a bf16/fp32 X
   w.partials = take((size_t)n_alpha * n_tiles * 8);
   w.total = o;
   return w;
@@ -78,7 +81,7 @@ int awq_channel_stats(const void* X, int dtype, int64_t N, int64_t in, double* s
                       int32_t* dev_status, awq_stream_t stream) {
   (void)dev_status;  // no device-side errors in this kernel
   if (!X || !sx || !dtype_ok(dtype) || N < 1 || in < 1) return AWQ_ERR_INVALID_ARG;
-  return cuda_status(launch_channel_stats(X, dtype, N, in, sx, (cudaStream_t)stream));
+  return cuda_status(launch_channel_stats(X, dtype, N, in, sx, nullptr, (cudaStream_t)stream));
 }
 
 size_t awq_search_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N, int group,
@@ -111,32 +114,34 @@ int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t 
   // max|W| and max|X| set the exact power-of-two scalings of the fp16 GEMM operands
   uint32_t* absmax = reinterpret_cast<uint32_t*>(wsb + ws.ctl);
   uint32_t* diag = (opts && opts->diag) ? opts->diag : absmax + 4;
-  int32_t* pow2_s = reinterpret_cast<int32_t*>(wsb + ws.pow2);
   cudaError_t e = cudaMemsetAsync(absmax, 0, 8 * sizeof(uint32_t), s);
   if (e == cudaSuccess && opts && opts->diag)
     e = cudaMemsetAsync(opts->diag, 0, 4 * sizeof(uint32_t), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(pow2_s, 0xFF, (size_t)n_alpha * 4, s);
   if (e == cudaSuccess) e = launch_absmax(W, dtype, out * in, absmax, s);
-  const void* xh = X;
-  if (e == cudaSuccess && dtype != kDtF16) {
-    e = launch_absmax(X, dtype, N * in, absmax + 1, s);
-    if (e == cudaSuccess) e = launch_to_f16(X, dtype, N * in, absmax + 1, wsb + ws.xf16, s);
-    xh = wsb + ws.xf16;
-  }
   if (e != cudaSuccess) return AWQ_ERR_CUDA;
+  // channel statistics; for a bf16 or fp32 X the same pass also finds max|X|,
+  // then X is copied to fp16 (scaled by a power of two) for the tensor cores
+  const bool x_copy = dtype != kDtF16;
   const double* sxp = sx;
   if (!sxp) {
-    e = launch_channel_stats(X, dtype, N, in, reinterpret_cast<double*>(wsb + ws.sx64), s);
-    if (e != cudaSuccess) return AWQ_ERR_CUDA;
+    e = launch_channel_stats(X, dtype, N, in, reinterpret_cast<double*>(wsb + ws.sx64),
+                             x_copy ? absmax + 1 : nullptr, s);
     sxp = reinterpret_cast<const double*>(wsb + ws.sx64);
+  } else if (x_copy) {
+    e = launch_absmax(X, dtype, N * in, absmax + 1, s);
   }
+  if (e == cudaSuccess && x_copy) e = launch_to_f16(X, dtype, N * in, absmax + 1, wsb + ws.xf16, s);
+  if (e != cudaSuccess) return AWQ_ERR_CUDA;
+  const void* xh = x_copy ? static_cast<const void*>(wsb + ws.xf16) : X;
+  int32_t* pow2_s = reinterpret_cast<int32_t*>(wsb + ws.pow2);
   float* s32 = reinterpret_cast<float*>(wsb + ws.s32);
   float* inv_s32 = reinterpret_cast<float*>(wsb + ws.inv_s32);
   double* unscale = reinterpret_cast<double*>(wsb + ws.unscale);
-  e = launch_alpha_prep(sxp, in, grid, absmax, dtype != kDtF16 ? 1 : 0,
-                        reinterpret_cast<double*>(wsb + ws.s64),
-                        reinterpret_cast<double*>(wsb + ws.minmax), s32, inv_s32, unscale, pow2_s,
-                        s);
+  e = launch_alpha_prep(sxp, in, grid, absmax, x_copy ? 1 : 0,
+                        reinterpret_cast<double*>(wsb + ws.root),
+                        reinterpret_cast<double*>(wsb + ws.minmax),
+                        reinterpret_cast<double*>(wsb + ws.inv_c),
+                        reinterpret_cast<float*>(wsb + ws.escale), s32, inv_s32, unscale, pow2_s, s);
   if (e != cudaSuccess) return AWQ_ERR_CUDA;
 
   const SearchPlan pl = plan_search(dtype, out, in, N, n_alpha, group, device_sm_count());

@@ -16,9 +16,11 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int device_sm_count();
 
 // ---- statistics and conversions (awq_stats.cu)
-// sx[j] = sum_n |X[n, j]| / N + 1e-8, float64.
+// sx[j] = sum_n |X[n, j]| / N + 1e-8, float64.  With xmax != nullptr the same
+// pass folds max|X| into *xmax (the bits of a non-negative float; *xmax must
+// start at 0; needs in % 8 == 0 and X 16-byte aligned).
 cudaError_t launch_channel_stats(const void* X, int dt, int64_t N, int64_t in, double* sx,
-                                 cudaStream_t s);
+                                 uint32_t* xmax, cudaStream_t s);
 // *out = max(*out, bits of max_i |p[i]|); *out must start at 0.
 cudaError_t launch_absmax(const void* p, int dt, int64_t n, uint32_t* out, cudaStream_t s);
 // dst = fp16(X * 2^m) with m = pow2_exponent_for(max|X|) read from *xmax_bits;
@@ -32,13 +34,15 @@ cudaError_t launch_to_f16(const void* X, int dt, int64_t n, const uint32_t* xmax
 // weight changes of alpha k into the fp16 range of the error GEMM
 // (absmax[0] = max|W| bits).  unscale[k] = 2^-2(e_k + m_x) undoes both
 // operand scalings on the squared sums (absmax[1] = max|X| bits; m_x = 0
-// when x_scaled == 0).  pow2_s[k] (set to all ones beforehand) ends nonzero
-// iff every s32[k][j] is a power of two.  s64 holds the powers and
-// minmax[k][c] the per-chunk (max, min) between the two kernels.
+// when x_scaled == 0).  pow2_s[k] ends nonzero iff every s32[k][j] is a
+// power of two.  root ([in] doubles) holds sx^(1/grid), minmax
+// (prep_chunks(in) pairs) the per-chunk max and min of sx, inv_c and escale
+// ([grid + 1] each) the centring factors and 2^e_k.
 size_t prep_chunks(int64_t in);
 cudaError_t launch_alpha_prep(const double* sx, int64_t in, int grid, const uint32_t* absmax,
-                              int x_scaled, double* s64, double* minmax, float* s32,
-                              float* inv_s32, double* unscale, int32_t* pow2_s, cudaStream_t s);
+                              int x_scaled, double* root, double* minmax, double* inv_c,
+                              float* escale, float* s32, float* inv_s32, double* unscale,
+                              int32_t* pow2_s, cudaStream_t s);
 // err[k] = unscale[k] * sum_t partials[k][t] / denom (fixed order),
 // best = strict-< argmin, s_best = s32[best].
 cudaError_t launch_reduce_argmin(const double* partials, const double* unscale, int n_alpha,

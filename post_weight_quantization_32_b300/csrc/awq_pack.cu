@@ -31,37 +31,41 @@ struct QParams {
   int sym;
 };
 
-// round(t / scale) with the exact-division fallback near ties.
-__device__ __forceinline__ float round_quotient(float t, float scale, float rcp) {
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+
+// round(t / scale) as an integer.  r = t * (1/scale) is rounded to the
+// nearest integer (ties to even) by adding and subtracting 1.5 * 2^23, exact
+// for |r| < 2^22, and the integer is read off the bits of r + 1.5 * 2^23.
+// Where r lies within 2^-21 (relative) of a half-integer the correctly
+// rounded quotient is formed by true division instead, so the result is
+// that of rounding fl32(t / scale).
+__device__ __forceinline__ int round_quotient(float t, float scale, float rcp) {
   const float r = __fmul_rn(t, rcp);
-  const float k = rintf(r);
+  const float rm = __fadd_rn(r, kMagic);
+  const float k = __fsub_rn(rm, kMagic);
   const float fr = fabsf(__fsub_rn(r, k));
   if (fabsf(__fsub_rn(fr, 0.5f)) <= __fmul_rn(fabsf(r), 4.76837158203125e-7f))  // 2^-21
-    return rintf(__fdiv_rn(t, scale));
-  return k;
+    return (int)rintf(__fdiv_rn(t, scale));
+  return __float_as_int(rm) - __float_as_int(kMagic);
 }
 
 __device__ __forceinline__ void group_params_sym(float m, const QParams& qp, float& scale,
-                                                 float& zero) {
+                                                 int& zero) {
   scale = fmaxf(__fdiv_rn(m, qp.Lf), 1e-8f);
-  zero = 0.0f;
+  zero = 1 << (qp.bits - 1);
 }
 __device__ __forceinline__ void group_params_asym(float lo, float hi, const QParams& qp,
-                                                  float& scale, float& zero) {
+                                                  float& scale, int& zero) {
   scale = fmaxf(__fdiv_rn(__fsub_rn(hi, lo), qp.maxqf), 1e-8f);
-  zero = rintf(__fdiv_rn(-lo, scale));
+  zero = (int)rintf(__fdiv_rn(-lo, scale));
 }
 
-// Unsigned storage code of one value.
-__device__ __forceinline__ uint32_t code_of(float t, float scale, float rcp, float zero,
-                                            const QParams& qp) {
-  const float q = round_quotient(t, scale, rcp);
-  if (qp.sym) {
-    const float c = fminf(fmaxf(q, -qp.Lf - 1.0f), qp.Lf);
-    return (uint32_t)((int)c + (1 << (qp.bits - 1)));
-  }
-  const float c = fminf(fmaxf(__fadd_rn(q, zero), 0.0f), qp.maxqf);
-  return (uint32_t)(int)c;
+// Unsigned storage code of one value: symmetric q + 2^(b-1) with q clamped
+// to [-2^(b-1), 2^(b-1) - 1]; asymmetric q + zero clamped to [0, 2^b - 1].
+// Both are clamp(q + zero, lo, hi) with (lo, hi) = (0, 2^b - 1).
+__device__ __forceinline__ uint32_t code_of(float t, float scale, float rcp, int zero, int maxq) {
+  const int q = round_quotient(t, scale, rcp) + zero;
+  return (uint32_t)min(max(q, 0), maxq);
 }
 
 // Fast path: group = 8 * LPG columns, LPG lanes per group (a power of two
@@ -101,7 +105,8 @@ __global__ void __launch_bounds__(256) pack_warp_kernel(const T* __restrict__ W,
       for (int e = 0; e < 8; ++e) t[e] = 0.0f;
     }
     if (__any_sync(0xffffffffu, nan) && lane == 0) set_status(dev_status, ST_NONFINITE);
-    float scale, zero;
+    float scale;
+    int zero;
     if (qp.sym) {
       float m = 0.0f;
 #pragma unroll
@@ -124,15 +129,16 @@ __global__ void __launch_bounds__(256) pack_warp_kernel(const T* __restrict__ W,
       group_params_asym(lo, hi, qp, scale, zero);
     }
     const float rcp = __frcp_rn(scale);
+    const int maxq = (1 << bits) - 1;
     uint64_t chunk = 0;
     if (valid) {
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        chunk |= (uint64_t)code_of(t[e], scale, rcp, zero, qp) << (e * bits);
+        chunk |= (uint64_t)code_of(t[e], scale, rcp, zero, maxq) << (e * bits);
       if ((lane & (LPG - 1)) == 0) {
         const int64_t g = c0 / (8 * LPG);
         scales[row * ngroups + g] = scale;
-        zeros[row * ngroups + g] = qp.sym ? (uint8_t)(1 << (bits - 1)) : (uint8_t)(int)zero;
+        zeros[row * ngroups + g] = (uint8_t)zero;
       }
     }
     // word k of this segment (8*b words) covers bits [32k, 32k + 32): at most two lanes
@@ -187,19 +193,21 @@ __global__ void __launch_bounds__(256) pack_general_kernel(const T* __restrict__
       hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
     }
     if (__any_sync(0xffffffffu, nan) && lane == 0) set_status(dev_status, ST_NONFINITE);
-    float scale, zero;
+    float scale;
+    int zero;
     if (qp.sym)
       group_params_sym(m, qp, scale, zero);
     else
       group_params_asym(lo, hi, qp, scale, zero);
     const float rcp = __frcp_rn(scale);
+    const int maxq = (1 << qp.bits) - 1;
     if (lane == 0) {
       scales[row * ngroups + g] = scale;
-      zeros[row * ngroups + g] = qp.sym ? (uint8_t)(1 << (qp.bits - 1)) : (uint8_t)(int)zero;
+      zeros[row * ngroups + g] = (uint8_t)zero;
     }
     for (int j = lane; j < group; j += 32) {
       const float t = __fmul_rn(Elt<T>::to_f32(wr[j]), sr[j]);
-      const uint32_t u = code_of(t, scale, rcp, zero, qp);
+      const uint32_t u = code_of(t, scale, rcp, zero, maxq);
       const int64_t bit = (g * group + j) * (int64_t)qp.bits;
       const int64_t wi = bit >> 5;
       const int sh = (int)(bit & 31);

@@ -1,11 +1,10 @@
 // Channel statistics s_X[j] = mean_n |X[n, j]| + 1e-8 ("AWQ (activation-aware
 // weight quantization)", "How it works" step 1), the max |.| reductions that
 // set the power-of-two operand scalings, and the fp16 copy of X that the
-// tensor-core error GEMM reads.
+// tensor-core error GEMM reads when X is not fp16 already.
 //
-// All three are HBM-bound passes.  The statistic is accumulated in float64
-// in a fixed order; for 16-bit inputs every partial sum is exact, so the
-// result does not depend on that order at all.
+// All are HBM-bound passes.  The statistic is accumulated in float64 in a
+// fixed order, so repeated calls give identical results.
 #include <algorithm>
 
 #include "awq_device.cuh"
@@ -15,30 +14,67 @@ namespace awq {
 
 namespace {
 
-constexpr int kStatCols = 64;    // columns per CTA (8 lanes x 8 columns)
-constexpr int kStatSlices = 32;  // row slices per CTA
+constexpr int kStatCols = 32;    // columns per CTA of the vector path (4 lanes x 8 columns)
+constexpr int kStatSlices = 64;  // row slices per CTA of the vector path
+constexpr int kScalarCols = 64;  // columns per CTA of the scalar path
+
+// max(|v|) over a CTA as the bit pattern of a non-negative float, folded into
+// *out with one atomicMax (the integer order of such patterns is the float
+// order, so the result does not depend on the order of the CTAs).  NaN is
+// ignored.
+__device__ __forceinline__ void block_absmax(float m, uint32_t* out) {
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float wm[32];
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, wm[w]);
+    atomicMax(out, __float_as_uint(m));
+  }
+}
 
 // Vector path: in % 8 == 0 and 16-byte aligned rows.  Thread (c, r) sums the
-// 8 columns c*8..c*8+7 of the CTA's 64 over rows r, r+32, r+64, ...
+// 8 columns c*8..c*8+7 of the CTA's 32 over rows r, r+64, r+128, ..., four
+// 16-byte loads in flight at a time; the 64 slices are then added in a fixed
+// order.  With xmax != nullptr the pass also folds max|X| into *xmax.
 template <typename T>
 __global__ void __launch_bounds__(256) stats_vec_kernel(const T* __restrict__ X, int64_t N,
-                                                        int64_t in, double* __restrict__ sx) {
+                                                        int64_t in, double* __restrict__ sx,
+                                                        uint32_t* __restrict__ xmax) {
   __shared__ double red[kStatSlices][kStatCols + 1];
-  const int c = threadIdx.x % 8, r = threadIdx.x / 8;
+  const int c = threadIdx.x % 4, r = threadIdx.x / 4;
   const int64_t col0 = (int64_t)blockIdx.x * kStatCols + c * 8;
   double acc[8];
+  float m = 0.0f;
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.0;
   if (col0 < in) {
-    for (int64_t n = r; n < N; n += kStatSlices) {
+    int64_t n = r;
+    for (; n + 3 * kStatSlices < N; n += 4 * kStatSlices) {
+      float v[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) load8_f32<T>(X + (n + u * kStatSlices) * in + col0, v[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc[e] += (double)fabsf(v[u][e]);
+          m = fmaxf(m, fabsf(v[u][e]));
+        }
+    }
+    for (; n < N; n += kStatSlices) {
       float v[8];
       load8_f32<T>(X + n * in + col0, v);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += (double)fabsf(v[e]);
+      for (int e = 0; e < 8; ++e) {
+        acc[e] += (double)fabsf(v[e]);
+        m = fmaxf(m, fabsf(v[e]));
+      }
     }
   }
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[r][c * 8 + e] = acc[e];
+  if (xmax != nullptr) block_absmax(m, xmax);  // contains __syncthreads
   __syncthreads();
   if (threadIdx.x < kStatCols) {
     const int64_t j = (int64_t)blockIdx.x * kStatCols + threadIdx.x;
@@ -54,9 +90,9 @@ __global__ void __launch_bounds__(256) stats_vec_kernel(const T* __restrict__ X,
 template <typename T>
 __global__ void __launch_bounds__(256) stats_scalar_kernel(const T* __restrict__ X, int64_t N,
                                                            int64_t in, double* __restrict__ sx) {
-  __shared__ double red[4][kStatCols];
-  const int c = threadIdx.x % kStatCols, r = threadIdx.x / kStatCols;
-  const int64_t j = (int64_t)blockIdx.x * kStatCols + c;
+  __shared__ double red[4][kScalarCols];
+  const int c = threadIdx.x % kScalarCols, r = threadIdx.x / kScalarCols;
+  const int64_t j = (int64_t)blockIdx.x * kScalarCols + c;
   double acc = 0.0;
   if (j < in)
     for (int64_t n = r; n < N; n += 4) acc += (double)fabsf(Elt<T>::to_f32(X[n * in + j]));
@@ -66,9 +102,8 @@ __global__ void __launch_bounds__(256) stats_scalar_kernel(const T* __restrict__
     sx[j] = (((red[0][c] + red[1][c]) + red[2][c]) + red[3][c]) / (double)N + 1e-8;
 }
 
-// max |x| over n values as the bit pattern of a non-negative float (the
-// integer order of such patterns is the float order), combined across CTAs
-// with atomicMax: order-independent, so deterministic.  NaN is ignored.
+// max |x| over n values into *out (see block_absmax), four 16-byte loads in
+// flight per thread.
 template <typename T>
 __global__ void __launch_bounds__(256) absmax_kernel(const T* __restrict__ p, int64_t n, bool vec,
                                                      uint32_t* __restrict__ out) {
@@ -76,7 +111,18 @@ __global__ void __launch_bounds__(256) absmax_kernel(const T* __restrict__ p, in
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (vec) {
-    for (int64_t i = i0; i < n / 8; i += stride) {
+    const int64_t n8 = n / 8;
+    int64_t i = i0;
+    for (; i + 3 * stride < n8; i += 4 * stride) {
+      float v[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) load8_f32<T>(p + (i + u * stride) * 8, v[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[u][e]));
+    }
+    for (; i < n8; i += stride) {
       float v[8];
       load8_f32<T>(p + i * 8, v);
 #pragma unroll
@@ -85,8 +131,7 @@ __global__ void __launch_bounds__(256) absmax_kernel(const T* __restrict__ p, in
   } else {
     for (int64_t i = i0; i < n; i += stride) m = fmaxf(m, fabsf(Elt<T>::to_f32(p[i])));
   }
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(m));
+  block_absmax(m, out);
 }
 
 // dst = fp16(X * 2^m), m from max|X| (pow2_exponent_for): an exact
@@ -111,30 +156,34 @@ __global__ void __launch_bounds__(256) to_f16_kernel(const T* __restrict__ X, in
 }
 
 template <typename T>
-cudaError_t stats_dispatch(const void* X, int64_t N, int64_t in, double* sx, cudaStream_t s) {
+cudaError_t stats_dispatch(const void* X, int64_t N, int64_t in, double* sx, uint32_t* xmax,
+                           cudaStream_t s) {
   const bool vec = (in % 8 == 0) && ((reinterpret_cast<uintptr_t>(X) & 15) == 0);
-  const unsigned grid = (unsigned)((in + kStatCols - 1) / kStatCols);
-  if (vec)
-    stats_vec_kernel<T><<<grid, 256, 0, s>>>(static_cast<const T*>(X), N, in, sx);
-  else
-    stats_scalar_kernel<T><<<grid, 256, 0, s>>>(static_cast<const T*>(X), N, in, sx);
+  if (vec) {
+    stats_vec_kernel<T><<<(unsigned)((in + kStatCols - 1) / kStatCols), 256, 0, s>>>(
+        static_cast<const T*>(X), N, in, sx, xmax);
+  } else {
+    if (xmax != nullptr) return cudaErrorInvalidValue;
+    stats_scalar_kernel<T><<<(unsigned)((in + kScalarCols - 1) / kScalarCols), 256, 0, s>>>(
+        static_cast<const T*>(X), N, in, sx);
+  }
   return cudaGetLastError();
 }
 
 unsigned grid_for(int64_t work) {
   const int64_t want = (work + 255) / 256;
-  const int64_t cap = (int64_t)device_sm_count() * 8;
+  const int64_t cap = (int64_t)device_sm_count() * 4;
   return (unsigned)std::max<int64_t>(1, std::min(want, cap));
 }
 
 }  // namespace
 
 cudaError_t launch_channel_stats(const void* X, int dt, int64_t N, int64_t in, double* sx,
-                                 cudaStream_t s) {
+                                 uint32_t* xmax, cudaStream_t s) {
   switch (dt) {
-    case kDtF32: return stats_dispatch<float>(X, N, in, sx, s);
-    case kDtF16: return stats_dispatch<__half>(X, N, in, sx, s);
-    default: return stats_dispatch<__nv_bfloat16>(X, N, in, sx, s);
+    case kDtF32: return stats_dispatch<float>(X, N, in, sx, xmax, s);
+    case kDtF16: return stats_dispatch<__half>(X, N, in, sx, xmax, s);
+    default: return stats_dispatch<__nv_bfloat16>(X, N, in, sx, xmax, s);
   }
 }
 

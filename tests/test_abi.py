@@ -64,11 +64,12 @@ def _ws(lib, *a):
 
 
 def test_workspace_query(lib):
-    # fp16 notebook-shaped layer: no copy of X, tables for 21 alphas
+    # fp16 notebook-shaped layer: X is read in place; s and 1/s tables for 21 alphas
     n = _ws(lib, 1, 4096, 4096, 256, 128, 20)
-    assert n >= 21 * 4096 * (8 + 4 + 4) and n % 256 == 0
-    # bf16 and fp32 add the fp16 copy of X
+    assert n >= 21 * 4096 * (4 + 4) and n % 256 == 0
+    # bf16 and fp32 add the fp16 copy of X the tensor cores read
     assert _ws(lib, 2, 4096, 4096, 256, 128, 20) >= n + 256 * 4096 * 2
+    assert _ws(lib, 0, 4096, 4096, 256, 128, 20) >= n + 256 * 4096 * 2
     assert _ws(lib, 2, 4096, 4096, 256, 100, 20) == 0      # group does not divide in
     assert _ws(lib, 2, 0, 4096, 256, 128, 20) == 0
     assert _ws(lib, 7, 16, 16, 16, 16, 20) == 0
