@@ -40,10 +40,11 @@ def _deps_mtime() -> float:
 
 
 # The search kernels split their registers between warpgroups with
-# setmaxnreg (128 threads x 56 + 256 threads x 216); that split must fit in
-# what the block is launched with, so every search kernel has to be compiled
-# to the full 168 registers a thread that its launch bounds allow.
-SEARCH_KERNEL_REGS = 168
+# setmaxnreg (128 threads x 48 + 256 threads x 200 + 128 threads x 56); that
+# split must fit in what the block is launched with, so every search kernel
+# has to be compiled to the full 128 registers a thread that its launch
+# bounds allow.
+SEARCH_KERNEL_REGS = 128
 
 
 def _check_registers(src: str, text: str) -> None:

@@ -7,23 +7,26 @@
 //
 // Work unit = (128-row tile of W, a group of up to 8 alphas, a token tile of
 // T <= 256 tokens).  One persistent CTA per SM walks a static list of units.
-// Warp roles inside a CTA (384 threads, three warpgroups):
-//   warpgroup 0 (56 registers a thread after setmaxnreg):
+// Warp roles inside a CTA (512 threads, four warpgroups):
+//   warpgroup 0 (48 registers a thread after setmaxnreg):
 //     warp 0    TMA loads of W blocks (128 rows x 64 columns) together with
 //               the matching 64 columns of the s and 2^e/s tables of the
 //               unit's alphas, into one ring stage
 //     warp 1    TMA loads of X blocks (T tokens x 64 columns, fp16)
 //     warp 2    tensor memory owner and the single tcgen05.mma issuer
 //     warp 3    idle
-//   warpgroups 1 and 2 (216 registers a thread): producers, thread = one W
+//   warpgroups 1 and 2 (200 registers a thread): producers, thread = one W
 //     row.  Per 128-column job (one quantization group for group 128) and
 //     alpha, pass 1 forms t = w * s in registers and the group's range;
 //     pass 2 rounds t to the group's grid and writes -dW (fp16; the sign
 //     does not change the squared error) straight into tensor memory,
-//     where the MMA reads it as operand A.  After the last K block they
-//     read the fp32 accumulators (128 rows x T tokens per alpha) back,
-//     square and sum them.  Warpgroup 1 takes the even jobs of a unit,
-//     warpgroup 2 the odd ones, each with its own ring bank and dW slots.
+//     where the MMA reads it as operand A.  Warpgroup 1 takes the even jobs
+//     of a unit, warpgroup 2 the odd ones, each with its own ring bank and
+//     dW slots; they run on into the next unit while the last MMAs of a
+//     unit drain.
+//   warpgroup 3 (56 registers a thread): epilogue.  After a unit's last MMA
+//     it reads the fp32 accumulators (128 rows x T tokens per alpha) back,
+//     squares and sums them, and frees the accumulator for the next unit.
 // Tensor memory (512 columns): columns [0, 256) hold a_per accumulators of
 // T columns; columns [256, 512) are eight 32-column slots of dW (64 fp16
 // values per row each), four per producer warpgroup.  X is the MMA's B
@@ -76,7 +79,7 @@ namespace awq {
 
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kRows = 128;       // MMA M: weight rows per tile
 constexpr int kKB = 64;          // K columns per block: one 128-byte fp16 swizzle row
 constexpr int kBankSlots = 4;    // dW slots in tensor memory per producer warpgroup
@@ -85,12 +88,14 @@ constexpr int kMaxSW = 8, kMaxSX = 8, kMaxAPer = 8;
 constexpr uint32_t kSlotCol0 = 256;
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: fma(x, r, M) - M = rint(x * r)
 constexpr uint32_t kCtrlBytes = 1024;
-// Register split after setmaxnreg: 128 * 56 + 256 * 216 = 62464 must not
-// exceed the 384 * 168 = 64512 registers the block is launched with (the
-// build checks that every search kernel is compiled to 168 registers).
-constexpr uint32_t kRegsCtl = 56, kRegsProd = 216;
-constexpr uint32_t kLaunchRegs = 168;
-static_assert(128 * kRegsCtl + 256 * kRegsProd <= kThreads * kLaunchRegs, "register split");
+// Register split after setmaxnreg: 128 * 48 + 256 * 200 + 128 * 56 = 64512
+// must not exceed the 512 * 128 = 65536 registers the block is launched
+// with (the build checks that every search kernel is compiled to 128
+// registers).
+constexpr uint32_t kRegsCtl = 48, kRegsProd = 200, kRegsEpi = 56;
+constexpr uint32_t kLaunchRegs = 128;
+static_assert(128 * kRegsCtl + 256 * kRegsProd + 128 * kRegsEpi <= kThreads * kLaunchRegs,
+              "register split");
 
 struct SearchArgs {
   const int32_t* pow2_s;  // [n_alpha]: nonzero when every scale of that alpha is a power of two
@@ -113,7 +118,7 @@ struct Ctrl {
   uint64_t acc_full, acc_empty, epi_full, never, drain;
   uint32_t tmem_base;
   int abort;
-  float epi[2][kMaxAPer][8];
+  float epi[2][kMaxAPer][4];
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
@@ -260,8 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&c.d_empty[i]), 1);
     }
     mbar_init(smem_addr(&c.acc_full), 1);
-    mbar_init(smem_addr(&c.acc_empty), 8);
-    mbar_init(smem_addr(&c.epi_full), 8);
+    mbar_init(smem_addr(&c.acc_empty), 4);
+    mbar_init(smem_addr(&c.epi_full), 4);
     mbar_init(smem_addr(&c.never), 1);
     mbar_init(smem_addr(&c.drain), 1);
     c.abort = 0;
@@ -400,18 +405,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       int never_set = 0;
       mbar_wait(smem_addr(&c.drain), 0, &never_set, lim);
     }
-  } else {
-    // ------------------------------------------------------------ producers + epilogue
+  } else if (warp < 12) {
+    // ------------------------------------------------------------ producers
     setmaxnreg_inc<kRegsProd>();
     const int wg = (warp - 4) >> 2;
     const int q = warp & 3;  // tensor memory lanes 32q .. 32q+31
     const int row = q * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-    uint32_t wm = 0, dn = 0, useq = 0;  // this warpgroup's W-block and dW-slot counters
+    uint32_t wm = 0, dn = 0;  // this warpgroup's W-block and dW-slot counters
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       const int rem = u % units_per_rt;
-      const int rt = u / units_per_rt, ag = rem / p.n_tt, tt = rem % p.n_tt;
+      const int ag = rem / p.n_tt;
       const int na = min(p.a_per, p.n_alpha - ag * p.a_per);
       uint32_t exact_mask = 0;
       for (int a = 0; a < na; ++a)
@@ -506,17 +511,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(smem_addr(&c.w_empty[wg * hw + (wm + kbi) % hw]));
         wm += KBJ;
       }
-      if (!ok) break;
-      // epilogue: sum of squares of this unit's accumulators
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // warp 12 + q reads tensor memory lanes 32q .. 32q+31 (rows of the tile)
+    // once the unit's MMAs are done, squares and sums the accumulators, and
+    // hands the accumulator back; the producers meanwhile run on into the
+    // next unit.
+    setmaxnreg_dec<kRegsEpi>();
+    const int q = warp & 3;
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    uint32_t useq = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      const int rem = u % units_per_rt;
+      const int rt = u / units_per_rt, ag = rem / p.n_tt, tt = rem % p.n_tt;
+      const int na = min(p.a_per, p.n_alpha - ag * p.a_per);
       ok = mbar_wait(smem_addr(&c.acc_full), useq & 1, abort, lim, p.diag, 12, useq);
       ok = __all_sync(FULL, ok);
       if (!ok) break;
       tc_fence_after();
-      const int half = p.T >> 1;
       for (int a = 0; a < na; ++a) {
         float acc = 0.0f;
-        const uint32_t cb = tmem + lane_addr + (uint32_t)(a * p.T + wg * half);
-        for (int cc = 0; cc < half; cc += 16) {
+        const uint32_t cb = tmem + lane_addr + (uint32_t)(a * p.T);
+        for (int cc = 0; cc < p.T; cc += 16) {
           uint32_t v[16];
           tmem_ld16(cb + (uint32_t)cc, v);
           tmem_wait_ld();
@@ -528,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(FULL, acc, o);
-        if (lane == 0) c.epi[useq & 1][a][warp - 4] = acc;
+        if (lane == 0) c.epi[useq & 1][a][q] = acc;
       }
       tc_fence_before();
       __syncwarp();
@@ -536,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(smem_addr(&c.acc_empty));
         mbar_arrive(smem_addr(&c.epi_full));
       }
-      if (warp == 4) {
+      if (warp == 12) {
         bool ok2 = true;
         if (lane == 0) ok2 = mbar_wait(smem_addr(&c.epi_full), useq & 1, abort, lim, p.diag, 13, useq);
         __syncwarp();
@@ -547,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane < na) {
           double s = 0.0;
-          for (int w = 0; w < 8; ++w) s += (double)c.epi[useq & 1][lane][w];
+          for (int w = 0; w < 4; ++w) s += (double)c.epi[useq & 1][lane][w];
           p.partials[(size_t)(ag * p.a_per + lane) * p.n_tiles + rt * p.n_tt + tt] = s;
         }
       }
