@@ -279,7 +279,7 @@ def main():
     e2e_v = n_alpha * world / (r["e2e_ms"] * 1e-3)
     achieved = flops / (r["search_ms"] * 1e-3) / 1e12
     cpu_t, cpu_n = run_oracle_sample(cfg, args.cpu_sample)
-    launches_per_step = 7 + (0 if cfg.dtype == "f16" else 2)
+    launches_per_step = 6 + (0 if cfg.dtype == "f16" else 1)
     line = {
         "metric": METRIC, "value": value, "unit": "layer-alpha-evals/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],

@@ -71,8 +71,9 @@ const char* awq_status_string(int status);
  *   X   [N][in] of `dtype`          (read)
  *   sx  [in] double                 (written)
  * N >= 1, in >= 1.  The sums are taken in a fixed order, so repeated calls
- * give identical results; for fp16 X with N <= 8192 every partial sum is
- * exact, so sx then equals the exactly rounded mean.
+ * give identical results.  For fp16 X (with 8 | in and X 16-byte aligned)
+ * the column sum is formed exactly, as an integer multiple of 2^-24, so sx
+ * then equals the correctly rounded float64 mean plus 1e-8.
  */
 int awq_channel_stats(const void* X, int dtype, int64_t N, int64_t in,
                       double* sx, int32_t* dev_status, awq_stream_t stream);
@@ -168,8 +169,9 @@ int awq_search_ex(const void* W, const void* X, int dtype,
  * Arithmetic is IEEE float32 with round-to-nearest on every operation and
  * round-half-to-even for the codes: t = w*s, scale = max(m/L, 1e-8) or
  * max((hi-lo)/maxq, 1e-8), code = round(t/scale) (+ zero, clamped).
- * Any group size dividing `in` is accepted.  A NaN product w*s sets
- * AWQ_ERR_NONFINITE.
+ * Any group size dividing `in` is accepted.  A NaN or infinite product w*s
+ * sets AWQ_ERR_NONFINITE; the codes, scale and zero of its group are then
+ * unspecified (codes stay within [0, 2^b - 1]).
  */
 int awq_quantize_pack(const void* W, int dtype, int64_t out, int64_t in,
                       const float* s, int bits, int group, int sym,

@@ -38,14 +38,14 @@ WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int grid) {
     o = align_up(o + bytes, 256);
     return at;
   };
-  w.ctl = take(8 * sizeof(uint32_t));  // max|W| and max|X| bits; 4 words of wait diagnostics
+  w.ctl = take(8 * sizeof(uint32_t));  // max|W|, max|X| bits, a ticket; 4 words of wait diagnostics
   w.pow2 = take((size_t)n_alpha * 4);
   w.unscale = take((size_t)n_alpha * 8);
   w.escale = take((size_t)n_alpha * 4);
   w.inv_c = take((size_t)n_alpha * 8);
   w.sx64 = take((size_t)in * 8);
   w.root = take((size_t)in * 8);                   // s_X ^ (1 / grid)
-  w.minmax = take(prep_chunks(in) * 16);           // per-chunk max and min of s_X
+  w.minmax = take(prep_chunks(in) * 32);           // per-chunk extremes of s_X with their roots
   w.s32 = take((size_t)n_alpha * in * 4);
   w.inv_s32 = take((size_t)n_alpha * in * 4);
   w.xf16 = take(dt == kDtF16 ? 0 : (size_t)N * in * 2);  // fp16 copy of a bf16/fp32 X
@@ -81,7 +81,9 @@ int awq_channel_stats(const void* X, int dtype, int64_t N, int64_t in, double* s
                       int32_t* dev_status, awq_stream_t stream) {
   (void)dev_status;  // no device-side errors in this kernel
   if (!X || !sx || !dtype_ok(dtype) || N < 1 || in < 1) return AWQ_ERR_INVALID_ARG;
-  return cuda_status(launch_channel_stats(X, dtype, N, in, sx, nullptr, (cudaStream_t)stream));
+  return cuda_status(
+      launch_channel_stats(X, dtype, N, in, sx, nullptr, nullptr, 0, nullptr, CentreArgs{},
+                           (cudaStream_t)stream));
 }
 
 size_t awq_search_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N, int group,
@@ -117,32 +119,42 @@ int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t 
   cudaError_t e = cudaMemsetAsync(absmax, 0, 8 * sizeof(uint32_t), s);
   if (e == cudaSuccess && opts && opts->diag)
     e = cudaMemsetAsync(opts->diag, 0, 4 * sizeof(uint32_t), s);
-  if (e == cudaSuccess) e = launch_absmax(W, dtype, out * in, absmax, s);
   if (e != cudaSuccess) return AWQ_ERR_CUDA;
-  // channel statistics; for a bf16 or fp32 X the same pass also finds max|X|,
-  // then X is copied to fp16 (scaled by a power of two) for the tensor cores
-  const bool x_copy = dtype != kDtF16;
-  const double* sxp = sx;
-  if (!sxp) {
-    e = launch_channel_stats(X, dtype, N, in, reinterpret_cast<double*>(wsb + ws.sx64),
-                             x_copy ? absmax + 1 : nullptr, s);
-    sxp = reinterpret_cast<const double*>(wsb + ws.sx64);
-  } else if (x_copy) {
-    e = launch_absmax(X, dtype, N * in, absmax + 1, s);
-  }
-  if (e == cudaSuccess && x_copy) e = launch_to_f16(X, dtype, N * in, absmax + 1, wsb + ws.xf16, s);
-  if (e != cudaSuccess) return AWQ_ERR_CUDA;
-  const void* xh = x_copy ? static_cast<const void*>(wsb + ws.xf16) : X;
   int32_t* pow2_s = reinterpret_cast<int32_t*>(wsb + ws.pow2);
   float* s32 = reinterpret_cast<float*>(wsb + ws.s32);
   float* inv_s32 = reinterpret_cast<float*>(wsb + ws.inv_s32);
   double* unscale = reinterpret_cast<double*>(wsb + ws.unscale);
-  e = launch_alpha_prep(sxp, in, grid, absmax, x_copy ? 1 : 0,
-                        reinterpret_cast<double*>(wsb + ws.root),
-                        reinterpret_cast<double*>(wsb + ws.minmax),
-                        reinterpret_cast<double*>(wsb + ws.inv_c),
-                        reinterpret_cast<float*>(wsb + ws.escale), s32, inv_s32, unscale, pow2_s, s);
+  const bool x_copy = dtype != kDtF16;
+  CentreArgs ca{};
+  ca.grid = grid;
+  ca.x_scaled = x_copy ? 1 : 0;
+  ca.root = reinterpret_cast<double*>(wsb + ws.root);
+  ca.minmax = reinterpret_cast<double*>(wsb + ws.minmax);
+  ca.ticket = absmax + 2;
+  ca.absmax = absmax;
+  ca.inv_c = reinterpret_cast<double*>(wsb + ws.inv_c);
+  ca.escale = reinterpret_cast<float*>(wsb + ws.escale);
+  ca.unscale = unscale;
+  ca.pow2_s = pow2_s;
+  // One launch: channel statistics, max|W| (and max|X| for a bf16 or fp32
+  // X), sx^(1/grid) and, in its last CTA, the per-alpha centring values.
+  // Then a bf16 / fp32 X is copied to fp16 (scaled by a power of two) for
+  // the tensor cores.
+  const double* sxp = sx;
+  if (!sxp) {
+    e = launch_channel_stats(X, dtype, N, in, reinterpret_cast<double*>(wsb + ws.sx64),
+                             x_copy ? absmax + 1 : nullptr, W, out * in, absmax, ca, s);
+    sxp = reinterpret_cast<const double*>(wsb + ws.sx64);
+  } else {
+    e = launch_absmax(W, dtype, out * in, absmax, s);
+    if (e == cudaSuccess && x_copy) e = launch_absmax(X, dtype, N * in, absmax + 1, s);
+    if (e == cudaSuccess) e = launch_alpha_root(sxp, in, ca, s);
+  }
+  if (e == cudaSuccess && x_copy) e = launch_to_f16(X, dtype, N * in, absmax + 1, wsb + ws.xf16, s);
+  if (e == cudaSuccess)
+    e = launch_alpha_table(sxp, ca.root, ca.inv_c, ca.escale, in, grid, s32, inv_s32, pow2_s, s);
   if (e != cudaSuccess) return AWQ_ERR_CUDA;
+  const void* xh = x_copy ? static_cast<const void*>(wsb + ws.xf16) : X;
 
   const SearchPlan pl = plan_search(dtype, out, in, N, n_alpha, group, device_sm_count());
   double* partials = reinterpret_cast<double*>(wsb + ws.partials);

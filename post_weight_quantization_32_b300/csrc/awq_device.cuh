@@ -83,6 +83,18 @@ __host__ __device__ __forceinline__ int pow2_exponent_for(double v) {
   return m < -60 ? -60 : (m > 60 ? 60 : m);
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// A kernel launched with the programmatic-stream-serialization attribute may
+// begin while the kernel before it in the stream is still running.
+// pdl_wait() returns once that kernel has completed and its memory writes
+// are visible (at once for an ordinary launch); nothing that kernel writes
+// may be touched before it.  pdl_trigger() lets the next such kernel begin
+// launching once every CTA of this one has triggered or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ shared
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

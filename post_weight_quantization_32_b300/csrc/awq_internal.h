@@ -15,12 +15,55 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Launch with the programmatic-stream-serialization attribute: the kernel
+// may begin while the previous kernel in the stream is still running, and
+// must call pdl_wait() before touching anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---- statistics and conversions (awq_stats.cu)
+// Where the per-alpha centring values go, for a launch that also forms them
+// (grid == 0: none).  root[j] = sx[j] ^ (1 / grid); minmax holds each CTA
+// chunk's max and min of sx with their roots (4 doubles per chunk,
+// prep_chunks(in) chunks at most); ticket is a
+// zeroed counter; absmax = {max|W|, max|X|} as float bits (max|X| is used
+// when x_scaled, i.e. X is copied to fp16 with a power-of-two scaling);
+// inv_c, escale, unscale, pow2_s have grid + 1 entries.
+struct CentreArgs {
+  int grid;
+  int x_scaled;
+  double* root;
+  double* minmax;
+  uint32_t* ticket;
+  const uint32_t* absmax;
+  double* inv_c;
+  float* escale;
+  double* unscale;
+  int32_t* pow2_s;
+};
+
 // sx[j] = sum_n |X[n, j]| / N + 1e-8, float64.  With xmax != nullptr the same
-// pass folds max|X| into *xmax (the bits of a non-negative float; *xmax must
-// start at 0; needs in % 8 == 0 and X 16-byte aligned).
+// pass folds max|X| into *xmax, and with W != nullptr the same launch folds
+// max|W| (nW values) into *wmax (bits of non-negative floats; both words must
+// start at 0; needs in % 8 == 0, nW % 8 == 0 and 16-byte aligned X and W).
+// With ca.grid != 0 the launch also writes ca.root and, once every CTA is
+// done, the centring values (needs the same vector conditions).
 cudaError_t launch_channel_stats(const void* X, int dt, int64_t N, int64_t in, double* sx,
-                                 uint32_t* xmax, cudaStream_t s);
+                                 uint32_t* xmax, const void* W, int64_t nW, uint32_t* wmax,
+                                 const CentreArgs& ca, cudaStream_t s);
 // *out = max(*out, bits of max_i |p[i]|); *out must start at 0.
 cudaError_t launch_absmax(const void* p, int dt, int64_t n, uint32_t* out, cudaStream_t s);
 // dst = fp16(X * 2^m) with m = pow2_exponent_for(max|X|) read from *xmax_bits;
@@ -29,20 +72,19 @@ cudaError_t launch_to_f16(const void* X, int dt, int64_t n, const uint32_t* xmax
                           cudaStream_t s);
 
 // ---- alpha tables, reduction and argmin (awq_prep.cu)
-// For k = 0..grid: s = sx^alpha_k / sqrt(max * min), written as float32
-// s32[k][j], and inv_s32[k][j] = 2^e_k / s32[k][j] where 2^e_k scales the
-// weight changes of alpha k into the fp16 range of the error GEMM
-// (absmax[0] = max|W| bits).  unscale[k] = 2^-2(e_k + m_x) undoes both
-// operand scalings on the squared sums (absmax[1] = max|X| bits; m_x = 0
-// when x_scaled == 0).  pow2_s[k] ends nonzero iff every s32[k][j] is a
-// power of two.  root ([in] doubles) holds sx^(1/grid), minmax
-// (prep_chunks(in) pairs) the per-chunk max and min of sx, inv_c and escale
-// ([grid + 1] each) the centring factors and 2^e_k.
+// Column chunks of the statistics / root launches: minmax needs
+// 4 * prep_chunks(in) doubles.
 size_t prep_chunks(int64_t in);
-cudaError_t launch_alpha_prep(const double* sx, int64_t in, int grid, const uint32_t* absmax,
-                              int x_scaled, double* root, double* minmax, double* inv_c,
-                              float* escale, float* s32, float* inv_s32, double* unscale,
-                              int32_t* pow2_s, cudaStream_t s);
+// ca.root and the centring values (see CentreArgs) from a given sx.
+cudaError_t launch_alpha_root(const double* sx, int64_t in, const CentreArgs& ca, cudaStream_t s);
+// For k = 0..grid: s = sx^alpha_k * inv_c[k], as the running product of
+// root = sx^(1/grid) (exactly sx at k = grid), written as float32 s32[k][j],
+// and inv_s32[k][j] = escale[k] / s32[k][j], where escale[k] = 2^e_k scales
+// the weight changes of alpha k into the fp16 range of the error GEMM.
+// pow2_s[k] (1 on entry) ends nonzero iff every s32[k][j] is a power of two.
+cudaError_t launch_alpha_table(const double* sx, const double* root, const double* inv_c,
+                               const float* escale, int64_t in, int grid, float* s32,
+                               float* inv_s32, int32_t* pow2_s, cudaStream_t s);
 // err[k] = unscale[k] * sum_t partials[k][t] / denom (fixed order),
 // best = strict-< argmin, s_best = s32[best].
 cudaError_t launch_reduce_argmin(const double* partials, const double* unscale, int n_alpha,

@@ -17,6 +17,9 @@
 // half-integer, the only place where the two could round differently: the
 // multiply-by-reciprocal result is within 3 float32 ulps of the true
 // quotient.  Codes therefore equal those of true division exactly.
+#include <algorithm>
+#include <type_traits>
+
 #include "awq_device.cuh"
 #include "awq_internal.h"
 
@@ -78,6 +81,8 @@ __global__ void __launch_bounds__(256) pack_warp_kernel(const T* __restrict__ W,
                                                         int64_t nwords, float* __restrict__ scales,
                                                         uint8_t* __restrict__ zeros,
                                                         int32_t* dev_status) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t segs = (in + 255) / 256;
   const int64_t total = out * segs;
@@ -98,7 +103,7 @@ __global__ void __launch_bounds__(256) pack_warp_kernel(const T* __restrict__ W,
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         t[e] = __fmul_rn(v[e], sv[e]);
-        nan |= (t[e] != t[e]);
+        nan |= !(fabsf(t[e]) <= 3.402823466e38f);  // NaN or infinite
       }
     } else {
 #pragma unroll
@@ -158,6 +163,285 @@ __global__ void __launch_bounds__(256) pack_warp_kernel(const T* __restrict__ W,
   }
 }
 
+// NaN-propagating max / min (the plain fmaxf / fminf drop NaN operands).
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ float min_nan(float a, float b) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3_nan(float a, float b, float c) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Sixteen consecutive elements of a row as loaded (raw bits), widened later,
+// so that several rows' loads are in flight before any arithmetic.
+template <typename T>
+struct Raw16 {
+  uint4 u[2];
+  __device__ __forceinline__ void load(const T* p) {
+    u[0] = __ldg(reinterpret_cast<const uint4*>(p));
+    u[1] = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+  }
+  __device__ __forceinline__ void widen(float (&v)[16]) const {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t w[4] = {u[h].x, u[h].y, u[h].z, u[h].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float2 f;
+        if constexpr (std::is_same<T, __half>::value) {
+          f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        } else {
+          f = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+        }
+        v[8 * h + 2 * i] = f.x;
+        v[8 * h + 2 * i + 1] = f.y;
+      }
+    }
+  }
+};
+template <>
+struct Raw16<float> {
+  float4 u[4];
+  __device__ __forceinline__ void load(const float* p) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = __ldg(reinterpret_cast<const float4*>(p) + i);
+  }
+  __device__ __forceinline__ void widen(float (&v)[16]) const {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[4 * i] = u[i].x;
+      v[4 * i + 1] = u[i].y;
+      v[4 * i + 2] = u[i].z;
+      v[4 * i + 3] = u[i].w;
+    }
+  }
+};
+
+// 16-byte asynchronous copy global -> shared (bypassing L1), and the
+// per-thread group bookkeeping of those copies.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Fast path for b in {2, 4, 8} and group in {32, 64, ..., 1024} (lpg =
+// group / 32 lanes per group).  CTA (x, y) works on the 1024-column segment
+// y; its warps take rows (warp w: row x*8 + w, then every gridDim.x*8
+// rows), 32 columns per lane, so each lane's 32 codes fill b whole words and
+// are stored without exchange.  Each thread streams its own slice of W
+// through a kPackStages-deep ring in shared memory with cp.async (no
+// barriers: a thread reads only what it copied), so the loads of the next
+// rows are in flight while the current one is quantized.
+//
+// Rounding as in round_quotient, with the screen for half-integers taken
+// once per lane: |t / scale| < 2^B for every finite group (the group's own
+// extreme sets the scale), so the multiply-by-reciprocal error stays below
+// 2^(B-21) and only a lane with some |r - round(r)| >= 0.5 - 2^(B-21)
+// re-forms its codes by true division (clamped).  Away from half-integers
+// the codes need no clamp: symmetric ones lie in [1, 2^B - 1] by
+// construction, and an asymmetric code can only exceed 2^B - 1 when both
+// t / scale and -lo / scale sit on half-integers, which the screen catches.
+// So a word is formed as sum_i bits(r_i + 1.5 * 2^23) << (i * B) plus one
+// constant that removes the magic number and adds the zero point to every
+// field.  A NaN or infinite product sends the row's lanes down the
+// clamped path (codes unspecified but within [0, 2^B - 1]) and sets the
+// status.
+constexpr int kPackSeg = 1024;
+constexpr int kPackStages = 3;
+constexpr int kPackThreads = 256;
+constexpr int kPackCtasPerSm = 2;
+
+template <typename T>
+constexpr int pack_chunks() {  // 16-byte chunks of one lane's 32 weights
+  return 32 * (int)sizeof(T) / 16;
+}
+template <typename T>
+constexpr size_t pack_smem_bytes() {
+  return (size_t)kPackStages * pack_chunks<T>() * kPackThreads * 16;
+}
+
+template <typename T, int B>
+__global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_fast_kernel(
+    const T* __restrict__ W, int64_t out, int64_t in, const float* __restrict__ s, QParams qp,
+    int lpg, uint32_t* __restrict__ qweight, int64_t nwords, float* __restrict__ scales,
+    uint8_t* __restrict__ zeros, int32_t* dev_status) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int kChunks = pack_chunks<T>();
+  constexpr int kPerWord = 32 / B;  // codes per 32-bit word
+  constexpr uint32_t kMaxq = (1u << B) - 1u;
+  // sum over one word's fields of 2^(i * B)
+  constexpr uint32_t kRep = B == 2 ? 0x55555555u : (B == 4 ? 0x11111111u : 0x01010101u);
+  extern __shared__ uint4 ring[];  // [stage][chunk][thread]
+  const float thr = 0.5f - ldexpf(1.0f, B - 21);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t segs = (in + kPackSeg - 1) / kPackSeg;
+  const int64_t ngroups = in / (32 * lpg);
+  const int64_t rstep = (int64_t)gridDim.x * 8;
+  for (int64_t seg = blockIdx.y; seg < segs; seg += gridDim.y) {
+    const int64_t c0 = seg * kPackSeg + lane * 32;
+    const bool live = c0 < in;  // in is a multiple of the group, so all 32 columns are live
+    float sv[32];
+    if (live) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 q = __ldg(reinterpret_cast<const float4*>(s + c0) + i);
+        sv[4 * i] = q.x;
+        sv[4 * i + 1] = q.y;
+        sv[4 * i + 2] = q.z;
+        sv[4 * i + 3] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) sv[e] = 0.0f;
+    }
+    const int64_t r0 = (int64_t)blockIdx.x * 8 + warp;
+    // copies of row r0 + i * rstep into ring stage i % kPackStages (one group per row)
+    auto issue = [&](int64_t i) {
+      const int64_t row = r0 + i * rstep;
+      if (row < out && live) {
+        uint4* st = ring + (size_t)(i % kPackStages) * kChunks * kPackThreads + threadIdx.x;
+        const uint4* src = reinterpret_cast<const uint4*>(W + row * in + c0);
+#pragma unroll
+        for (int h = 0; h < kChunks; ++h) cp_async16(st + (size_t)h * kPackThreads, src + h);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int i = 0; i < kPackStages - 1; ++i) issue(i);
+    for (int64_t i = 0; r0 + i * rstep < out; ++i) {
+      issue(i + kPackStages - 1);
+      cp_async_wait<kPackStages - 1>();
+      const int64_t row = r0 + i * rstep;
+      const uint4* st = ring + (size_t)(i % kPackStages) * kChunks * kPackThreads + threadIdx.x;
+      // t = w * s (zero on lanes past the end of the row)
+      float t[32];
+      if (live) {
+#pragma unroll
+        for (int h = 0; h < 32 * (int)sizeof(T) / 32; ++h) {
+          Raw16<T> raw;
+#pragma unroll
+          for (int c = 0; c < (int)sizeof(Raw16<T>) / 16; ++c)
+            reinterpret_cast<uint4*>(&raw)[c] =
+                st[(size_t)(h * (int)sizeof(Raw16<T>) / 16 + c) * kPackThreads];
+          float v[16];
+          raw.widen(v);
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const float2 p = __fmul2_rn(make_float2(v[e], v[e + 1]),
+                                        make_float2(sv[16 * h + e], sv[16 * h + e + 1]));
+            t[16 * h + e] = p.x;
+            t[16 * h + e + 1] = p.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) t[e] = 0.0f;
+      }
+      // group parameters (NaN-propagating extremes: a NaN marks the row bad)
+      float scale;
+      int zero;
+      bool bad;
+      if (qp.sym) {
+        float m = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) m = max3_nan(m, fabsf(t[e]), fabsf(t[e + 1]));
+        for (int o = 1; o < lpg; o <<= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+        bad = !(m <= 3.402823466e38f);
+        scale = fmaxf(__fdiv_rn(m, qp.Lf), 1e-8f);
+        zero = 1 << (B - 1);
+      } else {
+        float lo = 0.0f, hi = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          lo = min3_nan(lo, t[e], t[e + 1]);
+          hi = max3_nan(hi, t[e], t[e + 1]);
+        }
+        for (int o = 1; o < lpg; o <<= 1) {
+          lo = min_nan(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+          hi = max_nan(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        const float span = __fsub_rn(hi, lo);
+        bad = !(span <= 3.402823466e38f);
+        scale = fmaxf(__fdiv_rn(span, qp.maxqf), 1e-8f);
+        zero = (int)rintf(__fdiv_rn(-lo, scale));
+      }
+      const bool row_bad = __any_sync(0xffffffffu, bad);
+      if (row_bad && lane == 0) set_status(dev_status, ST_NONFINITE);
+      if (!live) continue;
+      // codes: each word is a sum of shifted magic-number bit patterns plus
+      // one constant (see above)
+      const float rcp = __frcp_rn(scale);
+      const uint32_t cw = (uint32_t)(zero - __float_as_int(kMagic)) * kRep;
+      uint32_t wd[B];
+      float dmax = 0.0f;
+#pragma unroll
+      for (int w = 0; w < B; ++w) {
+        uint32_t acc = cw;
+#pragma unroll
+        for (int e = 0; e < kPerWord; e += 2) {
+          const int x = w * kPerWord + e;
+          const float2 rr = __fmul2_rn(make_float2(t[x], t[x + 1]), make_float2(rcp, rcp));
+          const float2 rm = __fadd2_rn(rr, make_float2(kMagic, kMagic));
+          const float2 k = __fadd2_rn(rm, make_float2(-kMagic, -kMagic));
+          const float2 d = __fadd2_rn(rr, make_float2(-k.x, -k.y));
+          dmax = fmax3f(dmax, fabsf(d.x), fabsf(d.y));
+          acc += (uint32_t)__float_as_int(rm.x) << (e * B);
+          acc += (uint32_t)__float_as_int(rm.y) << ((e + 1) * B);
+        }
+        wd[w] = acc;
+      }
+      if (dmax >= thr || row_bad) {  // rare: a quotient close to a half-integer, or NaN / inf
+#pragma unroll
+        for (int w = 0; w < B; ++w) {
+          uint32_t acc = 0u;
+#pragma unroll
+          for (int e = 0; e < kPerWord; ++e) {
+            const uint32_t q = min(
+                (uint32_t)((int)rintf(__fdiv_rn(t[w * kPerWord + e], scale)) + zero), kMaxq);
+            acc |= q << (e * B);
+          }
+          wd[w] = acc;
+        }
+      }
+      uint32_t* dst = qweight + row * nwords + seg * (kPackSeg * B / 32) + lane * B;
+      if constexpr (B == 2) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(wd[0], wd[1]);
+      } else {
+#pragma unroll
+        for (int w = 0; w < B; w += 4)
+          *reinterpret_cast<uint4*>(dst + w) = make_uint4(wd[w], wd[w + 1], wd[w + 2], wd[w + 3]);
+      }
+      if ((lane & (lpg - 1)) == 0) {
+        const int64_t g = c0 / (32 * lpg);
+        scales[row * ngroups + g] = scale;
+        zeros[row * ngroups + g] = (uint8_t)zero;
+      }
+    }
+    cp_async_wait<0>();  // no copy may still target the ring when it is reused
+  }
+}
+
 // General path (any group size): one warp per (row, group), lanes strided
 // over the group's columns; codes are OR-ed into the zeroed output words
 // (OR is exact and order-independent, so the result is deterministic).
@@ -182,7 +466,7 @@ __global__ void __launch_bounds__(256) pack_general_kernel(const T* __restrict__
     bool nan = false;
     for (int j = lane; j < group; j += 32) {
       const float t = __fmul_rn(Elt<T>::to_f32(wr[j]), sr[j]);
-      nan |= (t != t);
+      nan |= !(fabsf(t) <= 3.402823466e38f);  // NaN or infinite
       m = fmaxf(m, fabsf(t));
       lo = fminf(lo, t);
       hi = fmaxf(hi, t);
@@ -227,8 +511,32 @@ unsigned pack_grid(int64_t warps) {
 template <typename T, int LPG>
 void launch_warp(const void* W, int64_t out, int64_t in, const float* s, QParams qp, uint32_t* qw,
                  int64_t nwords, float* sc, uint8_t* z, int32_t* st, cudaStream_t stream) {
-  pack_warp_kernel<T, LPG><<<pack_grid(out * ((in + 255) / 256)), 256, 0, stream>>>(
-      static_cast<const T*>(W), out, in, s, qp, qw, nwords, sc, z, st);
+  launch_pdl(pack_warp_kernel<T, LPG>, pack_grid(out * ((in + 255) / 256)), 256, 0, stream,
+             static_cast<const T*>(W), out, in, s, qp, qw, nwords, sc, z, st);
+}
+
+template <typename T, int B>
+cudaError_t launch_fast(const void* W, int64_t out, int64_t in, const float* s, QParams qp,
+                        int lpg, uint32_t* qw, int64_t nwords, float* sc, uint8_t* z, int32_t* st,
+                        cudaStream_t stream) {
+  const size_t smem = pack_smem_bytes<T>();
+  static bool attr_set[64] = {false};  // per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(pack_fast_kernel<T, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  // about kPackCtasPerSm CTAs per SM in all, spread over the segments
+  const int64_t segs = (in + kPackSeg - 1) / kPackSeg;
+  const int64_t ys = segs < 65535 ? segs : 65535;
+  int64_t xs = (kPackCtasPerSm * (int64_t)device_sm_count() + ys - 1) / ys;
+  xs = std::min<int64_t>(std::max<int64_t>(xs, 1), (out + 7) / 8);
+  return launch_pdl(pack_fast_kernel<T, B>, dim3((unsigned)xs, (unsigned)ys), kPackThreads, smem,
+                    stream, static_cast<const T*>(W), out, in, s, qp, lpg, qw, nwords, sc, z, st);
 }
 
 template <typename T>
@@ -237,6 +545,17 @@ cudaError_t pack_dispatch(const void* W, int64_t out, int64_t in, const float* s
                           int32_t* st, cudaStream_t stream) {
   bool vec = (in % 8 == 0) && ((reinterpret_cast<uintptr_t>(W) & 15) == 0) &&
              ((reinterpret_cast<uintptr_t>(s) & 15) == 0);
+  const bool fast_shape = (qp.bits == 2 || qp.bits == 4 || qp.bits == 8) && group >= 32 &&
+                          group <= 1024 && (group & (group - 1)) == 0;
+  if (vec && fast_shape &&
+      (reinterpret_cast<uintptr_t>(qw) & (uintptr_t)(qp.bits == 2 ? 7 : 15)) == 0) {
+    const int lpg = group / 32;
+    switch (qp.bits) {
+      case 2: return launch_fast<T, 2>(W, out, in, s, qp, lpg, qw, nwords, sc, z, st, stream);
+      case 4: return launch_fast<T, 4>(W, out, in, s, qp, lpg, qw, nwords, sc, z, st, stream);
+      default: return launch_fast<T, 8>(W, out, in, s, qp, lpg, qw, nwords, sc, z, st, stream);
+    }
+  }
   if (vec) {
     switch (group) {
       case 8: launch_warp<T, 1>(W, out, in, s, qp, qw, nwords, sc, z, st, stream); break;

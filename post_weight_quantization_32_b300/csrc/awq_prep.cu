@@ -15,6 +15,7 @@
 // errors are never kept ("Source code": if err < best_err).
 #include <math.h>
 
+#include "awq_alpha.cuh"
 #include "awq_device.cuh"
 #include "awq_internal.h"
 
@@ -23,118 +24,77 @@ namespace awq {
 namespace {
 
 constexpr int kPrepChunk = 64;   // columns per CTA of the per-column kernels
+constexpr int kMaxGrid = 4096;   // largest grid the C ABI accepts
 
 // grid = chunks: root[j] = sx[j] ^ (1 / grid) in float64 and each chunk's
-// max and min of sx.
+// max and min of sx; the last CTA to finish reduces the chunk extremes and
+// forms the per-alpha centring values.  (The statistics launch does the same
+// when it computes sx itself; this kernel serves a caller-given sx.)
 __global__ void __launch_bounds__(kPrepChunk) alpha_root_kernel(const double* __restrict__ sx,
-                                                                int64_t in, int grid,
-                                                                double* __restrict__ root,
-                                                                double* __restrict__ minmax) {
-  double mx = -INFINITY, mn = INFINITY;
+                                                               int64_t in, CentreArgs ca) {
+  pdl_wait();
+  pdl_trigger();
+  SxExt x;
+  x.init();
   const int64_t j = (int64_t)blockIdx.x * kPrepChunk + threadIdx.x;
   if (j < in) {
     const double v = sx[j];
-    root[j] = exp(log(v) / (double)grid);
-    mx = v;
-    mn = v;
+    const double r = exp(log(v) / (double)ca.grid);
+    ca.root[j] = r;
+    x.take(v, r);
   }
-  __shared__ double smx[kPrepChunk / 32], smn[kPrepChunk / 32];
-  for (int o = 16; o > 0; o >>= 1) {
-    mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    mn = fmin(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-  }
-  if ((threadIdx.x & 31) == 0) {
-    smx[threadIdx.x >> 5] = mx;
-    smn[threadIdx.x >> 5] = mn;
-  }
+  __shared__ SxExt sext[kPrepChunk / 32];
+  x.warp_merge();
+  if ((threadIdx.x & 31) == 0) sext[threadIdx.x >> 5] = x;
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 0; w < kPrepChunk / 32; ++w) {
-      mx = fmax(mx, smx[w]);
-      mn = fmin(mn, smn[w]);
-    }
-    minmax[2 * blockIdx.x + 0] = mx;
-    minmax[2 * blockIdx.x + 1] = mn;
+    for (int w = 1; w < kPrepChunk / 32; ++w) x.merge(sext[w]);
+    x.store(ca.minmax + 4 * blockIdx.x);
   }
+  centre_if_last(ca, gridDim.x);
 }
 
-// One CTA, thread k per alpha (strided).  The largest and smallest s_k over
-// the columns are s_k at the largest and smallest s_X (the power is
-// monotone); from them the centring factor inv_c[k] = 1 / sqrt(max * min),
-// and the fp16 scaling of the weight changes: one entry's change is
-// |q*scale - w*s| / s <= (group step) / s, and the group step is at most
-// max|W| * max(s) (either quantizer), so max|W| * max(s) / min(s) bounds
-// |dW| for the whole alpha; its power-of-two exponent sets e_k, folded into
-// the 1/s table, and unscale[k] = 2^-2(e_k + m_x) undoes both operand
-// scalings on the squared sums.  pow2_s[k] starts at 1 here.
-__global__ void __launch_bounds__(256) alpha_centre_kernel(
-    const double* __restrict__ minmax, int64_t nch, int grid,
-    const uint32_t* __restrict__ absmax, int x_scaled, double* __restrict__ inv_c,
-    float* __restrict__ escale, double* __restrict__ unscale, int32_t* __restrict__ pow2_s) {
-  __shared__ double smx[8], smn[8];
-  double mx = -INFINITY, mn = INFINITY;
-  for (int64_t ch = threadIdx.x; ch < nch; ch += blockDim.x) {
-    mx = fmax(mx, minmax[2 * ch + 0]);
-    mn = fmin(mn, minmax[2 * ch + 1]);
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    mn = fmin(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-  }
-  if ((threadIdx.x & 31) == 0) {
-    smx[threadIdx.x >> 5] = mx;
-    smn[threadIdx.x >> 5] = mn;
-  }
-  __syncthreads();
-  mx = smx[0];
-  mn = smn[0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
-    mx = fmax(mx, smx[w]);
-    mn = fmin(mn, smn[w]);
-  }
-  const double lmx = log(mx) / (double)grid, lmn = log(mn) / (double)grid;
-  const int m = x_scaled ? pow2_exponent_for((double)__uint_as_float(absmax[1])) : 0;
-  for (int k = threadIdx.x; k <= grid; k += blockDim.x) {
-    double smax, smin;
-    if (k == 0) {
-      smax = smin = 1.0;
-    } else if (k == grid) {
-      smax = mx;
-      smin = mn;
-    } else {
-      smax = exp(k * lmx);
-      smin = exp(k * lmn);
-    }
-    inv_c[k] = 1.0 / sqrt(smax * smin);
-    const int e = pow2_exponent_for((double)__uint_as_float(absmax[0]) * (smax / smin));
-    escale[k] = ldexpf(1.0f, e);
-    unscale[k] = ldexp(1.0, -2 * (e + m));
-    pow2_s[k] = 1;
-  }
-}
+// One CTA per kTabCols columns; warp q of the CTA takes the alphas k = q,
+// q + kTabSlices, q + 2 kTabSlices, ... of every column, so the float64
+// product chains are kTabSlices times shorter than one chain per column.
+// s_k = sx ^ (k / grid) = root^k: root^q by binary powering, then running
+// products by root^kTabSlices (exactly 1 at k = 0 and exactly sx at
+// k = grid), centred, rounded to float32; inv_s32 = 2^e_k / s.  pow2_s[k]
+// is cleared when some entry of the chunk is not a power of two (a bit per
+// alpha in shared memory, applied once per alpha at the end).
+constexpr int kTabCols = 32, kTabSlices = 4;
 
-// grid = chunks, one thread per column, looping over the alphas: s_k =
-// sx ^ (k / grid) as the running product root^k (exactly 1 at k = 0 and
-// exactly sx at k = grid), centred, rounded to float32; inv_s32 = 2^e_k / s.
-// pow2_s[k] is cleared when some entry of the chunk is not a power of two.
-__global__ void __launch_bounds__(kPrepChunk) alpha_table_kernel(
+__global__ void __launch_bounds__(kTabCols * kTabSlices) alpha_table_kernel(
     const double* __restrict__ sx, const double* __restrict__ root,
     const double* __restrict__ inv_c, const float* __restrict__ escale, int64_t in, int grid,
     float* __restrict__ s32, float* __restrict__ inv_s32, int32_t* __restrict__ pow2_s) {
-  const int64_t j = (int64_t)blockIdx.x * kPrepChunk + threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  __shared__ uint32_t not_pow2[(kMaxGrid + 1 + 31) / 32];
+  const int nwords = (grid + 1 + 31) / 32;
+  for (int i = threadIdx.x; i < nwords; i += blockDim.x) not_pow2[i] = 0u;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
+  const int64_t j = (int64_t)blockIdx.x * kTabCols + lane;
   const bool live = j < in;
   const double sxj = live ? sx[j] : 1.0, r = live ? root[j] : 1.0;
-  double v = 1.0;
-  for (int k = 0; k <= grid; ++k) {
-    if (k > 0) v = k == grid ? sxj : v * r;
-    const float f = __double2float_rn(v * inv_c[k]);
+  const double step = pow_int(r, kTabSlices);
+  double v = pow_int(r, q);
+  for (int k = q; k <= grid; k += kTabSlices) {
+    const double sk = k == grid ? sxj : v;
+    const float f = __double2float_rn(sk * inv_c[k]);
+    bool np2 = false;
     if (live) {
       s32[(int64_t)k * in + j] = f;
       inv_s32[(int64_t)k * in + j] = __frcp_rn(f) * escale[k];
+      np2 = (__float_as_uint(f) & 0x007FFFFFu) != 0u;
     }
-    const int p2 = (!live || (__float_as_uint(f) & 0x007FFFFFu) == 0u) ? 1 : 0;
-    if (!__syncthreads_and(p2) && threadIdx.x == 0) atomicAnd(&pow2_s[k], 0);
+    if (__any_sync(0xffffffffu, np2) && lane == 0) atomicOr(&not_pow2[k / 32], 1u << (k % 32));
+    v *= step;
   }
+  __syncthreads();
+  for (int k = threadIdx.x; k <= grid; k += blockDim.x)
+    if ((not_pow2[k / 32] >> (k % 32)) & 1u) atomicAnd(&pow2_s[k], 0);
 }
 
 // One CTA: per-alpha fixed-order sums, strict argmin, copy of the kept scales.
@@ -146,28 +106,48 @@ __global__ void __launch_bounds__(1024) reduce_argmin_kernel(const double* __res
                                                             int32_t* __restrict__ best_out,
                                                             float* __restrict__ s_best,
                                                             int32_t* dev_status) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int best_sh;
+  __shared__ double err_sh[kMaxGrid + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int k = warp; k < n_alpha; k += blockDim.x >> 5) {
     double s = 0.0;
-    for (int t = lane; t < n_tiles; t += 32) s += partials[(int64_t)k * n_tiles + t];
+    for (int t = lane; t < n_tiles; t += 32) s += __ldcg(partials + (int64_t)k * n_tiles + t);
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) err[k] = s * unscale[k] / denom;
+    if (lane == 0) {
+      const double e = s * unscale[k] / denom;
+      err[k] = e;
+      err_sh[k] = e;
+    }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (warp == 0) {
+    // first index of the smallest error under strict <, starting from +inf:
+    // each lane scans its own alphas in order, then lanes merge preferring
+    // the smaller error and, on equal errors, the smaller index
     int best = -1;
     double be = INFINITY;
-    for (int k = 0; k < n_alpha; ++k) {
-      const double e = err[k];
+    for (int k = lane; k < n_alpha; k += 32) {
+      const double e = err_sh[k];
       if (e < be) {
         be = e;
         best = k;
       }
     }
-    if (best < 0) set_status(dev_status, ST_NONFINITE);
-    *best_out = best;
-    best_sh = best;
+    for (int o = 16; o > 0; o >>= 1) {
+      const double oe = __shfl_xor_sync(0xffffffffu, be, o);
+      const int ob = __shfl_xor_sync(0xffffffffu, best, o);
+      if (ob >= 0 && (best < 0 || oe < be || (oe == be && ob < best))) {
+        be = oe;
+        best = ob;
+      }
+    }
+    if (lane == 0) {
+      if (best < 0) set_status(dev_status, ST_NONFINITE);
+      *best_out = best;
+      best_sh = best;
+    }
   }
   __syncthreads();
   const int best = best_sh;
@@ -186,32 +166,29 @@ __global__ void __launch_bounds__(1024) reduce_argmin_kernel(const double* __res
 
 }  // namespace
 
-size_t prep_chunks(int64_t in) { return (size_t)((in + kPrepChunk - 1) / kPrepChunk); }
+size_t prep_chunks(int64_t in) { return (size_t)((in + 31) / 32); }  // the finer of the two chunkings
 
-cudaError_t launch_alpha_prep(const double* sx, int64_t in, int grid, const uint32_t* absmax,
-                              int x_scaled, double* root, double* minmax, double* inv_c,
-                              float* escale, float* s32, float* inv_s32, double* unscale,
-                              int32_t* pow2_s, cudaStream_t s) {
-  const unsigned nch = (unsigned)prep_chunks(in);
-  alpha_root_kernel<<<nch, kPrepChunk, 0, s>>>(sx, in, grid, root, minmax);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  alpha_centre_kernel<<<1, 256, 0, s>>>(minmax, nch, grid, absmax, x_scaled, inv_c, escale,
-                                        unscale, pow2_s);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  alpha_table_kernel<<<nch, kPrepChunk, 0, s>>>(sx, root, inv_c, escale, in, grid, s32, inv_s32,
-                                                pow2_s);
-  return cudaGetLastError();
+cudaError_t launch_alpha_root(const double* sx, int64_t in, const CentreArgs& ca, cudaStream_t s) {
+  if (ca.grid < 1 || ca.grid > kMaxGrid) return cudaErrorInvalidValue;
+  return launch_pdl(alpha_root_kernel, (unsigned)((in + kPrepChunk - 1) / kPrepChunk), kPrepChunk,
+                    0, s, sx, in, ca);
+}
+
+cudaError_t launch_alpha_table(const double* sx, const double* root, const double* inv_c,
+                               const float* escale, int64_t in, int grid, float* s32,
+                               float* inv_s32, int32_t* pow2_s, cudaStream_t s) {
+  if (grid < 1 || grid > kMaxGrid) return cudaErrorInvalidValue;
+  return launch_pdl(alpha_table_kernel, (unsigned)((in + kTabCols - 1) / kTabCols),
+                    kTabCols * kTabSlices, 0, s, sx, root, inv_c, escale, in, grid, s32, inv_s32,
+                    pow2_s);
 }
 
 cudaError_t launch_reduce_argmin(const double* partials, const double* unscale, int n_alpha,
                                  int n_tiles, double denom, const float* s32, int64_t in,
                                  double* err, int32_t* best, float* s_best, int32_t* dev_status,
                                  cudaStream_t s) {
-  reduce_argmin_kernel<<<1, 1024, 0, s>>>(partials, unscale, n_alpha, n_tiles, denom, s32, in, err,
-                                          best, s_best, dev_status);
-  return cudaGetLastError();
+  return launch_pdl(reduce_argmin_kernel, 1, 1024, 0, s, partials, unscale, n_alpha, n_tiles, denom,
+                    s32, in, err, best, s_best, dev_status);
 }
 
 }  // namespace awq

@@ -251,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t x_ring = w_ring + (uint32_t)p.sw * W_STAGE;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.sw; ++i) {
       mbar_init(smem_addr(&c.w_full[i]), 1);
@@ -283,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // the scale tables, X and the status words come from earlier kernels
   const uint32_t tmem = c.tmem_base;
   volatile int* abort = &c.abort;
   const uint64_t lim = p.wait_limit_ns;
@@ -755,8 +757,7 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
   a.wait_limit_ns = (uint64_t)(wait_limit_ns > 0 ? wait_limit_ns : 2000000000LL);
   a.test_timeout = test_timeout;
   if (ev0 && (e = cudaEventRecord(ev0, s)) != cudaSuccess) return e;
-  fn<<<pl.grid, kThreads, pl.smem, s>>>(mw, mx, ms, a);
-  e = cudaGetLastError();
+  e = launch_pdl(fn, dim3((unsigned)pl.grid), dim3(kThreads), (size_t)pl.smem, s, mw, mx, ms, a);
   if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
   return e;
 }

@@ -3,10 +3,13 @@
 // set the power-of-two operand scalings, and the fp16 copy of X that the
 // tensor-core error GEMM reads when X is not fp16 already.
 //
-// All are HBM-bound passes.  The statistic is accumulated in float64 in a
-// fixed order, so repeated calls give identical results.
+// All are HBM-bound passes.  The statistic is accumulated in a fixed order
+// (exactly, as an integer, for fp16 X), so repeated calls give identical
+// results.
 #include <algorithm>
+#include <type_traits>
 
+#include "awq_alpha.cuh"
 #include "awq_device.cuh"
 #include "awq_internal.h"
 
@@ -33,57 +36,174 @@ __device__ __forceinline__ void block_absmax(float m, uint32_t* out) {
   }
 }
 
-// Vector path: in % 8 == 0 and 16-byte aligned rows.  Thread (c, r) sums the
-// 8 columns c*8..c*8+7 of the CTA's 32 over rows r, r+64, r+128, ..., four
-// 16-byte loads in flight at a time; the 64 slices are then added in a fixed
-// order.  With xmax != nullptr the pass also folds max|X| into *xmax.
+// Column sums of |x| over 8 columns.  For fp16 the sum is kept exactly as an
+// integer count of 2^-24 (every |x| is an integer multiple of 2^-24 below
+// 2^16, so sums of up to 2^24 rows stay below 2^64), which makes the mean
+// identical to the correctly rounded float64 one and independent of the
+// order of addition; infinities and NaN are tracked apart so the result is
+// what a float64 sum would give.  Other types accumulate in float64.
 template <typename T>
-__global__ void __launch_bounds__(256) stats_vec_kernel(const T* __restrict__ X, int64_t N,
-                                                        int64_t in, double* __restrict__ sx,
-                                                        uint32_t* __restrict__ xmax) {
-  __shared__ double red[kStatSlices][kStatCols + 1];
-  const int c = threadIdx.x % 4, r = threadIdx.x / 4;
-  const int64_t col0 = (int64_t)blockIdx.x * kStatCols + c * 8;
+struct ColSum {
+  using Part = double;
   double acc[8];
-  float m = 0.0f;
+  __device__ __forceinline__ void init() {
 #pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.0;
-  if (col0 < in) {
-    int64_t n = r;
-    for (; n + 3 * kStatSlices < N; n += 4 * kStatSlices) {
-      float v[4][8];
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0;
+  }
+  __device__ __forceinline__ void add(const T* p, float& m) {
+    float v[8];
+    load8_f32<T>(p, v);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) load8_f32<T>(X + (n + u * kStatSlices) * in + col0, v[u]);
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          acc[e] += (double)fabsf(v[u][e]);
-          m = fmaxf(m, fabsf(v[u][e]));
-        }
+    for (int e = 0; e < 8; ++e) {
+      acc[e] += (double)fabsf(v[e]);
+      m = fmaxf(m, fabsf(v[e]));
     }
-    for (; n < N; n += kStatSlices) {
-      float v[8];
-      load8_f32<T>(X + n * in + col0, v);
+  }
+  __device__ __forceinline__ Part part(int e) const { return acc[e]; }
+  __device__ __forceinline__ void flag_specials(uint32_t*) const {}
+  static __device__ __forceinline__ double total(Part a, uint32_t) { return a; }
+};
+
+template <>
+struct ColSum<__half> {
+  using Part = unsigned long long;
+  unsigned long long acc[8];
+  uint32_t special;  // bit e: column e saw an infinity; bit 8 + e: a NaN
+  __device__ __forceinline__ void init() {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        acc[e] += (double)fabsf(v[e]);
-        m = fmaxf(m, fabsf(v[e]));
+    for (int e = 0; e < 8; ++e) acc[e] = 0ull;
+    special = 0u;
+  }
+  // (max|X| is not tracked here: an fp16 X needs no copy, so no caller asks)
+  __device__ __forceinline__ void add(const __half* p, float&) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t h = (w[e >> 1] >> ((e & 1) * 16)) & 0x7FFFu;
+      const uint32_t ex = h >> 10, mant = h & 0x3FFu;
+      if (ex == 31u) {
+        special |= mant ? (1u << (8 + e)) : (1u << e);
+      } else {
+        acc[e] += ex == 0u ? (unsigned long long)mant
+                           : ((unsigned long long)(mant | 0x400u) << (ex - 1u));
       }
     }
   }
+  __device__ __forceinline__ Part part(int e) const { return acc[e]; }
+  // per column of the CTA: bit 0 = an infinity was seen, bit 1 = a NaN
+  __device__ __forceinline__ void flag_specials(uint32_t* spec) const {
+    if (special == 0u) return;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) red[r][c * 8 + e] = acc[e];
-  if (xmax != nullptr) block_absmax(m, xmax);  // contains __syncthreads
-  __syncthreads();
-  if (threadIdx.x < kStatCols) {
-    const int64_t j = (int64_t)blockIdx.x * kStatCols + threadIdx.x;
-    if (j < in) {
-      double s = 0.0;
-      for (int k = 0; k < kStatSlices; ++k) s += red[k][threadIdx.x];
-      sx[j] = s / (double)N + 1e-8;
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t f = ((special >> e) & 1u) | (((special >> (8 + e)) & 1u) << 1);
+      if (f) atomicOr(spec + e, f);
     }
   }
+  static __device__ __forceinline__ double total(Part a, uint32_t spec) {
+    if (spec & 2u) return __longlong_as_double(0x7FF8000000000000ll);
+    if (spec & 1u) return INFINITY;
+    return ldexp((double)a, -24);
+  }
+};
+
+// Vector path: in % 8 == 0 and 16-byte aligned rows.  Blocks [0, nx) do the
+// statistics: thread (c, r) sums the 8 columns c*8..c*8+7 of the CTA's 32
+// over rows r, r+64, r+128, ..., four 16-byte loads in flight at a time; the
+// 64 slices are then added in a fixed order.  With xmax != nullptr the pass
+// also folds max|X| into *xmax.  Blocks [nx, gridDim.x) fold max|W| (nW
+// values) into *wmax in the same launch.  With ca.grid != 0 the statistics
+// blocks also write root = sx^(1/grid) and their chunk's extremes of sx, and
+// the last block to finish forms the per-alpha centring values.
+template <typename T>
+__global__ void __launch_bounds__(256) stats_vec_kernel(const T* __restrict__ X, int64_t N,
+                                                        int64_t in, double* __restrict__ sx,
+                                                        uint32_t* __restrict__ xmax,
+                                                        const T* __restrict__ W, int64_t nW,
+                                                        uint32_t* __restrict__ wmax, int nx,
+                                                        CentreArgs ca) {
+  pdl_trigger();
+  if ((int)blockIdx.x >= nx) {
+    // ------------------------------------------------------------- max|W|
+    float m = 0.0f;
+    const int64_t n8 = nW / 8;
+    const int64_t stride = (int64_t)(gridDim.x - nx) * blockDim.x;
+    int64_t i = (int64_t)(blockIdx.x - nx) * blockDim.x + threadIdx.x;
+    for (; i < n8; i += 8 * stride) {  // eight 16-byte loads in flight
+      float v[8][8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (i + u * stride < n8) {
+          load8_f32<T>(W + (i + u * stride) * 8, v[u]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[u][e] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[u][e]));
+    }
+    block_absmax(m, wmax);
+    if (ca.grid != 0) centre_if_last(ca, (unsigned)nx);
+    return;
+  }
+  // --------------------------------------------------------------- statistics
+  using Part = typename ColSum<T>::Part;
+  __shared__ Part red[kStatSlices][kStatCols + 1];
+  __shared__ Part red2[kStatSlices / 8][kStatCols + 1];
+  __shared__ uint32_t spec[kStatCols];
+  if (threadIdx.x < kStatCols) spec[threadIdx.x] = 0u;
+  __syncthreads();
+  const int c = threadIdx.x % 4, r = threadIdx.x / 4;
+  const int64_t col0 = (int64_t)blockIdx.x * kStatCols + c * 8;
+  ColSum<T> cs;
+  cs.init();
+  float m = 0.0f;
+  if (col0 < in) {
+    int64_t n = r;
+    for (; n + 3 * kStatSlices < N; n += 4 * kStatSlices) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) cs.add(X + (n + u * kStatSlices) * in + col0, m);
+    }
+    for (; n < N; n += kStatSlices) cs.add(X + n * in + col0, m);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[r][c * 8 + e] = cs.part(e);
+  cs.flag_specials(spec + c * 8);
+  if (xmax != nullptr) block_absmax(m, xmax);  // contains __syncthreads
+  __syncthreads();
+  {  // the 64 slices in a fixed two-level order: 8 runs of 8, then the 8 run sums
+    const int cc = threadIdx.x % kStatCols, pp = threadIdx.x / kStatCols;
+    Part a = red[pp * 8][cc];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) a += red[pp * 8 + k][cc];
+    red2[pp][cc] = a;
+  }
+  __syncthreads();
+  if (threadIdx.x < kStatCols) {  // warp 0
+    const int64_t j = (int64_t)blockIdx.x * kStatCols + threadIdx.x;
+    SxExt x;
+    x.init();
+    if (j < in) {
+      Part a = red2[0][threadIdx.x];
+#pragma unroll
+      for (int k = 1; k < kStatSlices / 8; ++k) a += red2[k][threadIdx.x];
+      const double v = ColSum<T>::total(a, spec[threadIdx.x]) / (double)N + 1e-8;
+      sx[j] = v;
+      if (ca.grid != 0) {
+        const double r = exp(log(v) / (double)ca.grid);
+        ca.root[j] = r;
+        x.take(v, r);
+      }
+    }
+    if (ca.grid != 0) {
+      x.warp_merge();
+      if (threadIdx.x == 0) x.store(ca.minmax + 4 * blockIdx.x);
+    }
+  }
+  if (ca.grid != 0) centre_if_last(ca, (unsigned)nx);
 }
 
 // Scalar path for any shape: thread (c, r) sums column c over rows r, r+4, ...
@@ -140,6 +260,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) to_f16_kernel(const T* __restrict__ X, int64_t n8,
                                                      const uint32_t* __restrict__ xmax_bits,
                                                      uint4* __restrict__ dst) {
+  pdl_wait();
+  pdl_trigger();
   const float sc = ldexpf(1.0f, pow2_exponent_for((double)__uint_as_float(*xmax_bits)));
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -155,15 +277,26 @@ __global__ void __launch_bounds__(256) to_f16_kernel(const T* __restrict__ X, in
   }
 }
 
+unsigned grid_for(int64_t work);
+
 template <typename T>
 cudaError_t stats_dispatch(const void* X, int64_t N, int64_t in, double* sx, uint32_t* xmax,
+                           const void* W, int64_t nW, uint32_t* wmax, const CentreArgs& ca,
                            cudaStream_t s) {
   const bool vec = (in % 8 == 0) && ((reinterpret_cast<uintptr_t>(X) & 15) == 0);
-  if (vec) {
-    stats_vec_kernel<T><<<(unsigned)((in + kStatCols - 1) / kStatCols), 256, 0, s>>>(
-        static_cast<const T*>(X), N, in, sx, xmax);
+  const bool wvec = W != nullptr && nW % 8 == 0 && ((reinterpret_cast<uintptr_t>(W) & 15) == 0);
+  if (std::is_same<T, __half>::value && xmax != nullptr) return cudaErrorInvalidValue;
+  if (vec && (W == nullptr || wvec)) {
+    const int nx = (int)((in + kStatCols - 1) / kStatCols);
+    // max|W| blocks: about eight 16-byte loads per thread, all in flight at once
+    const int nw =
+        W != nullptr ? (int)std::max<int64_t>(1, std::min<int64_t>((nW / 8 + 2047) / 2048,
+                                                                   device_sm_count() * 8))
+                     : 0;
+    stats_vec_kernel<T><<<(unsigned)(nx + nw), 256, 0, s>>>(
+        static_cast<const T*>(X), N, in, sx, xmax, static_cast<const T*>(W), nW, wmax, nx, ca);
   } else {
-    if (xmax != nullptr) return cudaErrorInvalidValue;
+    if (xmax != nullptr || W != nullptr || ca.grid != 0) return cudaErrorInvalidValue;
     stats_scalar_kernel<T><<<(unsigned)((in + kScalarCols - 1) / kScalarCols), 256, 0, s>>>(
         static_cast<const T*>(X), N, in, sx);
   }
@@ -179,11 +312,12 @@ unsigned grid_for(int64_t work) {
 }  // namespace
 
 cudaError_t launch_channel_stats(const void* X, int dt, int64_t N, int64_t in, double* sx,
-                                 uint32_t* xmax, cudaStream_t s) {
+                                 uint32_t* xmax, const void* W, int64_t nW, uint32_t* wmax,
+                                 const CentreArgs& ca, cudaStream_t s) {
   switch (dt) {
-    case kDtF32: return stats_dispatch<float>(X, N, in, sx, xmax, s);
-    case kDtF16: return stats_dispatch<__half>(X, N, in, sx, xmax, s);
-    default: return stats_dispatch<__nv_bfloat16>(X, N, in, sx, xmax, s);
+    case kDtF32: return stats_dispatch<float>(X, N, in, sx, xmax, W, nW, wmax, ca, s);
+    case kDtF16: return stats_dispatch<__half>(X, N, in, sx, xmax, W, nW, wmax, ca, s);
+    default: return stats_dispatch<__nv_bfloat16>(X, N, in, sx, xmax, W, nW, wmax, ca, s);
   }
 }
 
@@ -210,11 +344,10 @@ cudaError_t launch_to_f16(const void* X, int dt, int64_t n, const uint32_t* xmax
   const unsigned grid = grid_for(n8);
   uint4* d = static_cast<uint4*>(dst);
   if (dt == kDtF32)
-    to_f16_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(X), n8, xmax_bits, d);
-  else
-    to_f16_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(X), n8,
-                                                      xmax_bits, d);
-  return cudaGetLastError();
+    return launch_pdl(to_f16_kernel<float>, grid, 256, 0, s, static_cast<const float*>(X), n8,
+                      xmax_bits, d);
+  return launch_pdl(to_f16_kernel<__nv_bfloat16>, grid, 256, 0, s,
+                    static_cast<const __nv_bfloat16*>(X), n8, xmax_bits, d);
 }
 
 }  // namespace awq

@@ -135,14 +135,35 @@ def test_quantize_pack_ragged_shapes(awq):
                 check_pack(awq, W, s32, bits, g, sym)
 
 
-def test_quantize_pack_nan_reports(awq):
+@pytest.mark.parametrize("bad", [float("nan"), float("inf"), -float("inf")])
+@pytest.mark.parametrize("bits,group,sym", [(4, 128, True), (4, 128, False), (3, 64, True),
+                                            (8, 32, False), (4, 8, True)])
+def test_quantize_pack_nonfinite_reports(awq, bad, bits, group, sym):
     W, _ = make_random_layer(4, 128, 2, dtype="bf16", seed=9)
     W = W.clone()
-    W[2, 5] = float("nan")
+    W[2, 5] = bad
     st = awq.new_status()
-    awq.awq_quantize_pack(W.cuda(), torch.ones(128, device="cuda"), 4, 128, True, dev_status=st,
-                          check=False)
+    qw, _, _ = awq.awq_quantize_pack(W.cuda(), torch.ones(128, device="cuda"), bits, group, sym,
+                                     dev_status=st, check=False)
     assert int(st.item()) == 3
+    # the other rows are unaffected: bit-exact against the oracle
+    Wn = _np_w(W)
+    ref, _, _ = O.quantize_pack(np.concatenate([Wn[:2], Wn[3:]]), np.ones(128, np.float32), bits,
+                                group, sym)
+    got = qw.cpu().numpy().view(np.uint32)
+    np.testing.assert_array_equal(np.concatenate([got[:2], got[3:]]), ref)
+
+
+@pytest.mark.parametrize("bits,group,sym,n_in", [(8, 512, True, 2560), (2, 512, False, 2560),
+                                                 (4, 256, True, 2560), (4, 32, False, 2560),
+                                                 (2, 32, True, 2560), (4, 1024, True, 3072),
+                                                 (8, 1024, False, 2048)])
+def test_quantize_pack_wide_groups(awq, bits, group, sym, n_in):
+    # 2560 columns: two full 1024-column segments and a half one; 70 rows: a
+    # partial block of rows
+    W, _ = make_random_layer(70, n_in, 2, dtype="f16", seed=bits + group)
+    s32 = np.random.default_rng(group).uniform(0.1, 10.0, size=n_in).astype(np.float32)
+    check_pack(awq, W, s32, bits, group, sym)
 
 
 # ---------------------------------------------------------------- search
