@@ -97,7 +97,10 @@ size_t awq_search_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N,
  *   bits   2..8                   code width
  *   group  columns per quantization group; divides `in`.  group == in is the
  *          pages' "one group per row".  This build's search handles group
- *          in {32, 64, 128}; others return AWQ_ERR_UNSUPPORTED.
+ *          in {32, 64, 128}, any multiple of 256, and group == in (the last
+ *          two need in % 8 == 0); others return AWQ_ERR_UNSUPPORTED.  The
+ *          last two get their group ranges from a pass over W ahead of the
+ *          search.
  *   sym    1: symmetric, scale = max|w| / (2^(b-1) - 1), codes in
  *             [-2^(b-1), 2^(b-1) - 1]
  *             ["GPTQ and AWQ weight quantisation", "Output MSE vs bit width"]
@@ -129,6 +132,27 @@ int awq_search(const void* W, const void* X, int dtype,
                void* workspace, size_t workspace_bytes,
                double* err, int32_t* best, float* s_best,
                int32_t* dev_status, awq_stream_t stream);
+
+/*
+ * awq_output_power - the size of the layer's exact output,
+ *   power = mean((X W^T)^2) over the N x out entries, float64,
+ * the denominator of the relative output error ||X W^T - X Wq^T||^2 /
+ * ||X W^T||^2 ["AWQ (activation-aware weight quantization)", "What the
+ * simulations show"]: with err from awq_search (a mean over the same
+ * entries), err / power is that ratio.
+ *
+ *   W, X, dtype, out, in, N   as for awq_search
+ *   workspace, workspace_bytes >= awq_search_workspace_bytes(dtype, out,
+ *                               in, N, in, 1) (one alpha, one group per row)
+ *   power  [1] double (written)
+ * The GEMM runs on the same tensor-core path as the search (fp16 operands
+ * scaled by exact powers of two, fp32 accumulation, float64 sums in a fixed
+ * order).  Requirements: in % 8 == 0, W and X 16-byte aligned.
+ */
+int awq_output_power(const void* W, const void* X, int dtype,
+                     int64_t out, int64_t in, int64_t N,
+                     void* workspace, size_t workspace_bytes,
+                     double* power, int32_t* dev_status, awq_stream_t stream);
 
 /* Options for awq_search_ex; zero-initialise, then set what you need. */
 typedef struct {

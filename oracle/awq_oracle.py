@@ -61,6 +61,7 @@ __all__ = [
     "channel_salience", "alpha_grid", "centred_scales", "quantize_groups",
     "quantize_groups_f64", "fake_quant", "output_mse", "awq_search", "SearchResult",
     "stored_codes", "pack_bits", "unpack_bits", "quantize_pack", "rtn_fake_quant",
+    "output_power", "sweep",
 ]
 
 _EPS_SALIENCE = 1e-8          # added to the mean |X| [AWQ guide, "The code, line by line"]
@@ -232,6 +233,36 @@ def awq_search(W, X, bits: int = 4, group: Optional[int] = None, grid: int = 20,
         if err < best_err:
             best, best_err = k, err
     return SearchResult(alphas, errs, best, sx, s32_all, s32_all[best] if best >= 0 else None)
+
+
+def output_power(W, X) -> float:
+    """mean((X @ W.T) ** 2) in float64: the size of the layer's exact output.
+
+    The relative output error of the pages is ||h W - h Wq||^2 / ||h W||^2
+    [AWQ guide, "What the simulations show"]; err (a mean over the same
+    N * out entries) divided by this mean is that ratio.
+    """
+    X64 = np.asarray(X, dtype=np.float64)
+    W64 = np.asarray(W, dtype=np.float32).astype(np.float64)
+    return float(np.mean((X64 @ W64.T) ** 2))
+
+
+def sweep(W, X, settings, sym: bool = True, grid: int = 20):
+    """The search at several (bits, group) settings of one layer, RTN (the
+    alpha = 0 point of the grid) beside AWQ, both also relative to
+    output_power.  [AWQ guide, "What the simulations show" and "Try this";
+    "GPTQ and AWQ weight quantisation", "Output MSE vs bit width" and its
+    group-size exercise]
+    """
+    power = output_power(W, X)
+    rows = []
+    for bits, group in settings:
+        res = awq_search(W, X, bits=bits, group=group, grid=grid, sym=sym)
+        b = res.best
+        rows.append(dict(bits=bits, group=group, best=b, alpha=float(res.alphas[b]),
+                         errs=res.errs, err_rtn=float(res.errs[0]), err_awq=float(res.errs[b]),
+                         rel_rtn=float(res.errs[0]) / power, rel_awq=float(res.errs[b]) / power))
+    return rows
 
 
 def stored_codes(q: np.ndarray, bits: int, sym: bool) -> np.ndarray:

@@ -29,7 +29,7 @@ import torch
 __all__ = [
     "AWQError", "SearchOpts", "lib", "awq_channel_stats", "awq_search",
     "awq_search_workspace_bytes", "awq_quantize_pack", "new_status", "check_status", "STATUS",
-    "DTYPE", "awq_search_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "DTYPE", "awq_search_noalloc", "NOALLOC_SCRATCH_BYTES", "awq_output_power", "awq_sweep",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -40,7 +40,7 @@ STATUS = {0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARG", 2: "AWQ_ERR_UNSUPPORTED", 3: "A
           4: "AWQ_ERR_TIMEOUT", 5: "AWQ_ERR_CUDA"}
 
 EXPORTS = ("awq_status_string", "awq_channel_stats", "awq_search_workspace_bytes", "awq_search",
-           "awq_search_ex", "awq_quantize_pack", "awq_search_noalloc")
+           "awq_search_ex", "awq_quantize_pack", "awq_search_noalloc", "awq_output_power")
 
 # Size of the library's fixed scratch array used by awq_search_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -64,6 +64,8 @@ def _load() -> ctypes.CDLL:
     L.awq_search_ex.argtypes = L.awq_search.argtypes + [vp]
     L.awq_quantize_pack.restype = i32
     L.awq_quantize_pack.argtypes = [vp, i32, i64, i64, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+    L.awq_output_power.restype = i32
+    L.awq_output_power.argtypes = [vp, vp, i32, i64, i64, i64, vp, sz, vp, vp, vp]
     L.awq_search_noalloc.restype = i32
     L.awq_search_noalloc.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, i32, vp, vp, vp,
                                      vp, vp]
@@ -229,3 +231,44 @@ def awq_search_noalloc(W: torch.Tensor, X: torch.Tensor, bits: int = 4, group: O
     if check:
         check_status(st, "awq_search_noalloc")
     return err, best, s_best
+
+
+def awq_output_power(W: torch.Tensor, X: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                     out: Optional[torch.Tensor] = None, stream=None,
+                     dev_status: Optional[torch.Tensor] = None, check: bool = True) -> torch.Tensor:
+    """mean((X W^T)^2) as a [1] float64 tensor: the denominator of the
+    relative output error err / power (err from ``awq_search``)."""
+    _need(W, "W", 2)
+    _need(X, "X", 2)
+    if W.dtype != X.dtype or W.shape[1] != X.shape[1]:
+        raise ValueError("W and X must share dtype and the input dimension")
+    n_out, n_in = W.shape
+    N = X.shape[0]
+    if workspace is None:
+        need = awq_search_workspace_bytes(W.dtype, n_out, n_in, N, n_in, 1)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=W.device)
+    power = out if out is not None else torch.empty(1, dtype=torch.float64, device=W.device)
+    st = dev_status if dev_status is not None else new_status(W.device)
+    _check(lib.awq_output_power(_ptr(W), _ptr(X), DTYPE[W.dtype], n_out, n_in, N, _ptr(workspace),
+                                workspace.numel(), _ptr(power), _ptr(st), _stream(stream)),
+           "awq_output_power")
+    if check:
+        check_status(st, "awq_output_power")
+    return power
+
+
+def awq_sweep(W: torch.Tensor, X: torch.Tensor, settings, sym: bool = True, grid: int = 20):
+    """The search at several (bits, group) settings of one layer, with RTN
+    (alpha = 0, the first grid point) beside AWQ and both errors also relative
+    to mean((X W^T)^2).  ``group=None`` means one group per row.  Returns one
+    dict per setting: bits, group, best (alpha index), alpha, err_rtn,
+    err_awq, rel_rtn, rel_awq."""
+    power = float(awq_output_power(W, X).item())
+    rows = []
+    for bits, group in settings:
+        err, best, _ = awq_search(W, X, bits=bits, group=group, sym=sym, grid=grid)
+        e = err.cpu().tolist()
+        b = int(best.item())
+        rows.append(dict(bits=bits, group=group, best=b, alpha=b / grid, err_rtn=e[0],
+                         err_awq=e[b], rel_rtn=e[0] / power, rel_awq=e[b] / power))
+    return rows

@@ -24,11 +24,11 @@ constexpr int kMaxGrid = 4096;
 
 // Byte offsets of the workspace regions of awq_search (each 256-aligned).
 struct WsLayout {
-  size_t ctl, pow2, unscale, escale, inv_c, sx64, root, minmax, s32, inv_s32, xf16, partials,
-      total;
+  size_t ctl, pow2, unscale, escale, inv_c, sx64, root, minmax, s32, inv_s32, xf16, gext,
+      gext_bytes, partials, total;
 };
 
-WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int grid) {
+WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int group, int grid) {
   WsLayout w{};
   const int64_t n_alpha = grid + 1;
   const int64_t n_tiles = ((out + 127) / 128) * ((N + 255) / 256);
@@ -49,6 +49,9 @@ WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int grid) {
   w.s32 = take((size_t)n_alpha * in * 4);
   w.inv_s32 = take((size_t)n_alpha * in * 4);
   w.xf16 = take(dt == kDtF16 ? 0 : (size_t)N * in * 2);  // fp16 copy of a bf16/fp32 X
+  // extremes of groups wider than a producer job: two floats per (alpha, row, group)
+  w.gext_bytes = search_wide_group(group, in) ? (size_t)n_alpha * out * (in / group) * 8 : 0;
+  w.gext = take(w.gext_bytes);
   w.partials = take((size_t)n_alpha * n_tiles * 8);
   w.total = o;
   return w;
@@ -91,7 +94,7 @@ size_t awq_search_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N,
   if (!dtype_ok(dtype) || out < 1 || in < 1 || N < 1 || grid < 1 || grid > kMaxGrid ||
       group < 1 || in % group != 0)
     return 0;
-  return ws_layout(dtype, out, in, N, grid).total;
+  return ws_layout(dtype, out, in, N, group, grid).total;
 }
 
 int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
@@ -103,7 +106,7 @@ int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t 
   if (out < 1 || in < 1 || N < 1 || bits < 2 || bits > 8 || grid < 1 || grid > kMaxGrid ||
       group < 1 || in % group != 0)
     return AWQ_ERR_INVALID_ARG;
-  const WsLayout ws = ws_layout(dtype, out, in, N, grid);
+  const WsLayout ws = ws_layout(dtype, out, in, N, group, grid);
   if (workspace_bytes < ws.total || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
     return AWQ_ERR_INVALID_ARG;
   if (!search_supported(dtype, out, in, N, bits, group, grid)) return AWQ_ERR_UNSUPPORTED;
@@ -119,6 +122,8 @@ int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t 
   cudaError_t e = cudaMemsetAsync(absmax, 0, 8 * sizeof(uint32_t), s);
   if (e == cudaSuccess && opts && opts->diag)
     e = cudaMemsetAsync(opts->diag, 0, 4 * sizeof(uint32_t), s);
+  float* gext = ws.gext_bytes ? reinterpret_cast<float*>(wsb + ws.gext) : nullptr;
+  if (e == cudaSuccess && gext) e = cudaMemsetAsync(gext, 0, ws.gext_bytes, s);
   if (e != cudaSuccess) return AWQ_ERR_CUDA;
   int32_t* pow2_s = reinterpret_cast<int32_t*>(wsb + ws.pow2);
   float* s32 = reinterpret_cast<float*>(wsb + ws.s32);
@@ -153,13 +158,16 @@ int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t 
   if (e == cudaSuccess && x_copy) e = launch_to_f16(X, dtype, N * in, absmax + 1, wsb + ws.xf16, s);
   if (e == cudaSuccess)
     e = launch_alpha_table(sxp, ca.root, ca.inv_c, ca.escale, in, grid, s32, inv_s32, pow2_s, s);
+  if (e == cudaSuccess && gext)
+    e = launch_group_extremes(W, dtype, out, in, s32, n_alpha, group, sym, gext, s);
   if (e != cudaSuccess) return AWQ_ERR_CUDA;
   const void* xh = x_copy ? static_cast<const void*>(wsb + ws.xf16) : X;
 
-  const SearchPlan pl = plan_search(dtype, out, in, N, n_alpha, group, device_sm_count());
+  const SearchPlan pl =
+      plan_search(dtype, out, in, N, n_alpha, group, gext != nullptr, device_sm_count());
   double* partials = reinterpret_cast<double*>(wsb + ws.partials);
   e = launch_search(W, xh, dtype, out, in, N, bits, group, sym ? 1 : 0, n_alpha, s32, inv_s32,
-                    pow2_s, partials, pl, opts ? opts->wait_limit_ns : 0,
+                    pow2_s, gext, partials, pl, opts ? opts->wait_limit_ns : 0,
                     opts ? opts->test_timeout : 0, dev_status, diag, s,
                     opts ? (cudaEvent_t)opts->ev_search_start : nullptr,
                     opts ? (cudaEvent_t)opts->ev_search_stop : nullptr);
@@ -176,6 +184,51 @@ int awq_search(const void* W, const void* X, int dtype, int64_t out, int64_t in,
                int32_t* dev_status, awq_stream_t stream) {
   return awq_search_ex(W, X, dtype, out, in, N, sx, bits, group, sym, grid, workspace,
                        workspace_bytes, err, best, s_best, dev_status, stream, nullptr);
+}
+
+int awq_output_power(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
+                     void* workspace, size_t workspace_bytes, double* power, int32_t* dev_status,
+                     awq_stream_t stream) {
+  if (!W || !X || !workspace || !power || !dtype_ok(dtype)) return AWQ_ERR_INVALID_ARG;
+  if (out < 1 || in < 1 || N < 1) return AWQ_ERR_INVALID_ARG;
+  // the workspace of a one-alpha search with one group per row
+  const WsLayout ws = ws_layout(dtype, out, in, N, (int)in, 1);
+  if (workspace_bytes < ws.total || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return AWQ_ERR_INVALID_ARG;
+  if (in % 8 != 0 || out > (1 << 24) || N > (1 << 24) || in > (1 << 24))
+    return AWQ_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(W) & 15) != 0 || (reinterpret_cast<uintptr_t>(X) & 15) != 0)
+    return AWQ_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  uint32_t* ctl = reinterpret_cast<uint32_t*>(wsb + ws.ctl);
+  cudaError_t e = cudaMemsetAsync(ctl, 0, 8 * sizeof(uint32_t), s);
+  // max|W| (and max|X| for a bf16 / fp32 X) set the fp16 operand scalings
+  if (e == cudaSuccess) e = launch_absmax(W, dtype, out * in, ctl, s);
+  const bool x_copy = dtype != kDtF16;
+  if (e == cudaSuccess && x_copy) e = launch_absmax(X, dtype, N * in, ctl + 1, s);
+  if (e == cudaSuccess && x_copy) e = launch_to_f16(X, dtype, N * in, ctl + 1, wsb + ws.xf16, s);
+  float* s32 = reinterpret_cast<float*>(wsb + ws.s32);
+  float* inv_s32 = reinterpret_cast<float*>(wsb + ws.inv_s32);
+  int32_t* pow2_s = reinterpret_cast<int32_t*>(wsb + ws.pow2);
+  double* unscale = reinterpret_cast<double*>(wsb + ws.unscale);
+  // one float per row for the symmetric group maximum (the region holds two)
+  float* ext = reinterpret_cast<float*>(wsb + ws.gext);
+  if (e == cudaSuccess)
+    e = launch_power_tables(out, in, ctl, x_copy ? 1 : 0, s32, inv_s32, pow2_s, unscale, ext, s);
+  if (e != cudaSuccess) return AWQ_ERR_CUDA;
+  const void* xh = x_copy ? static_cast<const void*>(wsb + ws.xf16) : X;
+  const SearchPlan pl = plan_search(dtype, out, in, N, 1, (int)in, true, device_sm_count());
+  double* partials = reinterpret_cast<double*>(wsb + ws.partials);
+  e = launch_search(W, xh, dtype, out, in, N, 4, (int)in, 1, 1, s32, inv_s32, pow2_s, ext,
+                    partials, pl, 0, 0, dev_status, ctl + 4, s, nullptr, nullptr);
+  if (e == cudaErrorInvalidValue) return AWQ_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return AWQ_ERR_CUDA;
+  // the reduction's argmin and kept-scale outputs land in scratch words
+  e = launch_reduce_argmin(partials, unscale, 1, pl.n_tiles, (double)N * (double)out, s32, in,
+                           power, reinterpret_cast<int32_t*>(ctl + 3),
+                           reinterpret_cast<float*>(wsb + ws.sx64), dev_status, s);
+  return cuda_status(e);
 }
 
 int awq_quantize_pack(const void* W, int dtype, int64_t out, int64_t in, const float* s, int bits,

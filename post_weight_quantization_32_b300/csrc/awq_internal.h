@@ -85,6 +85,14 @@ cudaError_t launch_alpha_root(const double* sx, int64_t in, const CentreArgs& ca
 cudaError_t launch_alpha_table(const double* sx, const double* root, const double* inv_c,
                                const float* escale, int64_t in, int grid, float* s32,
                                float* inv_s32, int32_t* pow2_s, cudaStream_t s);
+// Tables for the output power mean((X W^T)^2) run as a one-alpha search:
+// s32 = 1, inv_s32 = 2^e with e from max|W| (absmax[0]), pow2_s[0] = 1,
+// unscale[0] = 2^-2(e + m_x) (m_x from absmax[1] when x_scaled), and a
+// symmetric group maximum of 2^120 for every row (ext[out]), so that every
+// code rounds to zero and the weight change is -W itself.
+cudaError_t launch_power_tables(int64_t out, int64_t in, const uint32_t* absmax, int x_scaled,
+                                float* s32, float* inv_s32, int32_t* pow2_s, double* unscale,
+                                float* ext, cudaStream_t s);
 // err[k] = unscale[k] * sum_t partials[k][t] / denom (fixed order),
 // best = strict-< argmin, s_best = s32[best].
 cudaError_t launch_reduce_argmin(const double* partials, const double* unscale, int n_alpha,
@@ -107,15 +115,34 @@ struct SearchPlan {
   size_t smem;  // dynamic shared memory bytes
   int grid;     // persistent CTAs
 };
+// Groups whose ranges are formed by launch_group_extremes ahead of the
+// search: a multiple of 256 columns (wider than one 128-column producer
+// job), or one group per row (group == in, any width).  Needs in % 8 == 0.
+bool search_wide_group(int64_t group, int64_t in);
 bool search_supported(int dt, int64_t out, int64_t in, int64_t N, int bits, int group, int grid);
+// gp: the group extremes come precomputed (launch_search with gext).
 SearchPlan plan_search(int dt, int64_t out, int64_t in, int64_t N, int n_alpha, int group,
-                       int sms);
+                       bool gp, int sms);
+// With gext != nullptr the group extremes are read from gext (layout of
+// launch_group_extremes) instead of being formed per job; group must then be
+// in or a multiple of 128 (and must be when search_wide_group holds).
 cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, int64_t in,
                           int64_t N, int bits, int group, int sym, int n_alpha,
                           const float* s32, const float* inv_s32, const int32_t* pow2_s,
-                          double* partials, const SearchPlan& plan, int64_t wait_limit_ns,
+                          const float* gext, double* partials, const SearchPlan& plan,
+                          int64_t wait_limit_ns,
                           int test_timeout, int32_t* dev_status, uint32_t* diag, cudaStream_t s,
                           cudaEvent_t ev0, cudaEvent_t ev1);
+
+// ---- group extremes for wide groups (awq_groups.cu)
+// For every alpha k < n_alpha, row and group: the extremes of
+// t = fl32(W[row][j] * s32[k][j]) over the group's columns, folded into ext
+// (zeroed by the caller): symmetric ext[(k*out + row)*ngroups + g] = max|t|;
+// asymmetric ext[2i] = -min(min t, 0), ext[2i + 1] = max(max t, 0).
+// group is a multiple of 256 or equal to in; in % 8 == 0; W 16-byte aligned.
+cudaError_t launch_group_extremes(const void* W, int dt, int64_t out, int64_t in,
+                                  const float* s32, int n_alpha, int64_t group, int sym,
+                                  float* ext, cudaStream_t s);
 
 // ---- final quantization and packing (awq_pack.cu)
 cudaError_t launch_quantize_pack(const void* W, int dt, int64_t out, int64_t in, const float* s,

@@ -15,6 +15,8 @@
 // errors are never kept ("Source code": if err < best_err).
 #include <math.h>
 
+#include <algorithm>
+
 #include "awq_alpha.cuh"
 #include "awq_device.cuh"
 #include "awq_internal.h"
@@ -164,7 +166,42 @@ __global__ void __launch_bounds__(1024) reduce_argmin_kernel(const double* __res
   }
 }
 
+// Tables of the output-power pass (see launch_power_tables).
+__global__ void __launch_bounds__(256) power_tables_kernel(int64_t out, int64_t in,
+                                                           const uint32_t* __restrict__ absmax,
+                                                           int x_scaled, float* __restrict__ s32,
+                                                           float* __restrict__ inv_s32,
+                                                           int32_t* __restrict__ pow2_s,
+                                                           double* __restrict__ unscale,
+                                                           float* __restrict__ ext) {
+  pdl_wait();
+  pdl_trigger();
+  const int e = pow2_exponent_for((double)__uint_as_float(absmax[0]));
+  const float es = ldexpf(1.0f, e);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (int64_t j = i0; j < in; j += stride) {
+    s32[j] = 1.0f;
+    inv_s32[j] = es;
+  }
+  for (int64_t r = i0; r < out; r += stride) ext[r] = 0x1p120f;
+  if (i0 == 0) {
+    const int m_x = x_scaled ? pow2_exponent_for((double)__uint_as_float(absmax[1])) : 0;
+    pow2_s[0] = 1;
+    unscale[0] = ldexp(1.0, -2 * (e + m_x));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_power_tables(int64_t out, int64_t in, const uint32_t* absmax, int x_scaled,
+                                float* s32, float* inv_s32, int32_t* pow2_s, double* unscale,
+                                float* ext, cudaStream_t s) {
+  const int64_t n = std::max(out, in);
+  const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 1024);
+  return launch_pdl(power_tables_kernel, grid, 256, 0, s, out, in, absmax, x_scaled, s32, inv_s32,
+                    pow2_s, unscale, ext);
+}
 
 size_t prep_chunks(int64_t in) { return (size_t)((in + 31) / 32); }  // the finer of the two chunkings
 

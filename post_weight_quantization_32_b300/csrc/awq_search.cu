@@ -99,6 +99,8 @@ static_assert(128 * kRegsCtl + 256 * kRegsProd + 128 * kRegsEpi <= kThreads * kL
 
 struct SearchArgs {
   const int32_t* pow2_s;  // [n_alpha]: nonzero when every scale of that alpha is a power of two
+  const float* gext;      // group extremes [n_alpha][out][ngroups] (x2 asym) for wide groups
+  int group, ngroups;
   double* partials;       // [n_alpha][n_tiles]
   int32_t* status;
   uint32_t* diag;         // 4 words: where a wait gave up
@@ -231,10 +233,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     awq_search_kernel(const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ CUtensorMap tmS, const SearchArgs p) {
-  constexpr int KBJ = (G == 128) ? 2 : 1;  // K blocks per producer job
-  constexpr int JC = KBJ * kKB;            // columns per producer job
-  constexpr int NG = JC / G;               // groups per job
-  constexpr int CPG = G / 8;               // 8-column chunks per group
+  // G == 0: groups wider than a job (a multiple of 256 columns or the whole
+  // row) whose extremes come precomputed in p.gext
+  constexpr bool GP = (G == 0);
+  constexpr int KBJ = (G == 128 || GP) ? 2 : 1;  // K blocks per producer job
+  constexpr int JC = KBJ * kKB;                  // columns per producer job
+  constexpr int NG = GP ? 1 : JC / G;            // groups per job
+  constexpr int CPG = GP ? JC / 8 : G / 8;       // 8-column chunks per group
+  constexpr int GE = GP ? JC : G;                // group width as one job sees it
   constexpr uint32_t W_TILE = w_tile_bytes<WT>();
   constexpr uint32_t FULL = 0xffffffffu;
 
@@ -417,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t wm = 0, dn = 0;  // this warpgroup's W-block and dW-slot counters
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      const int rt = u / units_per_rt;
       const int rem = u % units_per_rt;
       const int ag = rem / p.n_tt;
       const int na = min(p.a_per, p.n_alpha - ag * p.a_per);
@@ -456,7 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   __fmul2_rn(make_float2(w8[2 * e], w8[2 * e + 1]), make_float2(s8[2 * e], s8[2 * e + 1]));
               t[cgi * 8 + 2 * e] = tv.x;
               t[cgi * 8 + 2 * e + 1] = tv.y;
-              if (SYM) {
+              if (GP) {
+              } else if (SYM) {
                 r0[g][e] = fmax3f(r0[g][e], fabsf(tv.x), fabsf(tv.y));
               } else {
                 r0[g][e] = fmin3f(r0[g][e], tv.x, tv.y);
@@ -465,6 +473,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           // group steps
+          if (GP) {  // the group's extremes over all its jobs, formed ahead of the search
+            const int64_t grow = min((int64_t)rt * kRows + row, (int64_t)p.out - 1);
+            const int64_t gi = ((int64_t)(ag * p.a_per + a) * p.out + grow) * p.ngroups +
+                               (int64_t)kg * JC / p.group;
+            if (SYM) {
+              r0[0][0] = __ldg(p.gext + gi);
+            } else {
+              r0[0][0] = -__ldg(p.gext + 2 * gi);
+              r1[0][0] = __ldg(p.gext + 2 * gi + 1);
+            }
+          }
           float scl[NG], rcp[NG], chi[NG];
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
@@ -494,9 +513,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reinterpret_cast<const float*>(stg[kbi] + W_TILE) + (p.a_per + a) * kKB;
             uint32_t pk[32];
             if (exact)
-              make_dw<true, !SYM, G, JC>(t, kbi, inv_row, scl, rcp, chi, pk);
+              make_dw<true, !SYM, GE, JC>(t, kbi, inv_row, scl, rcp, chi, pk);
             else
-              make_dw<false, false, G, JC>(t, kbi, inv_row, scl, rcp, chi, pk);
+              make_dw<false, false, GE, JC>(t, kbi, inv_row, scl, rcp, chi, pk);
             tmem_st32(tmem + lane_addr + kSlotCol0 + ds * 32u, pk);
             tmem_wait_st();
             tc_fence_before();
@@ -634,7 +653,8 @@ using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMa
                           const SearchArgs);
 
 template <typename WT>
-KernelFn pick_g(int group, int sym) {
+KernelFn pick_g(int group, int sym, bool gp) {
+  if (gp) return sym ? &awq_search_kernel<WT, 0, true> : &awq_search_kernel<WT, 0, false>;
   switch (group) {
     case 32: return sym ? &awq_search_kernel<WT, 32, true> : &awq_search_kernel<WT, 32, false>;
     case 64: return sym ? &awq_search_kernel<WT, 64, true> : &awq_search_kernel<WT, 64, false>;
@@ -652,16 +672,20 @@ int max_dyn_smem() {
 
 }  // namespace
 
+bool search_wide_group(int64_t group, int64_t in) {
+  return in % 8 == 0 && group > 0 && in % group == 0 && (group % 256 == 0 || group == in);
+}
+
 bool search_supported(int dt, int64_t out, int64_t in, int64_t N, int bits, int group, int grid) {
   (void)dt; (void)bits; (void)grid;
-  if (group != 32 && group != 64 && group != 128) return false;
+  if (group != 32 && group != 64 && group != 128 && !search_wide_group(group, in)) return false;
   if (in % group != 0) return false;
   if (out > (1 << 24) || N > (1 << 24) || in > (1 << 24)) return false;
   return true;
 }
 
 SearchPlan plan_search(int dt, int64_t out, int64_t in, int64_t N, int n_alpha, int group,
-                       int sms) {
+                       bool gp, int sms) {
   SearchPlan pl{};
   pl.n_tt = (int)((N + 255) / 256);
   const int64_t per = (N + pl.n_tt - 1) / pl.n_tt;
@@ -670,9 +694,13 @@ SearchPlan plan_search(int dt, int64_t out, int64_t in, int64_t N, int n_alpha, 
   pl.n_ag = (n_alpha + pl.a_per - 1) / pl.a_per;
   pl.n_rt = (int)((out + kRows - 1) / kRows);
   pl.n_kb = (int)((in + kKB - 1) / kKB);
+  // with precomputed group ranges a job always spans two K blocks; an odd
+  // count gets one more block, which lies wholly past the last column (the
+  // tensor-map loads fill it with zeros, so it adds nothing)
+  if (gp) pl.n_kb += pl.n_kb & 1;
   pl.n_units = pl.n_rt * pl.n_ag * pl.n_tt;
   pl.n_tiles = pl.n_rt * pl.n_tt;
-  const int kbj = group == 128 ? 2 : 1;
+  const int kbj = (group == 128 || gp) ? 2 : 1;
   const size_t w_tile = (size_t)kRows * kKB * dtype_size(dt);
   pl.w_stage = align_up(w_tile + 2 * (size_t)pl.a_per * kKB * 4, 1024);
   const size_t x_stage = (size_t)pl.T * 128;
@@ -695,7 +723,8 @@ SearchPlan plan_search(int dt, int64_t out, int64_t in, int64_t N, int n_alpha, 
 cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, int64_t in,
                           int64_t N, int bits, int group, int sym, int n_alpha,
                           const float* s32, const float* inv_s32, const int32_t* pow2_s,
-                          double* partials, const SearchPlan& pl, int64_t wait_limit_ns,
+                          const float* gext, double* partials, const SearchPlan& pl,
+                          int64_t wait_limit_ns,
                           int test_timeout, int32_t* dev_status, uint32_t* diag, cudaStream_t s,
                           cudaEvent_t ev0, cudaEvent_t ev1) {
   KernelFn fn = nullptr;
@@ -703,22 +732,25 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
   uint32_t wbox;
   switch (dt) {
     case kDtF32:
-      fn = pick_g<float>(group, sym);
+      fn = pick_g<float>(group, sym, gext != nullptr);
       wt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
       wbox = 32;
       break;
     case kDtF16:
-      fn = pick_g<__half>(group, sym);
+      fn = pick_g<__half>(group, sym, gext != nullptr);
       wt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
       wbox = 64;
       break;
     default:
-      fn = pick_g<__nv_bfloat16>(group, sym);
+      fn = pick_g<__nv_bfloat16>(group, sym, gext != nullptr);
       wt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
       wbox = 64;
       break;
   }
   if (!fn || pl.sw < 2 || pl.sx < 3) return cudaErrorInvalidValue;
+  if (search_wide_group(group, in) && gext == nullptr) return cudaErrorInvalidValue;
+  if (gext != nullptr && (in % 8 != 0 || (group != in && group % (2 * kKB) != 0)))
+    return cudaErrorInvalidValue;
   const uintptr_t tbl = reinterpret_cast<uintptr_t>(inv_s32) - reinterpret_cast<uintptr_t>(s32);
   if (inv_s32 <= s32 || (tbl & 15) != 0 || (reinterpret_cast<uintptr_t>(s32) & 15) != 0)
     return cudaErrorInvalidValue;
@@ -734,6 +766,9 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
   if (e != cudaSuccess) return e;
   SearchArgs a;
   a.pow2_s = pow2_s;
+  a.gext = gext;
+  a.group = group;
+  a.ngroups = (int)(in / group);
   a.partials = partials;
   a.status = dev_status;
   a.diag = diag;

@@ -70,6 +70,10 @@ def test_workspace_query(lib):
     # bf16 and fp32 add the fp16 copy of X the tensor cores read
     assert _ws(lib, 2, 4096, 4096, 256, 128, 20) >= n + 256 * 4096 * 2
     assert _ws(lib, 0, 4096, 4096, 256, 128, 20) >= n + 256 * 4096 * 2
+    # groups wider than a producer job add their precomputed ranges (two floats
+    # per alpha, row and group)
+    assert _ws(lib, 1, 4096, 4096, 256, 256, 20) >= n + 21 * 4096 * 16 * 8
+    assert _ws(lib, 1, 4096, 4096, 256, 4096, 20) >= n + 21 * 4096 * 8
     assert _ws(lib, 2, 4096, 4096, 256, 100, 20) == 0      # group does not divide in
     assert _ws(lib, 2, 0, 4096, 256, 128, 20) == 0
     assert _ws(lib, 7, 16, 16, 16, 16, 20) == 0
@@ -99,7 +103,7 @@ def test_search_rejects_bad_arguments_on_host(lib):
     assert call(group=100) == 1          # does not divide in
     assert call(wsb=16) == 1             # workspace too small
     assert call(ws=fake + 8) == 1        # workspace not 256-byte aligned
-    assert call(group=512) == 2          # valid for the method, not handled by the search kernels
+    assert call(group=384, n_in=768) == 2  # valid for the method, not handled by the search kernels
     assert call(group=16) == 2
     assert call(W=fake + 4) == 2         # TMA needs 16-byte aligned rows
 

@@ -196,6 +196,57 @@ def test_search_matches_oracle(awq, case):
     check_pack(awq, W, res.s32[b], bits, group, sym)
 
 
+WIDE_GROUP_CASES = [
+    # (out, in, N, dtype, bits, group, sym, grid); group None = one group per row.
+    # Groups wider than a 128-column producer job take their ranges from the
+    # pass over W ahead of the search.
+    (256, 512, 64, "bf16", 4, 256, True, 10),
+    (200, 768, 40, "f16", 3, None, False, 8),
+    (130, 1024, 33, "f32", 2, 512, True, 5),
+    (64, 96, 16, "bf16", 4, None, False, 6),       # one row group narrower than one job
+    (300, 2056, 20, "bf16", 8, None, False, 4),    # ragged last K block
+    (128, 1024, 300, "f16", 4, 1024, True, 20),    # two token tiles
+    (100, 1536, 24, "bf16", 4, 768, False, 20),    # three 256-column multiples per group
+]
+
+
+@pytest.mark.parametrize("case", WIDE_GROUP_CASES, ids=lambda c: "%dx%d_n%d_%s_b%d_g%s_%s_G%d" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], "sym" if c[6] else "asym", c[7]))
+def test_search_wide_groups_match_oracle(awq, case):
+    out, n_in, N, dtype, bits, group, sym, grid = case
+    W, X = make_random_layer(out, n_in, N, dtype=dtype, seed=out + n_in + N + 7,
+                             n_outlier=max(1, n_in // 64))
+    e, b, res = check_search(awq, W, X, bits, group, sym, grid, label=str(case))
+    check_pack(awq, W, res.s32[b], bits, n_in if group is None else group, sym)
+
+
+@pytest.mark.parametrize("dtype,shape", [("f16", (256, 512, 64)), ("bf16", (300, 1032, 300)),
+                                         ("f32", (96, 256, 17)), ("bf16", (1, 64, 1))])
+def test_output_power_matches_oracle(awq, dtype, shape):
+    out, n_in, N = shape
+    W, X = make_random_layer(out, n_in, N, dtype=dtype, seed=out * 3 + N,
+                             n_outlier=max(1, n_in // 64))
+    p = float(awq.awq_output_power(*_dev(W, X)).item())
+    ref = O.output_power(_np_w(W), _np_x(X))
+    assert abs(p - ref) <= ERR_RTOL * ref, (p, ref)
+
+
+def test_sweep_matches_oracle(awq):
+    """Bit widths and group sizes of the pages' sweeps, RTN beside AWQ."""
+    W, X = make_random_layer(192, 1024, 64, dtype="bf16", seed=11, n_outlier=16)
+    settings = [(8, 128), (4, 128), (3, 128), (2, 128), (4, 32), (4, 64), (4, 256), (4, None)]
+    got = awq.awq_sweep(*_dev(W, X), settings, sym=True, grid=10)
+    ref = O.sweep(_np_w(W), _np_x(X), settings, sym=True, grid=10)
+    for g, r in zip(got, ref):
+        label = (g["bits"], g["group"])
+        if g["best"] != r["best"]:
+            assert abs(r["errs"][g["best"]] - r["err_awq"]) <= TIE_RTOL * r["err_awq"], label
+        for key in ("err_rtn", "rel_rtn"):
+            assert abs(g[key] - r[key]) <= ERR_RTOL * r[key], (label, key, g[key], r[key])
+        assert abs(g["rel_awq"] - r["rel_awq"]) <= (ERR_RTOL + TIE_RTOL) * r["rel_awq"], label
+        assert g["err_awq"] <= g["err_rtn"], label
+
+
 def test_search_shared_input_group(awq):
     """q/k/v share X and one s: the concatenated rows are searched at once."""
     ws, X = [], None
@@ -275,5 +326,5 @@ def test_search_wait_timeout_reports_and_recovers(awq):
 def test_search_rejects_unsupported_group(awq):
     W, X = make_random_layer(64, 256, 16, dtype="bf16", seed=1)
     with pytest.raises(awq.AWQError) as ei:
-        awq.awq_search(W.cuda(), X.cuda(), 4, 256, True, 20)
+        awq.awq_search(W.cuda(), X.cuda(), 4, 16, True, 20)
     assert ei.value.code == 2

@@ -316,3 +316,72 @@ def test_asym_code_formula_at_exact_ties():
     gs = O.quantize_groups(ts, 4, 8, sym=True)
     assert gs.scale[0, 0] == 0.5
     assert list(gs.q[0]) == [7.0, 0.0, 2.0, -0.0, -2.0, 2.0, 0.0, -7.0]
+
+
+# --------------------------------------------------------------------------
+# Output power and relative error (AWQ guide, "What the simulations show":
+# error is ||h W - h Wq||^2 / ||h W||^2)
+# --------------------------------------------------------------------------
+
+def test_output_power_closed_forms():
+    W = np.array([[1.0, 2.0], [3.0, 4.0]])
+    # one token of ones: the outputs are the row sums 3 and 7
+    assert O.output_power(W, np.array([[1.0, 1.0]])) == (9.0 + 49.0) / 2
+    # the identity as calibration set: the outputs are W^T itself
+    rng = np.random.default_rng(3)
+    W = rng.normal(size=(5, 8)).astype(np.float32)
+    assert np.isclose(O.output_power(W, np.eye(8)), np.mean(W.astype(np.float64) ** 2),
+                      rtol=1e-15, atol=0)
+
+
+def test_relative_error_of_dropping_the_layer_is_one():
+    rng = np.random.default_rng(4)
+    W = rng.normal(size=(6, 16)).astype(np.float32)
+    X = rng.normal(size=(9, 16))
+    ref = X @ W.astype(np.float64).T
+    assert O.output_mse(X, np.zeros(W.shape), ref) / O.output_power(W, X) == pytest.approx(1.0, rel=1e-15)
+
+
+def test_worked_example_relative_errors():
+    # the page's two-channel layer: exact output 10 * 0.5 + 0.1 * 2.0 = 5.2;
+    # AWQ (alpha = 0.5) misses it by the printed 0.033, RTN by the printed 1.67
+    W = np.array([WE["w"]], dtype=np.float32)
+    X = np.array([WE["abar"]])
+    rows = O.sweep(W, X, [(int(WE["bits"][0]), None)], grid=2)
+    r = rows[0]
+    assert r["best"] == 1 and r["alpha"] == WE["alpha"][0]
+    y = float(np.dot(WE["w"], WE["abar"]))
+    assert O.output_power(W, X) == pytest.approx(y * y, rel=1e-12)
+    for key, printed in (("rel_awq", WE["err_awq"][1]), ("rel_rtn", WE["err_rtn"][0])):
+        lo = ((printed - _tol(printed)) / y) ** 2
+        hi = ((printed + _tol(printed)) / y) ** 2
+        assert lo <= r[key] <= hi, (key, r[key], lo, hi)
+
+
+def test_sweep_rtn_column_is_plain_rtn():
+    rng = np.random.default_rng(5)
+    W = rng.normal(0, 0.02, size=(8, 64)).astype(np.float32)
+    X = rng.normal(size=(12, 64))
+    X[:, 3] *= 20.0
+    ref = X @ W.astype(np.float64).T
+    for bits, group in ((4, 32), (3, None), (8, 64)):
+        r = O.sweep(W, X, [(bits, group)], grid=4)[0]
+        g = 64 if group is None else group
+        assert r["err_rtn"] == O.output_mse(X, O.rtn_fake_quant(W, bits, g, True), ref)
+        assert r["err_awq"] <= r["err_rtn"]
+
+
+def test_relative_error_is_scale_free():
+    # W -> 2W leaves s_X alone and doubles every fl32(w * s), group step and
+    # dequantized weight exactly, so err and power both grow by exactly 4
+    rng = np.random.default_rng(6)
+    W = rng.normal(0, 0.02, size=(8, 64)).astype(np.float32)
+    X = rng.normal(size=(12, 64))
+    a = O.sweep(W, X, [(4, 32)], grid=4)[0]
+    b = O.sweep(2 * W, X, [(4, 32)], grid=4)[0]
+    assert a["best"] == b["best"]
+    assert a["rel_awq"] == b["rel_awq"] and a["rel_rtn"] == b["rel_rtn"]
+    # X -> 2X also scales s_X, up to its 1e-8 floor: equal to ~1e-7
+    c = O.sweep(W, 2 * X, [(4, 32)], grid=4)[0]
+    assert a["best"] == c["best"]
+    assert c["rel_awq"] == pytest.approx(a["rel_awq"], rel=1e-6)
