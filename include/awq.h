@@ -203,6 +203,36 @@ int awq_quantize_pack(const void* W, int dtype, int64_t out, int64_t in,
                       int32_t* dev_status, awq_stream_t stream);
 
 /*
+ * awq_export_checkpoint - the tensors a quantized checkpoint stores for one
+ * linear layer, from awq_quantize_pack's outputs.
+ * ["AWQ vs GPTQ ...", "What lands on disk": qweight int32 words packing
+ *  4-bit values; FP16 scales, one per group per output channel, shape
+ *  [in/g, out]; qzeros, packed 4-bit zero points, one per group per output
+ *  channel.  "Sizes are easy to predict": 4 bits plus a 16-bit scale and a
+ *  4-bit zero per 128 weights is about 4.16 bits per weight.]
+ *
+ *   qweight, scales, zeros   awq_quantize_pack's outputs (read), out x in
+ *                            layer, `bits` in {2, 4, 8}, in % (32/bits) == 0
+ *   qweight_t [in*bits/32][out] uint32 (written): word (k, o) holds the codes
+ *            of inputs (32/bits)k .. (32/bits)k + 32/bits - 1 of output o,
+ *            the lowest input in the lowest bits
+ *   scales_h  [in/group][out] IEEE binary16 (written): the float32 steps
+ *            rounded to nearest (ties to even); a step beyond the binary16
+ *            range (or NaN) sets AWQ_ERR_NONFINITE
+ *   qzeros    [in/group][ceil(out*bits/32)] uint32 (written): word (g, w)
+ *            holds the zero points of outputs (32/bits)w .. of group g, the
+ *            lowest output in the lowest bits, stored as they are (no offset)
+ * The pages leave the packing axis and the nibble order to the format; these
+ * are this library's.  The weights are those of W * diag(s): the scales s
+ * (s_best) are folded into whatever produces the layer's input.  Every code
+ * decodes as scale * (code - zero).
+ */
+int awq_export_checkpoint(const uint32_t* qweight, const float* scales, const uint8_t* zeros,
+                          int64_t out, int64_t in, int bits, int group,
+                          uint32_t* qweight_t, void* scales_h, uint32_t* qzeros,
+                          int32_t* dev_status, awq_stream_t stream);
+
+/*
  * awq_search_noalloc - awq_search for callers that cannot allocate device
  * memory.  (The method itself has no counterpart of this: it is a calling
  * convenience of this library.)

@@ -61,7 +61,7 @@ __all__ = [
     "channel_salience", "alpha_grid", "centred_scales", "quantize_groups",
     "quantize_groups_f64", "fake_quant", "output_mse", "awq_search", "SearchResult",
     "stored_codes", "pack_bits", "unpack_bits", "quantize_pack", "rtn_fake_quant",
-    "output_power", "sweep",
+    "output_power", "sweep", "Checkpoint", "export_checkpoint", "dequantize_checkpoint",
 ]
 
 _EPS_SALIENCE = 1e-8          # added to the mean |X| [AWQ guide, "The code, line by line"]
@@ -323,3 +323,46 @@ def quantize_pack(W, s32, bits: int, group: int, sym: bool):
     else:
         zeros = gq.zero.astype(np.uint8)
     return pack_bits(u, bits), gq.scale.copy(), zeros
+
+
+@dataclasses.dataclass
+class Checkpoint:
+    qweight: np.ndarray   # uint32 [in * b / 32, out]
+    scales: np.ndarray    # float16 [in / g, out]
+    qzeros: np.ndarray    # uint32 [in / g, out * b / 32]
+
+
+def export_checkpoint(qweight, scales, zeros, n_in: int, bits: int) -> Checkpoint:
+    """The checkpoint tensors of one quantized layer, from quantize_pack's
+    outputs.  ["AWQ vs GPTQ ...", "What lands on disk": qweight int32 words
+    packing 4-bit values, FP16 scales one per group per output channel of
+    shape [in/g, out], qzeros packed 4-bit zero points one per group per
+    output channel.]  The pages leave the packing axis and the nibble order
+    open; taken here: qweight packs 32/b consecutive input channels of one
+    output channel per word, qzeros 32/b consecutive output channels of one
+    group per word, lowest index in the lowest bits; the zero points are
+    stored as they are (no offset); scales are the float32 steps rounded to
+    float16 (nearest, ties to even).
+    """
+    if 32 % bits != 0:
+        raise ValueError("bits must divide 32")
+    per = 32 // bits
+    if n_in % per != 0:
+        raise ValueError("in must be a multiple of 32 / bits")
+    u = unpack_bits(qweight, bits, n_in)               # [out, in] codes
+    # word k of output o: inputs per*k .. per*k + per - 1, lowest in the lowest bits
+    qw = np.ascontiguousarray(pack_bits(u, bits).T)    # [in / per, out]
+    sc = np.asarray(scales, dtype=np.float32).T.astype(np.float16)
+    qz = pack_bits(np.ascontiguousarray(np.asarray(zeros, dtype=np.uint32).T), bits)
+    return Checkpoint(qw, sc, qz)
+
+
+def dequantize_checkpoint(ck: Checkpoint, n_out: int, n_in: int, bits: int, group: int):
+    """W_hat[o, i] = scale * (code - zero) from the checkpoint tensors, float64
+    [out, in] (of W * diag(s): the scales s are folded elsewhere)."""
+    per = 32 // bits
+    codes = unpack_bits(ck.qweight.T.copy(), bits, per * ck.qweight.shape[0])  # [out, in]
+    zeros = unpack_bits(ck.qzeros, bits, n_out)                                # [in/g, out]
+    scale = ck.scales.astype(np.float64)                                       # [in/g, out]
+    gi = np.arange(n_in) // group
+    return scale[gi, :].T * (codes[:, :n_in].astype(np.float64) - zeros[gi, :].T.astype(np.float64))

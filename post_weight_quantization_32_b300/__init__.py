@@ -30,6 +30,7 @@ __all__ = [
     "AWQError", "SearchOpts", "lib", "awq_channel_stats", "awq_search",
     "awq_search_workspace_bytes", "awq_quantize_pack", "new_status", "check_status", "STATUS",
     "DTYPE", "awq_search_noalloc", "NOALLOC_SCRATCH_BYTES", "awq_output_power", "awq_sweep",
+    "awq_export_checkpoint",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -40,7 +41,8 @@ STATUS = {0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARG", 2: "AWQ_ERR_UNSUPPORTED", 3: "A
           4: "AWQ_ERR_TIMEOUT", 5: "AWQ_ERR_CUDA"}
 
 EXPORTS = ("awq_status_string", "awq_channel_stats", "awq_search_workspace_bytes", "awq_search",
-           "awq_search_ex", "awq_quantize_pack", "awq_search_noalloc", "awq_output_power")
+           "awq_search_ex", "awq_quantize_pack", "awq_search_noalloc", "awq_output_power",
+           "awq_export_checkpoint")
 
 # Size of the library's fixed scratch array used by awq_search_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -66,6 +68,8 @@ def _load() -> ctypes.CDLL:
     L.awq_quantize_pack.argtypes = [vp, i32, i64, i64, vp, i32, i32, i32, vp, vp, vp, vp, vp]
     L.awq_output_power.restype = i32
     L.awq_output_power.argtypes = [vp, vp, i32, i64, i64, i64, vp, sz, vp, vp, vp]
+    L.awq_export_checkpoint.restype = i32
+    L.awq_export_checkpoint.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, vp]
     L.awq_search_noalloc.restype = i32
     L.awq_search_noalloc.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, i32, vp, vp, vp,
                                      vp, vp]
@@ -272,3 +276,26 @@ def awq_sweep(W: torch.Tensor, X: torch.Tensor, settings, sym: bool = True, grid
         rows.append(dict(bits=bits, group=group, best=b, alpha=b / grid, err_rtn=e[0],
                          err_awq=e[b], rel_rtn=e[0] / power, rel_awq=e[b] / power))
     return rows
+
+
+def awq_export_checkpoint(qweight: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+                          n_in: int, bits: int = 4, group: Optional[int] = None, stream=None,
+                          dev_status: Optional[torch.Tensor] = None, check: bool = True):
+    """Checkpoint tensors of one layer from ``awq_quantize_pack``'s outputs:
+    (qweight [in*b/32, out] int32, scales [in/g, out] float16, qzeros
+    [in/g, ceil(out*b/32)] int32); see awq_export_checkpoint in awq.h for the
+    bit layout."""
+    _need(qweight, "qweight", 2)
+    n_out = qweight.shape[0]
+    g = n_in if group is None else int(group)
+    dev = qweight.device
+    qw_t = torch.empty((n_in * bits // 32, n_out), dtype=torch.int32, device=dev)
+    sc_h = torch.empty((n_in // g, n_out), dtype=torch.float16, device=dev)
+    qz = torch.empty((n_in // g, (n_out * bits + 31) // 32), dtype=torch.int32, device=dev)
+    st = dev_status if dev_status is not None else new_status(dev)
+    _check(lib.awq_export_checkpoint(_ptr(qweight), _ptr(scales), _ptr(zeros), n_out, n_in, bits,
+                                     g, _ptr(qw_t), _ptr(sc_h), _ptr(qz), _ptr(st),
+                                     _stream(stream)), "awq_export_checkpoint")
+    if check:
+        check_status(st, "awq_export_checkpoint")
+    return qw_t, sc_h, qz

@@ -241,4 +241,18 @@ int awq_quantize_pack(const void* W, int dtype, int64_t out, int64_t in, const f
                                           scales, zeros, dev_status, (cudaStream_t)stream));
 }
 
+int awq_export_checkpoint(const uint32_t* qweight, const float* scales, const uint8_t* zeros,
+                          int64_t out, int64_t in, int bits, int group, uint32_t* qweight_t,
+                          void* scales_h, uint32_t* qzeros, int32_t* dev_status,
+                          awq_stream_t stream) {
+  if (!qweight || !scales || !zeros || !qweight_t || !scales_h || !qzeros)
+    return AWQ_ERR_INVALID_ARG;
+  if (out < 1 || in < 1 || group < 1 || in % group != 0) return AWQ_ERR_INVALID_ARG;
+  if (bits != 2 && bits != 4 && bits != 8) return AWQ_ERR_INVALID_ARG;
+  if (in % (32 / bits) != 0) return AWQ_ERR_INVALID_ARG;
+  return cuda_status(launch_export_checkpoint(qweight, scales, zeros, out, in, bits, group,
+                                              qweight_t, scales_h, qzeros, dev_status,
+                                              (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -149,4 +149,14 @@ cudaError_t launch_quantize_pack(const void* W, int dt, int64_t out, int64_t in,
                                  int bits, int group, int sym, uint32_t* qweight, float* scales,
                                  uint8_t* zeros, int32_t* dev_status, cudaStream_t st);
 
+// ---- checkpoint export (awq_export.cu)
+// From quantize_pack's row-major outputs (bits divides 32, in % (32/bits) ==
+// 0): qweight_t [in*bits/32][out] (transposed words), scales_h [in/g][out]
+// fp16 (rounded to nearest; overflow sets ST_NONFINITE), qzeros
+// [in/g][ceil(out*bits/32)] (zero points packed along the output axis).
+cudaError_t launch_export_checkpoint(const uint32_t* qweight, const float* scales,
+                                     const uint8_t* zeros, int64_t out, int64_t in, int bits,
+                                     int group, uint32_t* qweight_t, void* scales_h,
+                                     uint32_t* qzeros, int32_t* dev_status, cudaStream_t s);
+
 }  // namespace awq

@@ -247,6 +247,31 @@ def test_sweep_matches_oracle(awq):
         assert g["err_awq"] <= g["err_rtn"], label
 
 
+@pytest.mark.parametrize("bits,group,sym,dtype", [(4, 128, False, "bf16"), (4, 128, True, "f16"),
+                                                  (2, 64, False, "bf16"), (8, 32, True, "f32"),
+                                                  (4, 256, False, "bf16")])
+def test_export_checkpoint_matches_oracle(awq, bits, group, sym, dtype):
+    out, n_in = 72, 512   # 72 outputs: a partial 32-wide tile and, at 4 bits, 9 zero words
+    W, _ = make_random_layer(out, n_in, 2, dtype=dtype, seed=bits * group)
+    s32 = np.random.default_rng(group).uniform(0.2, 5.0, size=n_in).astype(np.float32)
+    qw, sc, z = awq.awq_quantize_pack(W.cuda(), torch.from_numpy(s32).cuda(), bits, group, sym)
+    qw_t, sc_h, qz = awq.awq_export_checkpoint(qw, sc, z, n_in, bits, group)
+    ref = O.export_checkpoint(*O.quantize_pack(_np_w(W), s32, bits, group, sym), n_in, bits)
+    assert np.array_equal(qw_t.cpu().numpy().view(np.uint32), ref.qweight)
+    assert np.array_equal(sc_h.cpu().numpy().view(np.uint16), ref.scales.view(np.uint16))
+    assert np.array_equal(qz.cpu().numpy().view(np.uint32), ref.qzeros)
+
+
+def test_export_checkpoint_reports_fp16_overflow(awq):
+    W, _ = make_random_layer(8, 128, 2, dtype="f32", seed=2)
+    W = W.clone()
+    W[3, 7] = 1.0e6   # its group's step, 1e6 / 7, is beyond the binary16 range
+    qw, sc, z = awq.awq_quantize_pack(W.cuda(), torch.ones(128, device="cuda"), 4, 128, True)
+    st = awq.new_status()
+    awq.awq_export_checkpoint(qw, sc, z, 128, 4, 128, dev_status=st, check=False)
+    assert int(st.item()) == 3
+
+
 def test_search_shared_input_group(awq):
     """q/k/v share X and one s: the concatenated rows are searched at once."""
     ws, X = [], None

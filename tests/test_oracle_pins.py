@@ -385,3 +385,52 @@ def test_relative_error_is_scale_free():
     c = O.sweep(W, 2 * X, [(4, 32)], grid=4)[0]
     assert a["best"] == c["best"]
     assert c["rel_awq"] == pytest.approx(a["rel_awq"], rel=1e-6)
+
+
+# --------------------------------------------------------------------------
+# Checkpoint tensors ("AWQ vs GPTQ ...", "What lands on disk")
+# --------------------------------------------------------------------------
+
+def test_checkpoint_layout_by_hand():
+    # two output channels of eight inputs, 4-bit codes 0..7 and 15..8
+    u = np.array([list(range(8)), list(range(15, 7, -1))], dtype=np.uint32)
+    qw = O.pack_bits(u, 4)
+    ck = O.export_checkpoint(qw, np.array([[0.5], [2.0]], np.float32),
+                             np.array([[3], [12]], np.uint8), 8, 4)
+    assert ck.qweight.shape == (1, 2)
+    assert int(ck.qweight[0, 0]) == 0x76543210 and int(ck.qweight[0, 1]) == 0x89ABCDEF
+    assert ck.scales.dtype == np.float16 and ck.scales.tolist() == [[0.5, 2.0]]
+    assert ck.qzeros.shape == (1, 1) and int(ck.qzeros[0, 0]) == 0xC3
+
+
+def test_checkpoint_size_matches_the_pages_arithmetic():
+    # 4 bits plus a 16-bit scale and a 4-bit zero per 128 weights: "about 4.16
+    # bits per weight"; 6.98B decoder weights then take "3.63 GB"
+    out, n_in, g = 256, 1024, 128
+    rng = np.random.default_rng(7)
+    W = rng.normal(0, 0.02, size=(out, n_in)).astype(np.float32)
+    qw, sc, z = O.quantize_pack(W, np.ones(n_in, np.float32), 4, g, False)
+    ck = O.export_checkpoint(qw, sc, z, n_in, 4)
+    nbytes = ck.qweight.nbytes + ck.scales.nbytes + ck.qzeros.nbytes
+    bpw = nbytes * 8 / (out * n_in)
+    assert bpw == 4 + 16 / 128 + 4 / 128
+    assert abs(bpw - 4.16) <= 0.005
+    # half a unit of the printed 3.63, plus what half a unit of 6.98B moves it
+    assert abs(6.98e9 * bpw / 8 / 1e9 - 3.63) <= 0.005 + 0.005e9 * bpw / 8 / 1e9
+
+
+@pytest.mark.parametrize("sym", [True, False])
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_checkpoint_dequantizes_to_the_quantized_weights(sym, bits):
+    out, n_in, g = 24, 256, 64
+    rng = np.random.default_rng(bits)
+    W = rng.normal(0, 0.02, size=(out, n_in)).astype(np.float32)
+    s32 = rng.uniform(0.5, 4.0, size=n_in).astype(np.float32)
+    qw, sc, z = O.quantize_pack(W, s32, bits, g, sym)
+    ck = O.export_checkpoint(qw, sc, z, n_in, bits)
+    Wh = O.dequantize_checkpoint(ck, out, n_in, bits, g)
+    gq = O.quantize_groups(W * s32[None, :], bits, g, sym)
+    # equal but for the rounding of each step to float16 (relative 2^-11)
+    levels = np.abs(gq.q.astype(np.float64) - (0 if sym else gq.zero.repeat(g, axis=1)))
+    bound = levels * np.repeat(gq.scale, g, axis=1) * 2.0 ** -11 + 1e-12
+    assert np.all(np.abs(Wh - gq.w_hat) <= bound)
