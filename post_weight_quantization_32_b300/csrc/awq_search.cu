@@ -99,8 +99,6 @@ static_assert(128 * kRegsCtl + 256 * kRegsProd + 128 * kRegsEpi <= kThreads * kL
 
 struct SearchArgs {
   const int32_t* pow2_s;  // [n_alpha]: nonzero when every scale of that alpha is a power of two
-  const float* gext;      // group extremes [n_alpha][out][ngroups] (x2 asym) for wide groups
-  int group, ngroups;
   double* partials;       // [n_alpha][n_tiles]
   int32_t* status;
   uint32_t* diag;         // 4 words: where a wait gave up
@@ -111,6 +109,13 @@ struct SearchArgs {
   float Lf, maxqf;
   uint64_t wait_limit_ns;
   int test_timeout;
+};
+
+// Precomputed group ranges, read only by the wide-group instantiations (kept
+// out of SearchArgs, which the other kernels read on every job).
+struct WideArgs {
+  const float* gext;  // group extremes [n_alpha][out][ngroups] (x2 asym)
+  int group, ngroups;
 };
 
 struct Ctrl {
@@ -232,7 +237,8 @@ template <typename WT, int G, bool SYM>
 __global__ void __launch_bounds__(kThreads, 1)
     awq_search_kernel(const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmX,
-                      const __grid_constant__ CUtensorMap tmS, const SearchArgs p) {
+                      const __grid_constant__ CUtensorMap tmS, const SearchArgs p,
+                      const WideArgs wa) {
   // G == 0: groups wider than a job (a multiple of 256 columns or the whole
   // row) whose extremes come precomputed in p.gext
   constexpr bool GP = (G == 0);
@@ -423,7 +429,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t wm = 0, dn = 0;  // this warpgroup's W-block and dW-slot counters
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      const int rt = u / units_per_rt;
       const int rem = u % units_per_rt;
       const int ag = rem / p.n_tt;
       const int na = min(p.a_per, p.n_alpha - ag * p.a_per);
@@ -463,25 +468,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                   __fmul2_rn(make_float2(w8[2 * e], w8[2 * e + 1]), make_float2(s8[2 * e], s8[2 * e + 1]));
               t[cgi * 8 + 2 * e] = tv.x;
               t[cgi * 8 + 2 * e + 1] = tv.y;
-              if (GP) {
-              } else if (SYM) {
-                r0[g][e] = fmax3f(r0[g][e], fabsf(tv.x), fabsf(tv.y));
-              } else {
-                r0[g][e] = fmin3f(r0[g][e], tv.x, tv.y);
-                r1[g][e] = fmax3f(r1[g][e], tv.x, tv.y);
+              if constexpr (!GP) {
+                if (SYM) {
+                  r0[g][e] = fmax3f(r0[g][e], fabsf(tv.x), fabsf(tv.y));
+                } else {
+                  r0[g][e] = fmin3f(r0[g][e], tv.x, tv.y);
+                  r1[g][e] = fmax3f(r1[g][e], tv.x, tv.y);
+                }
               }
             }
           }
           // group steps
-          if (GP) {  // the group's extremes over all its jobs, formed ahead of the search
-            const int64_t grow = min((int64_t)rt * kRows + row, (int64_t)p.out - 1);
-            const int64_t gi = ((int64_t)(ag * p.a_per + a) * p.out + grow) * p.ngroups +
-                               (int64_t)kg * JC / p.group;
+          if constexpr (GP) {  // the group's extremes over all its jobs, formed ahead of the search
+            const int64_t grow =
+                min((int64_t)(u / units_per_rt) * kRows + row, (int64_t)p.out - 1);
+            const int64_t gi = ((int64_t)(ag * p.a_per + a) * p.out + grow) * wa.ngroups +
+                               (int64_t)kg * JC / wa.group;
             if (SYM) {
-              r0[0][0] = __ldg(p.gext + gi);
+              r0[0][0] = __ldg(wa.gext + gi);
             } else {
-              r0[0][0] = -__ldg(p.gext + 2 * gi);
-              r1[0][0] = __ldg(p.gext + 2 * gi + 1);
+              r0[0][0] = -__ldg(wa.gext + 2 * gi);
+              r1[0][0] = __ldg(wa.gext + 2 * gi + 1);
             }
           }
           float scl[NG], rcp[NG], chi[NG];
@@ -650,7 +657,7 @@ bool make_scale_map(CUtensorMap* m, const float* s32, uint64_t in, uint64_t n_al
 }
 
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
-                          const SearchArgs);
+                          const SearchArgs, const WideArgs);
 
 template <typename WT>
 KernelFn pick_g(int group, int sym, bool gp) {
@@ -766,9 +773,6 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
   if (e != cudaSuccess) return e;
   SearchArgs a;
   a.pow2_s = pow2_s;
-  a.gext = gext;
-  a.group = group;
-  a.ngroups = (int)(in / group);
   a.partials = partials;
   a.status = dev_status;
   a.diag = diag;
@@ -792,7 +796,12 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
   a.wait_limit_ns = (uint64_t)(wait_limit_ns > 0 ? wait_limit_ns : 2000000000LL);
   a.test_timeout = test_timeout;
   if (ev0 && (e = cudaEventRecord(ev0, s)) != cudaSuccess) return e;
-  e = launch_pdl(fn, dim3((unsigned)pl.grid), dim3(kThreads), (size_t)pl.smem, s, mw, mx, ms, a);
+  WideArgs wa;
+  wa.gext = gext;
+  wa.group = group;
+  wa.ngroups = (int)(in / group);
+  e = launch_pdl(fn, dim3((unsigned)pl.grid), dim3(kThreads), (size_t)pl.smem, s, mw, mx, ms, a,
+                 wa);
   if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
   return e;
 }

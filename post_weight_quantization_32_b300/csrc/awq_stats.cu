@@ -288,10 +288,12 @@ cudaError_t stats_dispatch(const void* X, int64_t N, int64_t in, double* sx, uin
   if (std::is_same<T, __half>::value && xmax != nullptr) return cudaErrorInvalidValue;
   if (vec && (W == nullptr || wvec)) {
     const int nx = (int)((in + kStatCols - 1) / kStatCols);
-    // max|W| blocks: about eight 16-byte loads per thread, all in flight at once
+    // max|W| blocks: eight 16-byte loads in flight per thread; at most four
+    // CTAs per SM, so that they and the statistics CTAs are resident at once
+    // (no second wave)
     const int nw =
         W != nullptr ? (int)std::max<int64_t>(1, std::min<int64_t>((nW / 8 + 2047) / 2048,
-                                                                   device_sm_count() * 8))
+                                                                   device_sm_count() * 4))
                      : 0;
     stats_vec_kernel<T><<<(unsigned)(nx + nw), 256, 0, s>>>(
         static_cast<const T*>(X), N, in, sx, xmax, static_cast<const T*>(W), nW, wmax, nx, ca);
