@@ -40,6 +40,12 @@ from synthetic import CONFIGS, config_by_name, make_layer  # noqa: E402
 DEFAULT_CONFIG = "nb-4096x4096-n256"
 METRIC = "AWQ search layer-alpha-evals/sec"
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one search-kernel
+# launch, from an ncu capture of this kernel build on that workload; None where
+# no capture of the current kernel exists.  A value far above W + X (each read
+# once) would mean wasted re-reads.
+SEARCH_TRAFFIC_BYTES = {"nb-4096x4096-n256": 36_407_808 + 3_328}
+
 
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -279,7 +285,9 @@ def main():
     e2e_v = n_alpha * world / (r["e2e_ms"] * 1e-3)
     achieved = flops / (r["search_ms"] * 1e-3) / 1e12
     cpu_t, cpu_n = run_oracle_sample(cfg, args.cpu_sample)
-    launches_per_step = 6 + (0 if cfg.dtype == "f16" else 1)
+    # statistics (with max|W| and the centring), alpha table, search, argmin, pack;
+    # a bf16 or fp32 X adds its fp16 copy
+    launches_per_step = 5 + (0 if cfg.dtype == "f16" else 1)
     line = {
         "metric": METRIC, "value": value, "unit": "layer-alpha-evals/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
@@ -288,7 +296,7 @@ def main():
         "gflops": flops / (r["ms"] * 1e-3) / 1e9,
         "search_kernel_ms": r["search_ms"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
-                     "frac": achieved / tflops_peak, "traffic": None,
+                     "frac": achieved / tflops_peak, "traffic": SEARCH_TRAFFIC_BYTES.get(cfg.name),
                      "kernel": "awq_search_kernel", "peak_kind": peak_kind + " (bf16 dense = fp16 dense)"},
         "cpu_baseline": {"value": cpu_n / cpu_t, "unit": "layer-alpha-evals/s", "cores": _cores(),
                          "kind": "oracle",
