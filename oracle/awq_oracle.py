@@ -62,6 +62,7 @@ __all__ = [
     "quantize_groups_f64", "fake_quant", "output_mse", "awq_search", "SearchResult",
     "stored_codes", "pack_bits", "unpack_bits", "quantize_pack", "rtn_fake_quant",
     "output_power", "sweep", "Checkpoint", "export_checkpoint", "dequantize_checkpoint",
+    "clip_factors", "quantize_groups_clipped", "ClipResult", "clip_search",
 ]
 
 _EPS_SALIENCE = 1e-8          # added to the mean |X| [AWQ guide, "The code, line by line"]
@@ -366,3 +367,94 @@ def dequantize_checkpoint(ck: Checkpoint, n_out: int, n_in: int, bits: int, grou
     scale = ck.scales.astype(np.float64)                                       # [in/g, out]
     gi = np.arange(n_in) // group
     return scale[gi, :].T * (codes[:, :n_in].astype(np.float64) - zeros[gi, :].T.astype(np.float64))
+
+
+# --------------------------------------------------------------------------
+# Per-group clipping search at fixed scales
+# --------------------------------------------------------------------------
+
+def clip_factors(n_grid: int = 20, max_shrink: float = 0.5) -> np.ndarray:
+    """The shrink factors tried for each group's range: 1, 1 - 1/n_grid, ...,
+    down to 1 - max_shrink, as float32.  c = 1 (no clipping) comes first, so
+    with a strict comparison clipping is kept only when it lowers the error.
+
+    The pages give the step in words only ("searches a clipping threshold
+    per group, shrinking the max range to cut rounding error", AWQ guide,
+    "Simplifications"; "a second search then shrinks each group's clipping
+    range a little when that lowers output error", comparison page, "AWQ:
+    move the error away from what matters"); the grid is this library's
+    reading.
+    """
+    k = int(round(max_shrink * n_grid))
+    return np.array([1.0 - i / n_grid for i in range(k + 1)], dtype=np.float32)
+
+
+def quantize_groups_clipped(t: np.ndarray, bits: int, group: int, sym: bool,
+                            c: np.ndarray) -> GroupQuant:
+    """The float32 group quantizer with each group's range scaled by its
+    factor c[row, group] (float32): symmetric m = fl32(c * max|t|); asymmetric
+    lo = fl32(c * min(min t, 0)), hi = fl32(c * max(max t, 0)).  Values
+    beyond the shrunk range take the end codes (the clamps of the quantizer).
+    With c = 1 this is quantize_groups exactly.
+    """
+    t = np.asarray(t, dtype=np.float32)
+    out, n_in = t.shape
+    ng = n_in // group
+    tg = t.reshape(out, ng, group)
+    c = np.asarray(c, dtype=np.float32).reshape(out, ng)
+    if sym:
+        L = np.float32((1 << (bits - 1)) - 1)
+        m = (c * np.abs(tg).max(-1)).astype(np.float32)
+        scale = np.maximum((m / L).astype(np.float32), _EPS_SCALE)
+        q = np.clip(np.round((tg / scale[..., None]).astype(np.float32)), -L - 1, L)
+        zero = np.zeros_like(scale)
+        w_hat = (q * scale[..., None]).astype(np.float32)
+    else:
+        maxq = np.float32((1 << bits) - 1)
+        lo = (c * np.minimum(tg.min(-1), np.float32(0))).astype(np.float32)
+        hi = (c * np.maximum(tg.max(-1), np.float32(0))).astype(np.float32)
+        scale = np.maximum(((hi - lo).astype(np.float32) / maxq).astype(np.float32), _EPS_SCALE)
+        zero = np.round((-lo / scale).astype(np.float32))
+        q = np.clip(np.round((tg / scale[..., None]).astype(np.float32)) + zero[..., None], 0, maxq)
+        w_hat = (scale[..., None] * (q - zero[..., None])).astype(np.float32)
+    return GroupQuant(q.reshape(out, n_in), scale, zero, w_hat.reshape(out, n_in))
+
+
+@dataclasses.dataclass
+class ClipResult:
+    factors: np.ndarray   # float32 [n_c]
+    errs: np.ndarray      # float64 [out, in/g, n_c]: each group's share of its row's output error
+    best: np.ndarray      # int [out, in/g]: index of the kept factor
+
+
+def clip_search(W, X, s32, bits: int, group: int, sym: bool, n_grid: int = 20,
+                max_shrink: float = 0.5) -> ClipResult:
+    """For each row r and group G of W * s (s fixed, e.g. the kept AWQ
+    scales) and each shrink factor c, the group's own share of the row's
+    output error, sum_n (sum_{j in G} X[n, j] * (Wq[r, j] - W[r, j]))^2 with
+    Wq = Q_c(W * s) / s, in float64; the kept factor is the first with the
+    smallest share (strict <).  The shares of different groups of a row do
+    not add up to the row's error (cross terms), which is why each group is
+    judged on its own share.
+    """
+    W32 = np.asarray(W, dtype=np.float32)
+    X64 = np.asarray(X, dtype=np.float64)
+    s32 = np.asarray(s32, dtype=np.float32)
+    out, n_in = W32.shape
+    ng = n_in // group
+    t = W32 * s32[None, :]
+    cs = clip_factors(n_grid, max_shrink)
+    errs = np.empty((out, ng, cs.size))
+    for i, c in enumerate(cs):
+        gq = quantize_groups_clipped(t, bits, group, sym, np.full((out, ng), c, np.float32))
+        dW = gq.w_hat.astype(np.float64) / s32.astype(np.float64)[None, :] - W32.astype(np.float64)
+        for g in range(ng):
+            sl = slice(g * group, (g + 1) * group)
+            errs[:, g, i] = np.sum((X64[:, sl] @ dW[:, sl].T) ** 2, axis=0)
+    best = np.zeros((out, ng), dtype=np.int64)
+    best_err = np.full((out, ng), np.inf)
+    for i in range(cs.size):
+        better = errs[:, :, i] < best_err
+        best[better] = i
+        best_err[better] = errs[:, :, i][better]
+    return ClipResult(cs, errs, best)

@@ -434,3 +434,63 @@ def test_checkpoint_dequantizes_to_the_quantized_weights(sym, bits):
     levels = np.abs(gq.q.astype(np.float64) - (0 if sym else gq.zero.repeat(g, axis=1)))
     bound = levels * np.repeat(gq.scale, g, axis=1) * 2.0 ** -11 + 1e-12
     assert np.all(np.abs(Wh - gq.w_hat) <= bound)
+
+
+# --------------------------------------------------------------------------
+# Per-group clipping search (AWQ guide, "Simplifications"; comparison page,
+# "AWQ: move the error away from what matters")
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("sym", [True, False])
+def test_clip_factor_one_is_the_plain_quantizer(sym):
+    rng = np.random.default_rng(8)
+    t = rng.normal(0, 0.05, size=(6, 96)).astype(np.float32)
+    a = O.quantize_groups(t, 3, 32, sym)
+    b = O.quantize_groups_clipped(t, 3, 32, sym, np.ones((6, 3), np.float32))
+    for x, y in ((a.q, b.q), (a.scale, b.scale), (a.zero, b.zero), (a.w_hat, b.w_hat)):
+        assert np.array_equal(x, y)
+
+
+def test_clip_search_by_hand_keeps_no_clipping():
+    # one group [1.0, 0.4], X = I, 3-bit symmetric (L = 3):
+    #   c = 1:    step 1/3,    codes [3, 1] -> [1, 1/3],       share (0.4 - 1/3)^2
+    #   c = 0.95: step 0.95/3, codes [3, 1] -> [0.95, 0.95/3], share 0.05^2 + (0.4 - 0.95/3)^2
+    #   c = 0.8:  step 0.8/3,  codes [3 (3.75 clamped), 2]    share 0.2^2 + (0.4 - 1.6/3)^2
+    W = np.array([[1.0, 0.4]], np.float32)
+    r = O.clip_search(W, np.eye(2), np.ones(2, np.float32), 3, 2, True)
+    e = r.errs[0, 0]
+    assert e[0] == pytest.approx((0.4 - 1 / 3) ** 2, rel=1e-6)
+    assert e[1] == pytest.approx(0.05 ** 2 + (0.4 - 0.95 / 3) ** 2, rel=1e-5)
+    assert e[4] == pytest.approx(0.2 ** 2 + (0.4 - 1.6 / 3) ** 2, rel=1e-5)
+    assert r.best[0, 0] == 0
+
+
+def test_clip_search_by_hand_clips_an_outlier():
+    # one group [1.0, 0.5, 0.5], X = I, 2-bit symmetric (L = 1): without
+    # clipping the step is 1 and both 0.5 round to 0 (ties to even), share
+    # 0.5; with 0.5 < c < 1 every value lands on the code for c, share
+    # (1 - c)^2 + 2 (0.5 - c)^2, least on the grid at c = 0.65 (0.1675)
+    W = np.array([[1.0, 0.5, 0.5]], np.float32)
+    r = O.clip_search(W, np.eye(3), np.ones(3, np.float32), 2, 3, True)
+    c = r.factors.astype(np.float64)
+    e = r.errs[0, 0]
+    assert e[0] == pytest.approx(0.5, rel=1e-12)
+    for i in range(1, 10):
+        assert e[i] == pytest.approx((1 - c[i]) ** 2 + 2 * (0.5 - c[i]) ** 2, rel=1e-6)
+    assert r.factors[r.best[0, 0]] == np.float32(0.65)
+
+
+@pytest.mark.parametrize("sym", [True, False])
+def test_clip_share_of_a_whole_row_group_is_the_row_error(sym):
+    # with one group per row the group's share is the row's whole output error
+    rng = np.random.default_rng(9)
+    W = rng.normal(0, 0.02, size=(5, 64)).astype(np.float32)
+    X = rng.normal(size=(7, 64))
+    s32 = rng.uniform(0.5, 2.0, size=64).astype(np.float32)
+    r = O.clip_search(W, X, s32, 3, 64, sym, n_grid=10, max_shrink=0.3)
+    ref = X @ W.astype(np.float64).T
+    for i, c in enumerate(r.factors):
+        gq = O.quantize_groups_clipped(W * s32[None, :], 3, 64, sym, np.full((5, 1), c, np.float32))
+        Wq = gq.w_hat.astype(np.float64) / s32.astype(np.float64)[None, :]
+        per_row = np.sum((X @ Wq.T - ref) ** 2, axis=0)
+        assert np.allclose(r.errs[:, 0, i], per_row, rtol=1e-10, atol=0)
