@@ -203,6 +203,55 @@ int awq_quantize_pack(const void* W, int dtype, int64_t out, int64_t in,
                       int32_t* dev_status, awq_stream_t stream);
 
 /*
+ * awq_clip_search - per-group clipping search at fixed scales.
+ * ["AWQ (activation-aware weight quantization)", "Simplifications": the
+ *  method also searches a clipping threshold per group, shrinking the max
+ *  range to cut rounding error; "AWQ vs GPTQ ...", "AWQ: move the error away
+ *  from what matters": a second search shrinks each group's clipping range
+ *  when that lowers output error.]
+ *
+ * For every row r and group G of W * diag(s) and each factor
+ *   c_i = 1 - i / n_grid,  i = 0 .. max_shrink_steps   (rounded to float32)
+ * the group's range is scaled by c_i (symmetric: max|t|; asymmetric: the
+ * min(min t, 0) and max(max t, 0) ends), the group is quantized with the
+ * quantizer's clamps, and the group's own share of the row's output error
+ *   e = sum_n (sum_{j in G} X[n, j] (Wq[r, j] - W[r, j]))^2
+ * is formed.  clip[r][G] receives the first factor with the smallest share
+ * (strict <; c_0 = 1, no clipping, is kept unless clipping lowers it).
+ *
+ *   W, X, dtype, out, in, N   as for awq_search; s [in] float (e.g. s_best)
+ *   bits, group, sym          as for awq_quantize_pack; group in {32, 64, 128}
+ *                             (others: AWQ_ERR_UNSUPPORTED)
+ *   n_grid >= 1, 0 <= max_shrink_steps < n_grid, max_shrink_steps <= 11
+ *   workspace, workspace_bytes >= awq_clip_search_workspace_bytes(in, N, group)
+ *   clip   [out][in/group] float (written): the kept factors
+ *   errs   [out][in/group][max_shrink_steps + 1] float (written) or NULL
+ * The shares are formed as d^T H_G d with the group's Gram matrix
+ * H_G = X_G^T X_G (fp32 sums in a fixed order), d = Wq - W in fp32.
+ * Pass clip to awq_quantize_pack_clipped for the codes.
+ */
+size_t awq_clip_search_workspace_bytes(int64_t in, int64_t N, int group);
+
+int awq_clip_search(const void* W, const void* X, int dtype,
+                    int64_t out, int64_t in, int64_t N, const float* s,
+                    int bits, int group, int sym, int n_grid, int max_shrink_steps,
+                    void* workspace, size_t workspace_bytes,
+                    float* clip, float* errs, int32_t* dev_status, awq_stream_t stream);
+
+/*
+ * awq_quantize_pack_clipped - awq_quantize_pack with each group's range
+ * scaled by clip[out][in/group] (float, e.g. from awq_clip_search) before its
+ * step and zero point are formed: symmetric m = fl32(c * max|t|), asymmetric
+ * lo = fl32(c * min(min t, 0)), hi = fl32(c * max(max t, 0)); values beyond
+ * the shrunk range take the end codes.  Same outputs and errors as
+ * awq_quantize_pack.
+ */
+int awq_quantize_pack_clipped(const void* W, int dtype, int64_t out, int64_t in,
+                              const float* s, int bits, int group, int sym,
+                              const float* clip, uint32_t* qweight, float* scales,
+                              uint8_t* zeros, int32_t* dev_status, awq_stream_t stream);
+
+/*
  * awq_export_checkpoint - the tensors a quantized checkpoint stores for one
  * linear layer, from awq_quantize_pack's outputs.
  * ["AWQ vs GPTQ ...", "What lands on disk": qweight int32 words packing

@@ -63,6 +63,7 @@ __all__ = [
     "stored_codes", "pack_bits", "unpack_bits", "quantize_pack", "rtn_fake_quant",
     "output_power", "sweep", "Checkpoint", "export_checkpoint", "dequantize_checkpoint",
     "clip_factors", "quantize_groups_clipped", "ClipResult", "clip_search",
+    "quantize_pack_clipped",
 ]
 
 _EPS_SALIENCE = 1e-8          # added to the mean |X| [AWQ guide, "The code, line by line"]
@@ -458,3 +459,17 @@ def clip_search(W, X, s32, bits: int, group: int, sym: bool, n_grid: int = 20,
         best[better] = i
         best_err[better] = errs[:, :, i][better]
     return ClipResult(cs, errs, best)
+
+
+def quantize_pack_clipped(W, s32, bits: int, group: int, sym: bool, clip):
+    """quantize_pack with each group's range scaled by clip[row, group]
+    (float32) first, as the clipping search keeps it."""
+    W32 = np.asarray(W, dtype=np.float32)
+    t = W32 * np.asarray(s32, dtype=np.float32)[None, :]
+    gq = quantize_groups_clipped(t, bits, group, sym, clip)
+    u = stored_codes(gq.q, bits, sym)
+    if sym:
+        zeros = np.full(gq.scale.shape, 1 << (bits - 1), dtype=np.uint8)
+    else:
+        zeros = gq.zero.astype(np.uint8)
+    return pack_bits(u, bits), gq.scale.copy(), zeros

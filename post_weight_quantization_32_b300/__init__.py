@@ -30,7 +30,8 @@ __all__ = [
     "AWQError", "SearchOpts", "lib", "awq_channel_stats", "awq_search",
     "awq_search_workspace_bytes", "awq_quantize_pack", "new_status", "check_status", "STATUS",
     "DTYPE", "awq_search_noalloc", "NOALLOC_SCRATCH_BYTES", "awq_output_power", "awq_sweep",
-    "awq_export_checkpoint",
+    "awq_export_checkpoint", "awq_clip_search", "awq_clip_search_workspace_bytes",
+    "awq_quantize_pack_clipped",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +43,8 @@ STATUS = {0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARG", 2: "AWQ_ERR_UNSUPPORTED", 3: "A
 
 EXPORTS = ("awq_status_string", "awq_channel_stats", "awq_search_workspace_bytes", "awq_search",
            "awq_search_ex", "awq_quantize_pack", "awq_search_noalloc", "awq_output_power",
-           "awq_export_checkpoint")
+           "awq_export_checkpoint", "awq_clip_search", "awq_clip_search_workspace_bytes",
+           "awq_quantize_pack_clipped")
 
 # Size of the library's fixed scratch array used by awq_search_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -70,6 +72,14 @@ def _load() -> ctypes.CDLL:
     L.awq_output_power.argtypes = [vp, vp, i32, i64, i64, i64, vp, sz, vp, vp, vp]
     L.awq_export_checkpoint.restype = i32
     L.awq_export_checkpoint.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, vp]
+    L.awq_clip_search_workspace_bytes.restype = sz
+    L.awq_clip_search_workspace_bytes.argtypes = [i64, i64, i32]
+    L.awq_clip_search.restype = i32
+    L.awq_clip_search.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, i32, i32, vp, sz,
+                                  vp, vp, vp, vp]
+    L.awq_quantize_pack_clipped.restype = i32
+    L.awq_quantize_pack_clipped.argtypes = [vp, i32, i64, i64, vp, i32, i32, i32, vp, vp, vp, vp,
+                                            vp, vp]
     L.awq_search_noalloc.restype = i32
     L.awq_search_noalloc.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, i32, vp, vp, vp,
                                      vp, vp]
@@ -299,3 +309,55 @@ def awq_export_checkpoint(qweight: torch.Tensor, scales: torch.Tensor, zeros: to
     if check:
         check_status(st, "awq_export_checkpoint")
     return qw_t, sc_h, qz
+
+
+def awq_clip_search_workspace_bytes(n_in: int, N: int, group: int) -> int:
+    return int(lib.awq_clip_search_workspace_bytes(n_in, N, group))
+
+
+def awq_clip_search(W: torch.Tensor, X: torch.Tensor, s: torch.Tensor, bits: int = 4,
+                    group: int = 128, sym: bool = True, n_grid: int = 20,
+                    max_shrink_steps: int = 10, want_errs: bool = False, stream=None,
+                    dev_status: Optional[torch.Tensor] = None, check: bool = True):
+    """Per-group clipping search at scales s; returns (clip [out, in/g] f32,
+    errs [out, in/g, steps + 1] f32 or None)."""
+    _need(W, "W", 2)
+    _need(X, "X", 2)
+    if W.dtype != X.dtype or W.shape[1] != X.shape[1]:
+        raise ValueError("W and X must share dtype and the input dimension")
+    n_out, n_in = W.shape
+    N = X.shape[0]
+    need = awq_clip_search_workspace_bytes(n_in, N, group)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=W.device)
+    clip = torch.empty((n_out, n_in // group), dtype=torch.float32, device=W.device)
+    errs = (torch.empty((n_out, n_in // group, max_shrink_steps + 1), dtype=torch.float32,
+                        device=W.device) if want_errs else None)
+    st = dev_status if dev_status is not None else new_status(W.device)
+    _check(lib.awq_clip_search(_ptr(W), _ptr(X), DTYPE[W.dtype], n_out, n_in, N, _ptr(s), bits,
+                               group, 1 if sym else 0, n_grid, max_shrink_steps, _ptr(ws),
+                               ws.numel(), _ptr(clip), _ptr(errs), _ptr(st), _stream(stream)),
+           "awq_clip_search")
+    if check:
+        check_status(st, "awq_clip_search")
+    return clip, errs
+
+
+def awq_quantize_pack_clipped(W: torch.Tensor, s: torch.Tensor, clip: torch.Tensor, bits: int = 4,
+                              group: int = 128, sym: bool = True, stream=None,
+                              dev_status: Optional[torch.Tensor] = None, check: bool = True):
+    """``awq_quantize_pack`` with each group's range scaled by clip [out, in/g]."""
+    _need(W, "W", 2)
+    n_out, n_in = W.shape
+    nwords = (n_in * bits + 31) // 32
+    dev = W.device
+    qw = torch.empty((n_out, nwords), dtype=torch.int32, device=dev)
+    sc = torch.empty((n_out, n_in // group), dtype=torch.float32, device=dev)
+    z = torch.empty((n_out, n_in // group), dtype=torch.uint8, device=dev)
+    st = dev_status if dev_status is not None else new_status(dev)
+    _check(lib.awq_quantize_pack_clipped(_ptr(W), DTYPE[W.dtype], n_out, n_in, _ptr(s), bits,
+                                         group, 1 if sym else 0, _ptr(clip), _ptr(qw), _ptr(sc),
+                                         _ptr(z), _ptr(st), _stream(stream)),
+           "awq_quantize_pack_clipped")
+    if check:
+        check_status(st, "awq_quantize_pack_clipped")
+    return qw, sc, z

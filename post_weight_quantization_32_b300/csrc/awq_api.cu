@@ -237,8 +237,48 @@ int awq_quantize_pack(const void* W, int dtype, int64_t out, int64_t in, const f
   if (!W || !s || !qweight || !scales || !zeros || !dtype_ok(dtype)) return AWQ_ERR_INVALID_ARG;
   if (out < 1 || in < 1 || bits < 2 || bits > 8 || group < 1 || in % group != 0)
     return AWQ_ERR_INVALID_ARG;
-  return cuda_status(launch_quantize_pack(W, dtype, out, in, s, bits, group, sym ? 1 : 0, qweight,
-                                          scales, zeros, dev_status, (cudaStream_t)stream));
+  return cuda_status(launch_quantize_pack(W, dtype, out, in, s, bits, group, sym ? 1 : 0, nullptr,
+                                          qweight, scales, zeros, dev_status,
+                                          (cudaStream_t)stream));
+}
+
+int awq_quantize_pack_clipped(const void* W, int dtype, int64_t out, int64_t in, const float* s,
+                              int bits, int group, int sym, const float* clip, uint32_t* qweight,
+                              float* scales, uint8_t* zeros, int32_t* dev_status,
+                              awq_stream_t stream) {
+  if (!W || !s || !clip || !qweight || !scales || !zeros || !dtype_ok(dtype))
+    return AWQ_ERR_INVALID_ARG;
+  if (out < 1 || in < 1 || bits < 2 || bits > 8 || group < 1 || in % group != 0)
+    return AWQ_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_pack(W, dtype, out, in, s, bits, group, sym ? 1 : 0, clip,
+                                          qweight, scales, zeros, dev_status,
+                                          (cudaStream_t)stream));
+}
+
+size_t awq_clip_search_workspace_bytes(int64_t in, int64_t N, int group) {
+  if (in < 1 || N < 1 || (group != 32 && group != 64 && group != 128) || in % group != 0)
+    return 0;
+  return align_up((size_t)clip_splits(N) * in * group * sizeof(float), 256);
+}
+
+int awq_clip_search(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
+                    const float* s, int bits, int group, int sym, int n_grid, int max_shrink_steps,
+                    void* workspace, size_t workspace_bytes, float* clip, float* errs,
+                    int32_t* dev_status, awq_stream_t stream) {
+  if (!W || !X || !s || !workspace || !clip || !dtype_ok(dtype)) return AWQ_ERR_INVALID_ARG;
+  if (out < 1 || in < 1 || N < 1 || bits < 2 || bits > 8 || group < 1 || in % group != 0)
+    return AWQ_ERR_INVALID_ARG;
+  if (n_grid < 1 || max_shrink_steps < 0 || max_shrink_steps >= n_grid) return AWQ_ERR_INVALID_ARG;
+  if (group != 32 && group != 64 && group != 128) return AWQ_ERR_UNSUPPORTED;
+  if (max_shrink_steps + 1 > kMaxClip) return AWQ_ERR_UNSUPPORTED;
+  if (workspace_bytes < awq_clip_search_workspace_bytes(in, N, group) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return AWQ_ERR_INVALID_ARG;
+  ClipFactors cf{};
+  for (int i = 0; i <= max_shrink_steps; ++i) cf.c[i] = (float)(1.0 - (double)i / n_grid);
+  return cuda_status(launch_clip_search(W, X, dtype, out, in, N, s, bits, group, sym ? 1 : 0,
+                                        max_shrink_steps + 1, cf, static_cast<float*>(workspace),
+                                        clip, errs, dev_status, (cudaStream_t)stream));
 }
 
 int awq_export_checkpoint(const uint32_t* qweight, const float* scales, const uint8_t* zeros,

@@ -145,9 +145,29 @@ cudaError_t launch_group_extremes(const void* W, int dt, int64_t out, int64_t in
                                   float* ext, cudaStream_t s);
 
 // ---- final quantization and packing (awq_pack.cu)
+// clip: null, or [out][in/group] factors scaling each group's range (the
+// codes then take the quantizer's clamps).
 cudaError_t launch_quantize_pack(const void* W, int dt, int64_t out, int64_t in, const float* s,
-                                 int bits, int group, int sym, uint32_t* qweight, float* scales,
-                                 uint8_t* zeros, int32_t* dev_status, cudaStream_t st);
+                                 int bits, int group, int sym, const float* clip,
+                                 uint32_t* qweight, float* scales, uint8_t* zeros,
+                                 int32_t* dev_status, cudaStream_t st);
+
+// ---- per-group clipping search (awq_clip.cu)
+constexpr int kMaxClip = 12;  // shrink factors per search (a multiple of 4)
+struct ClipFactors {
+  float c[kMaxClip];
+};
+// Token splits of the Gram-matrix pass: the workspace holds
+// clip_splits(N) * in * group floats.
+int clip_splits(int64_t N);
+// For every row and group (group in {32, 64, 128}) of W * diag(s): the
+// group's share of the row's output error for each of the nc factors of cf,
+// and clip[row][group] = the first factor with the smallest share; errs
+// ([out][in/group][nc], may be null) receives the shares.
+cudaError_t launch_clip_search(const void* W, const void* X, int dt, int64_t out, int64_t in,
+                               int64_t N, const float* s, int bits, int group, int sym, int nc,
+                               const ClipFactors& cf, float* H, float* clip, float* errs,
+                               int32_t* dev_status, cudaStream_t stream);
 
 // ---- checkpoint export (awq_export.cu)
 // From quantize_pack's row-major outputs (bits divides 32, in % (32/bits) ==

@@ -12,6 +12,10 @@
 // round() is half-to-even.  Code i of a row goes to bit i*b of the row's
 // little-endian uint32 stream.
 //
+// With per-group clip factors c (the clipping search's result) the range is
+// scaled first: m = fl32(c * m), or lo = fl32(c * lo), hi = fl32(c * hi),
+// and values beyond it take the clamped end codes.
+//
 // The quotient t / scale is formed as t * (1/scale) and replaced by the
 // correctly rounded quotient whenever it lies within 2^-21 (relative) of a
 // half-integer, the only place where the two could round differently: the
@@ -32,6 +36,7 @@ struct QParams {
   float maxqf;  // asymmetric: 2^b - 1
   int bits;
   int sym;
+  const float* clip;  // null, or [out][in/group] factors scaling each group's range
 };
 
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
@@ -118,6 +123,7 @@ __global__ void __launch_bounds__(256) pack_warp_kernel(const T* __restrict__ W,
       for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(t[e]));
 #pragma unroll
       for (int o = 1; o < LPG; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (qp.clip != nullptr && valid) m = __fmul_rn(qp.clip[row * ngroups + c0 / (8 * LPG)], m);
       group_params_sym(m, qp, scale, zero);
     } else {
       float lo = 0.0f, hi = 0.0f;
@@ -130,6 +136,11 @@ __global__ void __launch_bounds__(256) pack_warp_kernel(const T* __restrict__ W,
       for (int o = 1; o < LPG; o <<= 1) {
         lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
         hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      }
+      if (qp.clip != nullptr && valid) {
+        const float f = qp.clip[row * ngroups + c0 / (8 * LPG)];
+        lo = __fmul_rn(f, lo);
+        hi = __fmul_rn(f, hi);
       }
       group_params_asym(lo, hi, qp, scale, zero);
     }
@@ -479,6 +490,12 @@ __global__ void __launch_bounds__(256) pack_general_kernel(const T* __restrict__
     if (__any_sync(0xffffffffu, nan) && lane == 0) set_status(dev_status, ST_NONFINITE);
     float scale;
     int zero;
+    if (qp.clip != nullptr) {
+      const float f = qp.clip[row * ngroups + g];
+      m = __fmul_rn(f, m);
+      lo = __fmul_rn(f, lo);
+      hi = __fmul_rn(f, hi);
+    }
     if (qp.sym)
       group_params_sym(m, qp, scale, zero);
     else
@@ -547,7 +564,7 @@ cudaError_t pack_dispatch(const void* W, int64_t out, int64_t in, const float* s
              ((reinterpret_cast<uintptr_t>(s) & 15) == 0);
   const bool fast_shape = (qp.bits == 2 || qp.bits == 4 || qp.bits == 8) && group >= 32 &&
                           group <= 1024 && (group & (group - 1)) == 0;
-  if (vec && fast_shape &&
+  if (vec && fast_shape && qp.clip == nullptr &&
       (reinterpret_cast<uintptr_t>(qw) & (uintptr_t)(qp.bits == 2 ? 7 : 15)) == 0) {
     const int lpg = group / 32;
     switch (qp.bits) {
@@ -579,9 +596,11 @@ cudaError_t pack_dispatch(const void* W, int64_t out, int64_t in, const float* s
 }  // namespace
 
 cudaError_t launch_quantize_pack(const void* W, int dt, int64_t out, int64_t in, const float* s,
-                                 int bits, int group, int sym, uint32_t* qweight, float* scales,
-                                 uint8_t* zeros, int32_t* dev_status, cudaStream_t st) {
+                                 int bits, int group, int sym, const float* clip,
+                                 uint32_t* qweight, float* scales, uint8_t* zeros,
+                                 int32_t* dev_status, cudaStream_t st) {
   QParams qp;
+  qp.clip = clip;
   qp.bits = bits;
   qp.sym = sym ? 1 : 0;
   qp.Lf = (float)((1 << (bits - 1)) - 1);

@@ -272,6 +272,45 @@ def test_export_checkpoint_reports_fp16_overflow(awq):
     assert int(st.item()) == 3
 
 
+CLIP_CASES = [
+    # (out, in, N, dtype, bits, group, sym, n_grid, max_shrink_steps)
+    (64, 256, 40, "bf16", 3, 128, True, 20, 10),
+    (37, 192, 17, "f16", 4, 64, False, 20, 10),
+    (50, 96, 300, "f32", 2, 32, True, 10, 5),
+    (130, 512, 64, "bf16", 4, 128, False, 20, 11),
+    (9, 128, 1, "bf16", 3, 128, False, 20, 0),      # one factor: nothing to choose
+]
+
+
+@pytest.mark.parametrize("case", CLIP_CASES, ids=lambda c: "%dx%d_n%d_%s_b%d_g%d_%s_%d_%d" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], "sym" if c[6] else "asym", c[7], c[8]))
+def test_clip_search_matches_oracle(awq, case):
+    out, n_in, N, dtype, bits, group, sym, n_grid, steps = case
+    W, X = make_random_layer(out, n_in, N, dtype=dtype, seed=out + n_in + 3,
+                             n_outlier=max(1, n_in // 64))
+    s32 = np.random.default_rng(n_in).uniform(0.5, 2.0, size=n_in).astype(np.float32)
+    Wd, Xd = _dev(W, X)
+    clip, errs = awq.awq_clip_search(Wd, Xd, torch.from_numpy(s32).cuda(), bits, group, sym,
+                                     n_grid, steps, want_errs=True)
+    ref = O.clip_search(_np_w(W), _np_x(X), s32, bits, group, sym, n_grid, steps / n_grid)
+    e = errs.cpu().numpy().astype(np.float64)
+    floor = 1e-6 * ref.errs.max(axis=-1, keepdims=True)
+    assert np.all(np.abs(e - ref.errs) <= ERR_RTOL * ref.errs + floor)
+    got = clip.cpu().numpy()
+    idx = np.argmax(got[..., None] == ref.factors[None, None, :], axis=-1)
+    assert np.all(got == ref.factors[idx])
+    chosen = np.take_along_axis(ref.errs, idx[..., None], -1)[..., 0]
+    best = np.take_along_axis(ref.errs, ref.best[..., None], -1)[..., 0]
+    assert np.all(chosen <= best * (1 + TIE_RTOL) + floor[..., 0])
+    # the kept factors give the oracle's codes exactly
+    qw, sc, z = awq.awq_quantize_pack_clipped(Wd, torch.from_numpy(s32).cuda(), clip, bits, group,
+                                              sym)
+    qo, so, zo = O.quantize_pack_clipped(_np_w(W), s32, bits, group, sym, got)
+    assert np.array_equal(qw.cpu().numpy().view(np.uint32), qo)
+    assert np.array_equal(sc.cpu().numpy(), so)
+    assert np.array_equal(z.cpu().numpy(), zo)
+
+
 def test_search_shared_input_group(awq):
     """q/k/v share X and one s: the concatenated rows are searched at once."""
     ws, X = [], None
