@@ -244,6 +244,9 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=[c.name for c in CONFIGS])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=2, help="alphas in the oracle's timed sample")
+    ap.add_argument("--next-rows", action="store_true",
+                    help="also time the clipping search, output power, wide-group searches and the "
+                         "checkpoint export on the same layer (one extra JSON line each, rank 0)")
     args = ap.parse_args()
     cfg = config_by_name(args.config)
     dist, rank, world = _dist()
@@ -307,6 +310,86 @@ def main():
         "clocks": r["clocks"],
     }
     print(json.dumps(line))
+    if args.next_rows:
+        for extra in run_next_rows(args, cfg, tflops_peak, hbm_peak, peak_kind):
+            print(json.dumps(extra))
+
+
+# FP32 FMA lanes per SM and the maximum SM clock of a B300: the peak of the
+# clipping search's quadratic forms, which run on the FMA pipe.
+FP32_LANES_PER_SM, SM_MAX_GHZ = 128, 2.032
+
+
+def run_next_rows(args, cfg, tflops_peak, hbm_peak, peak_kind):
+    """Event-timed runs of the rows beyond the headline path, on the same
+    layer and with the same L2 flush between runs."""
+    import post_weight_quantization_32_b300 as awq
+
+    dev = torch.device("cuda", 0)
+    W, X = make_layer(cfg, seed=0)
+    Wd, Xd = W.to(dev), X.to(dev)
+    out, n_in, N, g = cfg.out, cfg.in_, cfg.N, cfg.group
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        return sorted(ts)[len(ts) // 2]
+
+    _, _, s_best = awq.awq_search(Wd, Xd, cfg.bits, g, cfg.sym, cfg.grid)
+    steps_c = 10
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * SM_MAX_GHZ / 1e3          # TFLOP/s
+    rows = []
+
+    t = timed(lambda: awq.awq_clip_search(Wd, Xd, s_best, cfg.bits, g, cfg.sym, 20, steps_c,
+                                          check=False))
+    fl = 2.0 * out * n_in * g * (steps_c + 1) + 2.0 * n_in * g * N     # quadratic forms + Gram
+    rows.append({"row": "clip_search", "metric": "group-factor-evals/s",
+                 "value": out * (n_in // g) * (steps_c + 1) / t, "ms": t * 1e3,
+                 "roofline": {"bound": "alu", "achieved": fl / t / 1e12, "peak": fp32_peak,
+                              "unit": "TFLOP/s", "frac": fl / t / 1e12 / fp32_peak,
+                              "peak_kind": "fp32 FMA lanes x max clock"}})
+
+    t = timed(lambda: awq.awq_output_power(Wd, Xd, check=False))
+    fl = 2.0 * N * n_in * out
+    rows.append({"row": "output_power", "metric": "layers/s", "value": 1.0 / t, "ms": t * 1e3,
+                 "roofline": {"bound": "tensor", "achieved": fl / t / 1e12, "peak": tflops_peak,
+                              "unit": "TFLOP/s", "frac": fl / t / 1e12 / tflops_peak,
+                              "peak_kind": peak_kind}})
+
+    for wide in (256, None):
+        t = timed(lambda: awq.awq_search(Wd, Xd, cfg.bits, wide, cfg.sym, cfg.grid, check=False))
+        fl = cfg.search_flops
+        rows.append({"row": "search_group_%s" % ("row" if wide is None else wide),
+                     "metric": "layer-alpha-evals/s", "value": cfg.n_alpha / t, "ms": t * 1e3,
+                     "roofline": {"bound": "tensor", "achieved": fl / t / 1e12, "peak": tflops_peak,
+                                  "unit": "TFLOP/s", "frac": fl / t / 1e12 / tflops_peak,
+                                  "peak_kind": peak_kind + " (whole call incl. the range pass)"}})
+
+    qw, sc, z = awq.awq_quantize_pack(Wd, s_best, cfg.bits, g, cfg.sym)
+    if 32 % cfg.bits == 0:
+        t = timed(lambda: awq.awq_export_checkpoint(qw, sc, z, n_in, cfg.bits, g, check=False))
+        # read: codes, fp32 steps, uint8 zeros; written: codes, fp16 steps, packed zeros
+        nb = (qw.numel() * 4 + sc.numel() * 4 + z.numel()) + (qw.numel() * 4 + sc.numel() * 2
+                                                              + z.numel() * cfg.bits // 8)
+        rows.append({"row": "export_checkpoint", "metric": "GB/s", "value": nb / t / 1e9,
+                     "ms": t * 1e3,
+                     "roofline": {"bound": "hbm", "achieved": nb / t / 1e9, "peak": hbm_peak,
+                                  "unit": "GB/s", "frac": nb / t / 1e9 / hbm_peak}})
+    for r in rows:
+        r.update({"workload": cfg.name, "steps": args.steps, "warmup": args.warmup,
+                  "l2": "flushed between runs (512 MiB write)"})
+    return rows
 
 
 if __name__ == "__main__":

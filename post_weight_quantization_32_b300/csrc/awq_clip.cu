@@ -18,9 +18,10 @@
 // clip_kernel: CTA (group, row block) stages H_G in shared memory (each lane's
 // columns contiguous), one warp per row: the warp forms d_c for every factor
 // (each lane holds g/32 columns, codes by true division with the quantizer's
-// clamps), writes them to shared memory, and accumulates H_G d_c over k with
-// one 16-byte load of H and of the factors' d per step (fp32 FMA-bound), then
-// reduces d_c . (H_G d_c) across the warp.
+// clamps, d = w_hat * (1/s) - w), writes them to shared memory, and
+// accumulates H_G d_c over k with one 16-byte load of H and one per four
+// factors' d per step (fp32 FMA-bound), then reduces d_c . (H_G d_c) across
+// the warp.
 #include <algorithm>
 
 #include "awq_device.cuh"
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__((G / 8) * (G / 8)) gram_kernel(const T* __rest
     for (int b = 0; b < 8; ++b) Hg[(ti * 8 + a) * G + tj * 8 + b] = acc[a][b];
 }
 
-template <typename T, int G, bool SYM>
+template <typename T, int G, bool SYM, int NCQ>
 __global__ void __launch_bounds__(kClipWarps * 32) clip_kernel(
     const T* __restrict__ W, const float* __restrict__ s, const float* __restrict__ H, int nsplit,
     int64_t out, int64_t in, float Lf, float maxqf, int nc, ClipFactors cf,
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(kClipWarps * 32) clip_kernel(
   pdl_wait();
   pdl_trigger();
   constexpr int CPL = G / 32;  // columns per lane: j = lane + 32 i
+  constexpr int NCP = 4 * NCQ;  // factors carried through the quadratic forms (>= nc)
   extern __shared__ float4 csm[];
   // Hs[k][lane] holds H[k][lane + 32 i], i < CPL (a float4 slot each)
   float4* Hs = csm;
@@ -106,14 +108,19 @@ __global__ void __launch_bounds__(kClipWarps * 32) clip_kernel(
   for (int i = threadIdx.x; i < kClipWarps * G * kMaxClip; i += blockDim.x) dsm[i] = 0.0f;
   __syncthreads();
   float* dw = dsm + (size_t)warp * G * kMaxClip;
+  float sv[CPL], inv_s[CPL];  // the group's scales are the same for every row
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    sv[i] = s[(int64_t)g * G + lane + 32 * i];
+    inv_s[i] = 1.0f / sv[i];
+  }
   for (int64_t row = (int64_t)blockIdx.y * kClipWarps + warp; row < out;
        row += (int64_t)gridDim.y * kClipWarps) {
-    float w[CPL], sv[CPL], t[CPL];
+    float w[CPL], t[CPL];
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
       const int64_t j = (int64_t)g * G + lane + 32 * i;
       w[i] = Elt<T>::to_f32(W[row * in + j]);
-      sv[i] = s[j];
       t[i] = __fmul_rn(w[i], sv[i]);
     }
     float r0 = 0.0f, r1 = 0.0f;  // sym: max|t|; asym: min(min t, 0), max(max t, 0)
@@ -160,23 +167,23 @@ __global__ void __launch_bounds__(kClipWarps * 32) clip_kernel(
           q = fminf(fmaxf(__fadd_rn(q, zero), 0.0f), maxqf);
           what = __fmul_rn(scale, __fsub_rn(q, zero));
         }
-        dw[(lane + 32 * i) * kMaxClip + c] = __fsub_rn(__fdiv_rn(what, sv[i]), w[i]);
+        dw[(lane + 32 * i) * kMaxClip + c] = fmaf(what, inv_s[i], -w[i]);
       }
     }
     __syncwarp();
     // v_c = H_G d_c for this lane's columns
-    float v[kMaxClip][CPL];
+    float v[NCP][CPL];
 #pragma unroll
-    for (int c = 0; c < kMaxClip; ++c)
+    for (int c = 0; c < NCP; ++c)
 #pragma unroll
       for (int i = 0; i < CPL; ++i) v[c][i] = 0.0f;
     for (int k = 0; k < G; ++k) {
       const float4 h = Hs[k * 32 + lane];
       const float hv[4] = {h.x, h.y, h.z, h.w};
       const float4* dk = reinterpret_cast<const float4*>(dw + k * kMaxClip);
-      float dv[kMaxClip];
+      float dv[NCP];
 #pragma unroll
-      for (int q = 0; q < kMaxClip / 4; ++q) {
+      for (int q = 0; q < NCQ; ++q) {
         const float4 x = dk[q];
         dv[4 * q] = x.x;
         dv[4 * q + 1] = x.y;
@@ -184,7 +191,7 @@ __global__ void __launch_bounds__(kClipWarps * 32) clip_kernel(
         dv[4 * q + 3] = x.w;
       }
 #pragma unroll
-      for (int c = 0; c < kMaxClip; ++c)
+      for (int c = 0; c < NCP; ++c)
 #pragma unroll
         for (int i = 0; i < CPL; ++i) v[c][i] = fmaf(hv[i], dv[c], v[c][i]);
     }
@@ -192,7 +199,7 @@ __global__ void __launch_bounds__(kClipWarps * 32) clip_kernel(
     float best_e = INFINITY;
     int best = 0;
 #pragma unroll
-    for (int c = 0; c < kMaxClip; ++c) {
+    for (int c = 0; c < NCP; ++c) {
       if (c >= nc) break;
       float e = 0.0f;
 #pragma unroll
@@ -220,7 +227,14 @@ cudaError_t launch_clip_g(const void* W, const void* X, int64_t out, int64_t in,
                              nsplit, H);
   if (e != cudaSuccess) return e;
   const size_t smem = (size_t)G * 32 * sizeof(float4) + (size_t)kClipWarps * G * kMaxClip * 4;
-  auto kern = sym ? clip_kernel<T, G, true> : clip_kernel<T, G, false>;
+  using Kern = void (*)(const T*, const float*, const float*, int, int64_t, int64_t, float, float,
+                        int, ClipFactors, float*, float*, int32_t*);
+  const Kern table[2][3] = {{clip_kernel<T, G, false, 1>, clip_kernel<T, G, false, 2>,
+                             clip_kernel<T, G, false, 3>},
+                            {clip_kernel<T, G, true, 1>, clip_kernel<T, G, true, 2>,
+                             clip_kernel<T, G, true, 3>}};
+  static_assert(kMaxClip == 12, "three groups of four factors");
+  const Kern kern = table[sym ? 1 : 0][(nc + 3) / 4 - 1];
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t rb = (out + kClipWarps - 1) / kClipWarps;

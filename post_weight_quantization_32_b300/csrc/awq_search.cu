@@ -456,6 +456,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int g = 0; g < NG; ++g)
 #pragma unroll
             for (int j = 0; j < 4; ++j) r0[g][j] = r1[g][j] = 0.0f;
+          if constexpr (GP) {  // the group's extremes over all its jobs (loaded before pass 1
+                               // so that the load overlaps it)
+            const int64_t grow =
+                min((int64_t)(u / units_per_rt) * kRows + row, (int64_t)p.out - 1);
+            const int64_t gi = ((int64_t)(ag * p.a_per + a) * p.out + grow) * wa.ngroups +
+                               (int64_t)kg * JC / wa.group;
+            if (SYM) {
+              r0[0][0] = __ldg(wa.gext + gi);
+            } else {
+              r0[0][0] = -__ldg(wa.gext + 2 * gi);
+              r1[0][0] = __ldg(wa.gext + 2 * gi + 1);
+            }
+          }
 #pragma unroll
           for (int cgi = 0; cgi < JC / 8; ++cgi) {
             const int kbi = cgi >> 3, cc = cgi & 7, g = cgi / CPG;
@@ -479,18 +492,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           // group steps
-          if constexpr (GP) {  // the group's extremes over all its jobs, formed ahead of the search
-            const int64_t grow =
-                min((int64_t)(u / units_per_rt) * kRows + row, (int64_t)p.out - 1);
-            const int64_t gi = ((int64_t)(ag * p.a_per + a) * p.out + grow) * wa.ngroups +
-                               (int64_t)kg * JC / wa.group;
-            if (SYM) {
-              r0[0][0] = __ldg(wa.gext + gi);
-            } else {
-              r0[0][0] = -__ldg(wa.gext + 2 * gi);
-              r1[0][0] = __ldg(wa.gext + 2 * gi + 1);
-            }
-          }
           float scl[NG], rcp[NG], chi[NG];
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
