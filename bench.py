@@ -124,6 +124,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def world_max(v, dist, device):
+    """The largest v over the ranks (v itself without a process group): the
+    job takes as long as its slowest rank."""
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(n_alpha, world, ms):
+    """Whole-job layer-alpha-evals/s: each rank searches its own layer over
+    n_alpha alphas (weak scaling), all within the slowest rank's ms."""
+    return n_alpha * world / (ms * 1e-3)
+
+
 def run_ours(args, cfg, rank, world, dist):
     import post_weight_quantization_32_b300 as awq
 
@@ -205,16 +221,9 @@ def run_ours(args, cfg, rank, world, dist):
     h2d = W.numel() * W.element_size() + X.numel() * X.element_size()
     d2h = sum(t.numel() * t.element_size() for t in res_h)
 
-    def world_max(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    ms = world_max(sum(step_ms) / len(step_ms))
-    e2e = world_max(sum(e2e_ms) / len(e2e_ms))
-    t_search = world_max(sum(search_ms) / len(search_ms))
+    ms = world_max(sum(step_ms) / len(step_ms), dist, dev)
+    e2e = world_max(sum(e2e_ms) / len(e2e_ms), dist, dev)
+    t_search = world_max(sum(search_ms) / len(search_ms), dist, dev)
     return dict(ms=ms, e2e_ms=e2e, search_ms=t_search, h2d=h2d, d2h=d2h, clocks=clk.summary())
 
 
@@ -284,8 +293,8 @@ def main():
     if rank != 0:
         return
     n_alpha = cfg.n_alpha
-    value = n_alpha * world / (r["ms"] * 1e-3)
-    e2e_v = n_alpha * world / (r["e2e_ms"] * 1e-3)
+    value = job_throughput(n_alpha, world, r["ms"])
+    e2e_v = job_throughput(n_alpha, world, r["e2e_ms"])
     achieved = flops / (r["search_ms"] * 1e-3) / 1e12
     cpu_t, cpu_n = run_oracle_sample(cfg, args.cpu_sample)
     # statistics (with max|W| and the centring), alpha table, search, argmin, pack;
