@@ -280,7 +280,7 @@ __device__ __forceinline__ void cp_async_wait() {
 constexpr int kPackSeg = 1024;
 constexpr int kPackStages = 3;
 constexpr int kPackThreads = 256;
-constexpr int kPackCtasPerSm = 2;
+constexpr int kPackCtasPerSm = 3;
 
 template <typename T>
 constexpr int pack_chunks() {  // 16-byte chunks of one lane's 32 weights
@@ -304,6 +304,7 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_fast_kernel
   // sum over one word's fields of 2^(i * B)
   constexpr uint32_t kRep = B == 2 ? 0x55555555u : (B == 4 ? 0x11111111u : 0x01010101u);
   extern __shared__ uint4 ring[];  // [stage][chunk][thread]
+  __shared__ float4 s_seg[8][32];
   const float thr = 0.5f - ldexpf(1.0f, B - 21);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t segs = (in + kPackSeg - 1) / kPackSeg;
@@ -312,20 +313,16 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_fast_kernel
   for (int64_t seg = blockIdx.y; seg < segs; seg += gridDim.y) {
     const int64_t c0 = seg * kPackSeg + lane * 32;
     const bool live = c0 < in;  // in is a multiple of the group, so all 32 columns are live
-    float sv[32];
-    if (live) {
+    // the segment's scales, shared by every warp of the CTA: [i][lane] holds
+    // s[c0 + 4i .. c0 + 4i + 3] of that lane, so a warp's reads of one i are
+    // 32 consecutive 16-byte words
+    if (warp == 0) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 q = __ldg(reinterpret_cast<const float4*>(s + c0) + i);
-        sv[4 * i] = q.x;
-        sv[4 * i + 1] = q.y;
-        sv[4 * i + 2] = q.z;
-        sv[4 * i + 3] = q.w;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) sv[e] = 0.0f;
+      for (int i = 0; i < 8; ++i)
+        s_seg[i][lane] = live ? __ldg(reinterpret_cast<const float4*>(s + c0) + i)
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
+    __syncthreads();
     const int64_t r0 = (int64_t)blockIdx.x * 8 + warp;
     // copies of row r0 + i * rstep into ring stage i % kPackStages (one group per row)
     auto issue = [&](int64_t i) {
@@ -349,7 +346,16 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_fast_kernel
       float t[32];
       if (live) {
 #pragma unroll
-        for (int h = 0; h < 32 * (int)sizeof(T) / 32; ++h) {
+        for (int h = 0; h < 2; ++h) {
+          float sv[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 x = s_seg[4 * h + q][lane];
+            sv[4 * q] = x.x;
+            sv[4 * q + 1] = x.y;
+            sv[4 * q + 2] = x.z;
+            sv[4 * q + 3] = x.w;
+          }
           Raw16<T> raw;
 #pragma unroll
           for (int c = 0; c < (int)sizeof(Raw16<T>) / 16; ++c)
@@ -359,8 +365,8 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_fast_kernel
           raw.widen(v);
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
-            const float2 p = __fmul2_rn(make_float2(v[e], v[e + 1]),
-                                        make_float2(sv[16 * h + e], sv[16 * h + e + 1]));
+            const float2 p =
+                __fmul2_rn(make_float2(v[e], v[e + 1]), make_float2(sv[e], sv[e + 1]));
             t[16 * h + e] = p.x;
             t[16 * h + e + 1] = p.y;
           }
@@ -450,6 +456,7 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_fast_kernel
       }
     }
     cp_async_wait<0>();  // no copy may still target the ring when it is reused
+    __syncthreads();     // nor any warp still read the segment's scales
   }
 }
 
