@@ -127,3 +127,71 @@ def test_stats_rejects_bad_arguments_on_host(lib):
     assert lib.awq_channel_stats(None, 2, 4, 8, f, None, None) == 1
     assert lib.awq_channel_stats(f, 2, 0, 8, f, None, None) == 1
     assert lib.awq_channel_stats(f, 9, 4, 8, f, None, None) == 1
+
+
+def test_output_power_rejects_bad_arguments_on_host(lib):
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    lib.awq_output_power.restype = i32
+    lib.awq_output_power.argtypes = [vp, vp, i32, i64, i64, i64, vp, sz, vp, vp, vp]
+    f = 1 << 20   # never dereferenced
+    need = _ws(lib, 2, 64, 256, 16, 256, 1)
+    assert need > 0
+    ok = dict(W=f, X=f, dt=2, out=64, n_in=256, N=16, ws=f, wsb=need, p=f)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return lib.awq_output_power(a["W"], a["X"], a["dt"], a["out"], a["n_in"], a["N"], a["ws"],
+                                    a["wsb"], a["p"], None, None)
+
+    assert call(W=None) == 1 and call(p=None) == 1
+    assert call(N=0) == 1 and call(out=0) == 1 and call(dt=7) == 1
+    assert call(wsb=need - 1) == 1 and call(ws=f + 16) == 1
+    assert call(n_in=252, wsb=1 << 30) == 2     # in % 8 != 0: no tensor-map rows
+    assert call(X=f + 8) == 2                    # TMA needs 16-byte aligned rows
+
+
+def test_clip_search_rejects_bad_arguments_on_host(lib):
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    lib.awq_clip_search_workspace_bytes.restype = sz
+    lib.awq_clip_search_workspace_bytes.argtypes = [i64, i64, i32]
+    lib.awq_clip_search.restype = i32
+    lib.awq_clip_search.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, i32, i32, vp, sz,
+                                    vp, vp, vp, vp]
+    # Gram matrices: one g x g float block per group and token split of 256
+    assert lib.awq_clip_search_workspace_bytes(4096, 256, 128) == 4096 * 128 * 4
+    assert lib.awq_clip_search_workspace_bytes(4096, 2048, 128) == 8 * 4096 * 128 * 4
+    assert lib.awq_clip_search_workspace_bytes(4096, 256, 256) == 0     # group not handled
+    assert lib.awq_clip_search_workspace_bytes(100, 256, 32) == 0       # group does not divide in
+    f = 1 << 20
+    ok = dict(W=f, X=f, dt=1, out=8, n_in=256, N=4, s=f, bits=4, group=128, sym=1, n_grid=20,
+              steps=10, ws=f, wsb=1 << 30, clip=f)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return lib.awq_clip_search(a["W"], a["X"], a["dt"], a["out"], a["n_in"], a["N"], a["s"],
+                                   a["bits"], a["group"], a["sym"], a["n_grid"], a["steps"],
+                                   a["ws"], a["wsb"], a["clip"], None, None, None)
+
+    assert call(clip=None) == 1 and call(s=None) == 1 and call(bits=9) == 1
+    assert call(n_grid=0) == 1 and call(steps=-1) == 1 and call(steps=20) == 1
+    assert call(wsb=16) == 1 and call(ws=f + 64) == 1
+    assert call(group=64, n_in=256, steps=12) == 2     # more than twelve factors
+    assert call(group=256, n_in=512) == 2              # groups wider than 128 columns
+
+
+def test_export_and_clipped_pack_reject_bad_arguments_on_host(lib):
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.awq_export_checkpoint.restype = i32
+    lib.awq_export_checkpoint.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, vp]
+    f = 1 << 20
+    assert lib.awq_export_checkpoint(None, f, f, 4, 64, 4, 32, f, f, f, None, None) == 1
+    assert lib.awq_export_checkpoint(f, f, f, 4, 64, 3, 32, f, f, f, None, None) == 1  # 3 bits
+    assert lib.awq_export_checkpoint(f, f, f, 4, 60, 4, 30, f, f, f, None, None) == 1  # in % 8
+    assert lib.awq_export_checkpoint(f, f, f, 4, 64, 4, 48, f, f, f, None, None) == 1  # group
+    lib.awq_quantize_pack_clipped.restype = i32
+    lib.awq_quantize_pack_clipped.argtypes = [vp, i32, i64, i64, vp, i32, i32, i32, vp, vp, vp, vp,
+                                              vp, vp]
+    assert lib.awq_quantize_pack_clipped(f, 2, 4, 8, f, 4, 8, 1, None, f, f, f, None, None) == 1
+    assert lib.awq_quantize_pack_clipped(f, 2, 4, 8, f, 4, 3, 1, f, f, f, f, None, None) == 1
