@@ -63,7 +63,7 @@ __all__ = [
     "stored_codes", "pack_bits", "unpack_bits", "quantize_pack", "rtn_fake_quant",
     "output_power", "sweep", "Checkpoint", "export_checkpoint", "dequantize_checkpoint",
     "clip_factors", "quantize_groups_clipped", "ClipResult", "clip_search",
-    "quantize_pack_clipped",
+    "quantize_pack_clipped", "GptqResult", "inverse_hessian_factor", "gptq",
 ]
 
 _EPS_SALIENCE = 1e-8          # added to the mean |X| [AWQ guide, "The code, line by line"]
@@ -473,3 +473,77 @@ def quantize_pack_clipped(W, s32, bits: int, group: int, sym: bool, clip):
     else:
         zeros = gq.zero.astype(np.uint8)
     return pack_bits(u, bits), gq.scale.copy(), zeros
+
+
+# --------------------------------------------------------------------------
+# GPTQ rounding after AWQ scaling
+# --------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class GptqResult:
+    q: np.ndarray        # codes [out, in] (signed for the symmetric quantizer, as quantize_groups)
+    scale: np.ndarray    # float32 [out, in/g], fitted on the corrected weights at each group start
+    zero: np.ndarray     # float32 [out, in/g]
+    w_hat: np.ndarray    # float64 [out, in]: dequantized weights of W * s
+    Wq: np.ndarray       # float64 [out, in]: w_hat / s
+
+
+def inverse_hessian_factor(Xs, damp: float = 0.01) -> np.ndarray:
+    """The upper-triangular U with U^T U = H^-1, H = 2 Xs^T Xs plus `damp`
+    times the mean of its diagonal on the diagonal.  ["AWQ vs GPTQ ...",
+    "GPTQ: compensate the error you just made": H = 2 X X^T for one row of
+    weights, dampening by 1% of the mean diagonal, rows of H^-1 read from one
+    Cholesky factorisation.]  Xs: (N, in) inputs of the layer, float64."""
+    H = 2.0 * (Xs.T @ Xs)
+    H[np.diag_indices_from(H)] += damp * np.mean(np.diag(H))
+    Hinv = np.linalg.inv(H)
+    return np.linalg.cholesky(Hinv).T
+
+
+def gptq(W, X, bits: int, group: int, sym: bool, s32=None, damp: float = 0.01) -> GptqResult:
+    """GPTQ's rounding of W * diag(s) against the inputs X / s (AWQ's scaling
+    first, then GPTQ's choice of integers: "AWQ vs GPTQ ...", "Failure modes
+    and combining the two"; without s, plain GPTQ).
+
+    Columns are rounded in their natural order (no act-order).  At the first
+    column of each group the group's step and zero point are fitted on the
+    weights as they stand then, corrections from earlier columns included;
+    each column is rounded with the float32 quantizer of this module
+    (quantize_groups' arithmetic on fl32 of the corrected weight); the
+    rounding error, divided by U[i, i], is spread over the later columns of
+    every row through row i of U.  The running weights are float64.
+    ["AWQ vs GPTQ ...", "GPTQ: compensate the error you just made" and the
+    production details after it]
+    """
+    W32 = np.asarray(W, dtype=np.float32)
+    out, n_in = W32.shape
+    s32 = np.ones(n_in, np.float32) if s32 is None else np.asarray(s32, dtype=np.float32)
+    Ws = (W32 * s32[None, :]).astype(np.float64)          # W * s, as the quantizer sees it
+    Xs = np.asarray(X, dtype=np.float64) / s32.astype(np.float64)[None, :]
+    U = inverse_hessian_factor(Xs, damp)
+    ng = n_in // group
+    q = np.zeros((out, n_in))
+    w_hat = np.zeros((out, n_in))
+    scale = np.zeros((out, ng), np.float32)
+    zero = np.zeros((out, ng), np.float32)
+    for i in range(n_in):
+        g = i // group
+        if i % group == 0:
+            gq = quantize_groups(Ws[:, i:i + group].astype(np.float32), bits, group, sym)
+            scale[:, g], zero[:, g] = gq.scale[:, 0], gq.zero[:, 0]
+        col = Ws[:, i].astype(np.float32)
+        sc = scale[:, g]
+        if sym:
+            L = np.float32((1 << (bits - 1)) - 1)
+            qi = np.clip(np.round((col / sc).astype(np.float32)), -L - 1, L)
+            wh = (qi * sc).astype(np.float32)
+        else:
+            maxq = np.float32((1 << bits) - 1)
+            z = zero[:, g]
+            qi = np.clip(np.round((col / sc).astype(np.float32)) + z, 0, maxq)
+            wh = (sc * (qi - z)).astype(np.float32)
+        q[:, i] = qi
+        w_hat[:, i] = wh
+        err = (Ws[:, i] - wh.astype(np.float64)) / U[i, i]
+        Ws[:, i + 1:] -= np.outer(err, U[i, i + 1:])
+    return GptqResult(q, scale, zero, w_hat, w_hat / s32.astype(np.float64)[None, :])

@@ -494,3 +494,52 @@ def test_clip_share_of_a_whole_row_group_is_the_row_error(sym):
         Wq = gq.w_hat.astype(np.float64) / s32.astype(np.float64)[None, :]
         per_row = np.sum((X @ Wq.T - ref) ** 2, axis=0)
         assert np.allclose(r.errs[:, 0, i], per_row, rtol=1e-10, atol=0)
+
+
+# --------------------------------------------------------------------------
+# GPTQ rounding after AWQ scaling ("AWQ vs GPTQ ...", "GPTQ: compensate the
+# error you just made" and "Failure modes and combining the two")
+# --------------------------------------------------------------------------
+
+def test_inverse_hessian_factor_is_the_upper_cholesky_of_the_inverse():
+    rng = np.random.default_rng(10)
+    X = rng.normal(size=(40, 12))
+    X[:, 3] *= 15.0
+    U = O.inverse_hessian_factor(X, damp=0.01)
+    H = 2.0 * X.T @ X
+    H[np.diag_indices_from(H)] += 0.01 * np.mean(np.diag(H))
+    assert np.allclose(np.triu(U), U) and np.all(np.diag(U) > 0)
+    assert np.allclose(U.T @ U @ H, np.eye(12), atol=1e-9)
+
+
+@pytest.mark.parametrize("sym", [True, False])
+def test_gptq_with_uncorrelated_inputs_is_rtn(sym):
+    # X = 3 I: H is diagonal, so is U, and no error is passed on
+    rng = np.random.default_rng(11)
+    W = rng.normal(0, 0.02, size=(6, 64)).astype(np.float32)
+    r = O.gptq(W, 3.0 * np.eye(64), 4, 32, sym)
+    gq = O.quantize_groups(W, 4, 32, sym)
+    assert np.array_equal(r.q, gq.q) and np.array_equal(r.w_hat, gq.w_hat.astype(np.float64))
+
+
+def test_gptq_second_column_is_the_best_code_given_the_first():
+    # one row, two columns, one group: after column 0 is rounded, the
+    # quadratic error (w_hat - w)^T H (w_hat - w) is a parabola in column 1
+    # alone, so the nearest code to its minimum is the best code, found here
+    # by trying every code
+    rng = np.random.default_rng(12)
+    for trial in range(200):
+        X = rng.normal(size=(5, 2)) * rng.uniform(0.2, 3.0, size=2)
+        W = rng.normal(0, 0.5, size=(1, 2)).astype(np.float32)
+        r = O.gptq(W, X, 3, 2, True, damp=0.0)
+        H = 2.0 * X.T @ X
+        scale = float(r.scale[0, 0])
+        w = W[0].astype(np.float64)
+        errs = []
+        for code in range(-4, 4):
+            d = np.array([r.w_hat[0, 0], float(np.float32(code * np.float32(scale)))]) - w
+            errs.append(d @ H @ d)
+        errs = np.array(errs)
+        best = int(np.argmin(errs)) - 4
+        # the kept code is the best one, unless two codes are within rounding of a tie
+        assert r.q[0, 1] == best or errs[int(r.q[0, 1]) + 4] <= errs.min() * (1 + 1e-9), trial
