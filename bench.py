@@ -254,8 +254,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=2, help="alphas in the oracle's timed sample")
     ap.add_argument("--next-rows", action="store_true",
-                    help="also time the clipping search, output power, wide-group searches and the "
-                         "checkpoint export on the same layer (one extra JSON line each, rank 0)")
+                    help="also time the clipping search, output power, wide-group searches, GPTQ "
+                         "after AWQ and the checkpoint export on the same layer (one extra JSON "
+                         "line each, rank 0)")
     args = ap.parse_args()
     cfg = config_by_name(args.config)
     dist, rank, world = _dist()
@@ -384,6 +385,17 @@ def run_next_rows(args, cfg, tflops_peak, hbm_peak, peak_kind):
                      "roofline": {"bound": "tensor", "achieved": fl / t / 1e12, "peak": tflops_peak,
                                   "unit": "TFLOP/s", "frac": fl / t / 1e12 / tflops_peak,
                                   "peak_kind": peak_kind + " (whole call incl. the range pass)"}})
+
+    if g in (32, 64, 128):
+        t = timed(lambda: awq.awq_gptq(Wd, Xd, s_best, cfg.bits, g, cfg.sym, check=False))
+        # Hessian 2 N in^2, Cholesky in^3 / 3, triangular inverse in^3 / 3, error
+        # propagation out in^2 (each in multiply-adds: 2 flops)
+        fl = 2.0 * N * n_in ** 2 + 2.0 * n_in ** 3 / 3 * 2 + 2.0 * out * n_in ** 2 / 2 * 2
+        rows.append({"row": "gptq_after_awq", "metric": "layers/s", "value": 1.0 / t,
+                     "ms": t * 1e3,
+                     "roofline": {"bound": "alu", "achieved": fl / t / 1e12, "peak": fp32_peak,
+                                  "unit": "TFLOP/s", "frac": fl / t / 1e12 / fp32_peak,
+                                  "peak_kind": "fp32 FMA lanes x max clock"}})
 
     qw, sc, z = awq.awq_quantize_pack(Wd, s_best, cfg.bits, g, cfg.sym)
     if 32 % cfg.bits == 0:

@@ -252,6 +252,43 @@ int awq_quantize_pack_clipped(const void* W, int dtype, int64_t out, int64_t in,
                               uint8_t* zeros, int32_t* dev_status, awq_stream_t stream);
 
 /*
+ * awq_gptq - GPTQ's rounding after AWQ's scaling.
+ * ["AWQ vs GPTQ ...", "GPTQ: compensate the error you just made" (the
+ *  column-by-column rounding with error compensation through the Cholesky
+ *  factor of the inverse Hessian, dampening, lazily fitted group parameters)
+ *  and "Failure modes and combining the two" (AWQ's scaling, then GPTQ's
+ *  rounding).]
+ *
+ * Rounds W * diag(s) against the inputs X / s (s NULL: plain GPTQ):
+ *   H = 2 (X/s)^T (X/s) + damp * mean(diag) * I,  U^T U = H^-1 (U upper),
+ *   for each column i in natural order: at a group's first column its step
+ *   and zero point are fitted on the weights as corrected so far; column i
+ *   is rounded with awq_quantize_pack's quantizer; its error divided by
+ *   U[i][i] is taken off the later columns through row i of U.
+ *
+ *   W, X, dtype, out, in, N   as for awq_search
+ *   s       [in] float or NULL
+ *   bits, group, sym          as for awq_quantize_pack; group in {32, 64, 128}
+ *   damp    >= 0 (the pages' default is 0.01)
+ *   workspace, workspace_bytes >= awq_gptq_workspace_bytes(out, in, N)
+ *           (about 8 in^2 + 5 out*in + 4 N*in bytes)
+ *   qweight, scales, zeros   as awq_quantize_pack writes them (the codes of
+ *           W * s; decode as scale * (code - zero), then divide by s)
+ * Arithmetic is fp32 (the Hessian, its factors and the running weights), so
+ * codes can differ from a float64 evaluation where a corrected weight sits
+ * within rounding of a decision boundary.  A Hessian that is not positive
+ * definite after dampening sets AWQ_ERR_NONFINITE.
+ */
+size_t awq_gptq_workspace_bytes(int64_t out, int64_t in, int64_t N);
+
+int awq_gptq(const void* W, const void* X, int dtype,
+             int64_t out, int64_t in, int64_t N, const float* s,
+             int bits, int group, int sym, double damp,
+             void* workspace, size_t workspace_bytes,
+             uint32_t* qweight, float* scales, uint8_t* zeros,
+             int32_t* dev_status, awq_stream_t stream);
+
+/*
  * awq_export_checkpoint - the tensors a quantized checkpoint stores for one
  * linear layer, from awq_quantize_pack's outputs.
  * ["AWQ vs GPTQ ...", "What lands on disk": qweight int32 words packing

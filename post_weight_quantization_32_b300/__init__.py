@@ -31,7 +31,7 @@ __all__ = [
     "awq_search_workspace_bytes", "awq_quantize_pack", "new_status", "check_status", "STATUS",
     "DTYPE", "awq_search_noalloc", "NOALLOC_SCRATCH_BYTES", "awq_output_power", "awq_sweep",
     "awq_export_checkpoint", "awq_clip_search", "awq_clip_search_workspace_bytes",
-    "awq_quantize_pack_clipped",
+    "awq_quantize_pack_clipped", "awq_gptq", "awq_gptq_workspace_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -44,7 +44,7 @@ STATUS = {0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARG", 2: "AWQ_ERR_UNSUPPORTED", 3: "A
 EXPORTS = ("awq_status_string", "awq_channel_stats", "awq_search_workspace_bytes", "awq_search",
            "awq_search_ex", "awq_quantize_pack", "awq_search_noalloc", "awq_output_power",
            "awq_export_checkpoint", "awq_clip_search", "awq_clip_search_workspace_bytes",
-           "awq_quantize_pack_clipped")
+           "awq_quantize_pack_clipped", "awq_gptq", "awq_gptq_workspace_bytes")
 
 # Size of the library's fixed scratch array used by awq_search_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -80,6 +80,11 @@ def _load() -> ctypes.CDLL:
     L.awq_quantize_pack_clipped.restype = i32
     L.awq_quantize_pack_clipped.argtypes = [vp, i32, i64, i64, vp, i32, i32, i32, vp, vp, vp, vp,
                                             vp, vp]
+    L.awq_gptq_workspace_bytes.restype = sz
+    L.awq_gptq_workspace_bytes.argtypes = [i64, i64, i64]
+    L.awq_gptq.restype = i32
+    L.awq_gptq.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, ctypes.c_double, vp, sz,
+                           vp, vp, vp, vp, vp]
     L.awq_search_noalloc.restype = i32
     L.awq_search_noalloc.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, i32, vp, vp, vp,
                                      vp, vp]
@@ -360,4 +365,34 @@ def awq_quantize_pack_clipped(W: torch.Tensor, s: torch.Tensor, clip: torch.Tens
            "awq_quantize_pack_clipped")
     if check:
         check_status(st, "awq_quantize_pack_clipped")
+    return qw, sc, z
+
+
+def awq_gptq_workspace_bytes(n_out: int, n_in: int, N: int) -> int:
+    return int(lib.awq_gptq_workspace_bytes(n_out, n_in, N))
+
+
+def awq_gptq(W: torch.Tensor, X: torch.Tensor, s: Optional[torch.Tensor] = None, bits: int = 4,
+             group: int = 128, sym: bool = True, damp: float = 0.01, stream=None,
+             dev_status: Optional[torch.Tensor] = None, check: bool = True):
+    """GPTQ's rounding of W * diag(s) against X / s (s None: plain GPTQ);
+    returns (qweight, scales, zeros) laid out as ``awq_quantize_pack``'s."""
+    _need(W, "W", 2)
+    _need(X, "X", 2)
+    if W.dtype != X.dtype or W.shape[1] != X.shape[1]:
+        raise ValueError("W and X must share dtype and the input dimension")
+    n_out, n_in = W.shape
+    N = X.shape[0]
+    dev = W.device
+    ws = torch.empty(max(awq_gptq_workspace_bytes(n_out, n_in, N), 256), dtype=torch.uint8,
+                     device=dev)
+    qw = torch.empty((n_out, (n_in * bits + 31) // 32), dtype=torch.int32, device=dev)
+    sc = torch.empty((n_out, n_in // group), dtype=torch.float32, device=dev)
+    z = torch.empty((n_out, n_in // group), dtype=torch.uint8, device=dev)
+    st = dev_status if dev_status is not None else new_status(dev)
+    _check(lib.awq_gptq(_ptr(W), _ptr(X), DTYPE[W.dtype], n_out, n_in, N, _ptr(s), bits, group,
+                        1 if sym else 0, float(damp), _ptr(ws), ws.numel(), _ptr(qw), _ptr(sc),
+                        _ptr(z), _ptr(st), _stream(stream)), "awq_gptq")
+    if check:
+        check_status(st, "awq_gptq")
     return qw, sc, z

@@ -281,6 +281,30 @@ int awq_clip_search(const void* W, const void* X, int dtype, int64_t out, int64_
                                         clip, errs, dev_status, (cudaStream_t)stream));
 }
 
+size_t awq_gptq_workspace_bytes(int64_t out, int64_t in, int64_t N) {
+  if (out < 1 || in < 1 || N < 1) return 0;
+  return gptq_layout(out, in, N).total;
+}
+
+int awq_gptq(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
+             const float* s, int bits, int group, int sym, double damp, void* workspace,
+             size_t workspace_bytes, uint32_t* qweight, float* scales, uint8_t* zeros,
+             int32_t* dev_status, awq_stream_t stream) {
+  if (!W || !X || !workspace || !qweight || !scales || !zeros || !dtype_ok(dtype))
+    return AWQ_ERR_INVALID_ARG;
+  if (out < 1 || in < 1 || N < 1 || bits < 2 || bits > 8 || group < 1 || in % group != 0 ||
+      !(damp >= 0.0))
+    return AWQ_ERR_INVALID_ARG;
+  if (group != 32 && group != 64 && group != 128) return AWQ_ERR_UNSUPPORTED;
+  if (in > (1 << 30) / in || out > (1 << 24) || N > (1 << 24)) return AWQ_ERR_UNSUPPORTED;
+  if (workspace_bytes < gptq_layout(out, in, N).total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return AWQ_ERR_INVALID_ARG;
+  return cuda_status(launch_gptq(W, X, dtype, out, in, N, s, bits, group, sym ? 1 : 0,
+                                 (float)damp, workspace, qweight, scales, zeros, dev_status,
+                                 (cudaStream_t)stream));
+}
+
 int awq_export_checkpoint(const uint32_t* qweight, const float* scales, const uint8_t* zeros,
                           int64_t out, int64_t in, int bits, int group, uint32_t* qweight_t,
                           void* scales_h, uint32_t* qzeros, int32_t* dev_status,

@@ -1,0 +1,458 @@
+// GPTQ's rounding of W * diag(s) against the inputs X / s: AWQ's scaling
+// first, then GPTQ's choice of integers ("AWQ vs GPTQ Quantization
+// Architectures Compared", "GPTQ: compensate the error you just made" and
+// "Failure modes and combining the two").
+//
+//   H  = 2 Xs^T Xs + damp * mean(diag) * I,   Xs = X / s
+//   U  = upper Cholesky factor of H^-1 (U^T U = H^-1)
+//   for each column i (natural order): at a group's first column fit the
+//   group's step and zero on the corrected weights; round column i with the
+//   float32 quantizer; err = (w - w_hat) / U[i][i]; w[:, j>i] -= err U[i][j]
+//
+// Everything runs in fp32 on the CUDA cores, in this order:
+//  1. Xr = X / s with its columns reversed (Xr = Xs J, J the exchange matrix).
+//  2. A = 2 Xr^T Xr = J H J (a GEMM), dampened on its diagonal.
+//  3. A = M M^T, M lower (blocked right-looking Cholesky: a one-CTA factor of
+//     each 32 x 32 diagonal block, a row-parallel triangular solve for the
+//     panel below it, a GEMM for the trailing matrix).
+//  4. Y = M^-1 (blocked: the inverse of each diagonal block in one CTA, then
+//     Y[i, :i] = -Y[i, i] (M[i, :i] Y[:i, :i]) by two GEMMs).
+//  5. U = J Y J: with H = J M M^T J = R R^T, R = J M J upper, H^-1 = R^-T R^-1,
+//     so U = R^-1 = J M^-1 J (upper, positive diagonal: the Cholesky factor).
+//  6. The sweep in blocks of 128 columns: one thread per row runs the block's
+//     columns in order with the block's rows of U and the row's block of
+//     weights in shared memory, writing codes and the scaled errors; a GEMM
+//     then applies the block's errors to all later columns.
+//  7. The codes are packed as awq_quantize_pack packs them.
+#include <algorithm>
+
+#include "awq_device.cuh"
+#include "awq_internal.h"
+
+namespace awq {
+
+namespace {
+
+// ---------------------------------------------------------------- fp32 GEMM
+// C[m][n] = alpha * sum_k A(m, k) B(k, n) + beta * C[m][n]; A(m, k) is
+// A[m * lda + k] (or A[k * lda + m] when ta), B(k, n) is B[k * ldb + n] (or
+// B[n * ldb + k] when tb).  64 x 64 tiles, 16-deep k steps, 4 x 4 outputs a
+// thread.
+constexpr int kGT = 64, kGK = 16;
+
+__global__ void __launch_bounds__(256) sgemm_kernel(int m, int n, int k, float alpha,
+                                                    const float* __restrict__ A, int64_t lda,
+                                                    int ta, const float* __restrict__ B,
+                                                    int64_t ldb, int tb, float beta,
+                                                    float* __restrict__ C, int64_t ldc) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float as[kGK][kGT + 4], bs[kGK][kGT + 4];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * kGT, n0 = blockIdx.x * kGT;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < k; k0 += kGK) {
+    for (int i = threadIdx.x; i < kGK * kGT; i += 256) {
+      const int kk = i / kGT, mm = i % kGT;
+      const int gm = m0 + mm, gk = k0 + kk;
+      float a = 0.0f;
+      if (gm < m && gk < k) a = ta ? A[(int64_t)gk * lda + gm] : A[(int64_t)gm * lda + gk];
+      as[kk][mm] = a;
+      const int gn = n0 + mm;
+      float b = 0.0f;
+      if (gn < n && gk < k) b = tb ? B[(int64_t)gn * ldb + gk] : B[(int64_t)gk * ldb + gn];
+      bs[kk][mm] = b;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kGK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        a[r] = as[kk][ty * 4 + r];
+        b[r] = bs[kk][tx * 4 + r];
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int gm = m0 + ty * 4 + r, gn = n0 + tx * 4 + c;
+      if (gm < m && gn < n) {
+        float* p = C + (int64_t)gm * ldc + gn;
+        *p = beta == 0.0f ? alpha * acc[r][c] : fmaf(alpha, acc[r][c], beta * *p);
+      }
+    }
+}
+
+cudaError_t sgemm(cudaStream_t s, int m, int n, int k, float alpha, const float* A, int64_t lda,
+                  int ta, const float* B, int64_t ldb, int tb, float beta, float* C, int64_t ldc) {
+  if (m <= 0 || n <= 0 || k <= 0) return cudaSuccess;
+  const dim3 grid((unsigned)((n + kGT - 1) / kGT), (unsigned)((m + kGT - 1) / kGT));
+  return launch_pdl(sgemm_kernel, grid, dim3(256), 0, s, m, n, k, alpha, A, lda, ta, B, ldb, tb,
+                    beta, C, ldc);
+}
+
+// ------------------------------------------------------- inputs and Hessian
+// Xr[t][j] = X[t][in - 1 - j] / s[in - 1 - j] (fp32)
+template <typename T>
+__global__ void __launch_bounds__(256) scale_reverse_kernel(const T* __restrict__ X, int64_t N,
+                                                            int64_t in, const float* __restrict__ s,
+                                                            float* __restrict__ Xr) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t total = N * in;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / in, j = i % in, src = in - 1 - j;
+    const float sv = s != nullptr ? s[src] : 1.0f;
+    Xr[i] = Elt<T>::to_f32(X[t * in + src]) / sv;
+  }
+}
+
+// A[i][i] += damp * mean(diag A); one CTA
+__global__ void __launch_bounds__(1024) damp_kernel(float* __restrict__ A, int64_t n, float damp) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ double part[32];
+  double acc = 0.0;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) acc += (double)A[i * n + i];
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += part[w];
+    part[0] = t;
+  }
+  __syncthreads();
+  const float add = damp * (float)(part[0] / (double)n);
+  __syncthreads();
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) A[i * n + i] += add;
+}
+
+// ------------------------------------------------------- blocked Cholesky
+constexpr int kCB = 32;  // Cholesky / inverse block
+
+// Factor the diagonal block A[k0:k0+b, k0:k0+b] = L L^T in place (lower).
+// A non-positive pivot sets the status (the matrix is not positive definite).
+__global__ void __launch_bounds__(kCB * kCB) chol_diag_kernel(float* __restrict__ A, int64_t n,
+                                                             int64_t k0, int b,
+                                                             int32_t* dev_status) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float L[kCB][kCB + 1];
+  const int r = threadIdx.x / kCB, c = threadIdx.x % kCB;
+  if (r < b && c < b) L[r][c] = A[(k0 + r) * n + k0 + c];
+  __syncthreads();
+  for (int j = 0; j < b; ++j) {
+    if (threadIdx.x == 0) {
+      float d = L[j][j];
+      for (int t = 0; t < j; ++t) d -= L[j][t] * L[j][t];
+      if (!(d > 0.0f)) {
+        set_status(dev_status, ST_NONFINITE);
+        d = 1e-30f;
+      }
+      L[j][j] = sqrtf(d);
+    }
+    __syncthreads();
+    if (c == 0 && r > j && r < b) {
+      float v = L[r][j];
+      for (int t = 0; t < j; ++t) v -= L[r][t] * L[j][t];
+      L[r][j] = v / L[j][j];
+    }
+    __syncthreads();
+  }
+  if (r < b && c < b) A[(k0 + r) * n + k0 + c] = c <= r ? L[r][c] : 0.0f;
+}
+
+// Rows i >= k0 + b: solve x L11^T = A[i, k0:k0+b] (one thread per row).
+__global__ void __launch_bounds__(128) chol_panel_kernel(float* __restrict__ A, int64_t n,
+                                                        int64_t k0, int b) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float L[kCB][kCB + 1];
+  for (int i = threadIdx.x; i < b * b; i += blockDim.x)
+    L[i / b][i % b] = A[(k0 + i / b) * n + k0 + i % b];
+  __syncthreads();
+  const int64_t row = k0 + b + blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (row >= n) return;
+  float x[kCB];
+  float* a = A + row * n + k0;
+#pragma unroll
+  for (int j = 0; j < kCB; ++j) {
+    if (j < b) {
+      float v = a[j];
+      for (int t = 0; t < j; ++t) v -= x[t] * L[j][t];
+      x[j] = v / L[j][j];
+      a[j] = x[j];
+    }
+  }
+}
+
+// ------------------------------------------------- blocked lower inverse
+// Y[i0:i0+b, i0:i0+b] = inverse of the lower block M[i0:i0+b, i0:i0+b]:
+// thread c solves M y = e_c by forward substitution.
+__global__ void __launch_bounds__(kCB) tri_inv_diag_kernel(const float* __restrict__ M,
+                                                           float* __restrict__ Y, int64_t n,
+                                                           int64_t i0, int b) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float L[kCB][kCB + 1];
+  for (int i = threadIdx.x; i < b * b; i += blockDim.x)
+    L[i / b][i % b] = M[(i0 + i / b) * n + i0 + i % b];
+  __syncthreads();
+  const int c = threadIdx.x;
+  if (c >= b) return;
+  float y[kCB];
+#pragma unroll
+  for (int r = 0; r < kCB; ++r) {
+    if (r < b) {
+      float v = r == c ? 1.0f : 0.0f;
+      for (int t = 0; t < r; ++t) v -= L[r][t] * y[t];
+      y[r] = v / L[r][r];
+      Y[(i0 + r) * n + i0 + c] = y[r];
+    }
+  }
+}
+
+// U[r][c] = Y[n-1-r][n-1-c]
+__global__ void __launch_bounds__(256) reverse_kernel(const float* __restrict__ Y,
+                                                      float* __restrict__ U, int64_t n) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t total = n * n;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / n, c = i % n;
+    U[i] = Y[(n - 1 - r) * n + (n - 1 - c)];
+  }
+}
+
+// Ws = W * s (fp32 working copy)
+template <typename T>
+__global__ void __launch_bounds__(256) scale_weights_kernel(const T* __restrict__ W, int64_t out,
+                                                            int64_t in, const float* __restrict__ s,
+                                                            float* __restrict__ Ws) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t total = out * in;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float w = Elt<T>::to_f32(W[i]);
+    Ws[i] = s != nullptr ? __fmul_rn(w, s[i % in]) : w;
+  }
+}
+
+// ------------------------------------------------------------ the sweep
+constexpr int kSB = 128;       // columns per sweep block
+constexpr int kSRows = 128;    // rows per CTA of the in-block kernel
+
+// One thread per row runs columns b0 .. b0+bw-1 in order.  Shared memory:
+// U[b0:b0+bw, b0:b0+bw] and the CTA's rows of the weight block, [col][row].
+// Writes the storage codes, the group steps and zero points, and
+// Err[row][i - b0] = (w - w_hat) / U[i][i].
+__global__ void __launch_bounds__(kSRows) sweep_block_kernel(
+    float* __restrict__ Ws, const float* __restrict__ U, int64_t out, int64_t in, int64_t b0,
+    int bw, int group, int bits, int sym, uint8_t* __restrict__ codes, float* __restrict__ scales,
+    uint8_t* __restrict__ zeros, float* __restrict__ Err) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ float sm[];
+  float* Ub = sm;                   // [kSB][kSB]
+  float* wb = sm + kSB * kSB;       // [kSB][kSRows]
+  for (int i = threadIdx.x; i < bw * bw; i += blockDim.x)
+    Ub[(i / bw) * kSB + i % bw] = U[(b0 + i / bw) * in + b0 + i % bw];
+  const int64_t row = (int64_t)blockIdx.x * kSRows + threadIdx.x;
+  const bool live = row < out;
+  if (live)
+    for (int j = 0; j < bw; ++j) wb[j * kSRows + threadIdx.x] = Ws[row * in + b0 + j];
+  __syncthreads();
+  if (!live) return;
+  const float Lf = (float)((1 << (bits - 1)) - 1), maxqf = (float)((1 << bits) - 1);
+  const int64_t ng = in / group;
+  float scale = 1.0f, zero = 0.0f;
+  for (int i = 0; i < bw; ++i) {
+    const int64_t col = b0 + i;
+    if (col % group == 0) {  // fit the group on the corrected weights
+      float m = 0.0f, lo = 0.0f, hi = 0.0f;
+      for (int j = i; j < i + group && j < bw; ++j) {
+        const float v = wb[j * kSRows + threadIdx.x];
+        m = fmaxf(m, fabsf(v));
+        lo = fminf(lo, v);
+        hi = fmaxf(hi, v);
+      }
+      if (sym) {
+        scale = fmaxf(__fdiv_rn(m, Lf), 1e-8f);
+        zero = 0.0f;
+      } else {
+        scale = fmaxf(__fdiv_rn(__fsub_rn(hi, lo), maxqf), 1e-8f);
+        zero = rintf(__fdiv_rn(-lo, scale));
+      }
+      scales[row * ng + col / group] = scale;
+      zeros[row * ng + col / group] = (uint8_t)(sym ? (1 << (bits - 1)) : (int)zero);
+    }
+    const float w = wb[i * kSRows + threadIdx.x];
+    float q, what;
+    if (sym) {
+      q = fminf(fmaxf(rintf(__fdiv_rn(w, scale)), -Lf - 1.0f), Lf);
+      what = __fmul_rn(q, scale);
+      codes[row * in + col] = (uint8_t)((int)q + (1 << (bits - 1)));
+    } else {
+      q = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(w, scale)), zero), 0.0f), maxqf);
+      what = __fmul_rn(scale, __fsub_rn(q, zero));
+      codes[row * in + col] = (uint8_t)q;
+    }
+    const float err = (w - what) / Ub[i * kSB + i];
+    Err[row * kSB + i] = err;
+    for (int j = i + 1; j < bw; ++j) wb[j * kSRows + threadIdx.x] -= err * Ub[i * kSB + j];
+  }
+}
+
+// qweight[row][k]: bits [32k, 32k + 32) of the row's little-endian stream of
+// b-bit codes.
+__global__ void __launch_bounds__(256) pack_codes_kernel(const uint8_t* __restrict__ codes,
+                                                         int64_t out, int64_t in, int bits,
+                                                         uint32_t* __restrict__ qweight,
+                                                         int64_t nwords) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t total = out * nwords;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / nwords, k = i % nwords;
+    uint32_t word = 0u;
+    const int64_t c0 = (32 * k) / bits, c1 = std::min<int64_t>(in, (32 * k + 31) / bits + 1);
+    for (int64_t c = c0; c < c1; ++c) {
+      const int64_t bit = c * bits - 32 * k;  // may be negative for a code straddling in
+      const uint32_t u = codes[row * in + c];
+      if (bit >= 0)
+        word |= u << bit;
+      else
+        word |= u >> (-bit);
+    }
+    qweight[i] = word;
+  }
+}
+
+unsigned grid_for_elems(int64_t n) {
+  return (unsigned)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256,
+                                                          (int64_t)device_sm_count() * 8));
+}
+
+}  // namespace
+
+GptqLayout gptq_layout(int64_t out, int64_t in, int64_t N) {
+  GptqLayout w{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  w.xr = take((size_t)N * in * 4);
+  w.h = take((size_t)in * in * 4);
+  w.y = take((size_t)in * in * 4);
+  w.t = take((size_t)kCB * in * 4);
+  w.ws = take((size_t)out * in * 4);
+  w.err = take((size_t)out * kSB * 4);
+  w.codes = take((size_t)out * in);
+  w.total = o;
+  return w;
+}
+
+cudaError_t launch_gptq(const void* W, const void* X, int dt, int64_t out, int64_t in, int64_t N,
+                        const float* s, int bits, int group, int sym, float damp, void* workspace,
+                        uint32_t* qweight, float* scales, uint8_t* zeros, int32_t* dev_status,
+                        cudaStream_t st) {
+  const GptqLayout L = gptq_layout(out, in, N);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  float* Xr = reinterpret_cast<float*>(wsb + L.xr);
+  float* A = reinterpret_cast<float*>(wsb + L.h);     // J H J, then M, later U
+  float* Y = reinterpret_cast<float*>(wsb + L.y);     // M^-1
+  float* T = reinterpret_cast<float*>(wsb + L.t);
+  float* Ws = reinterpret_cast<float*>(wsb + L.ws);
+  float* Err = reinterpret_cast<float*>(wsb + L.err);
+  uint8_t* codes = wsb + L.codes;
+  cudaError_t e;
+#define AWQ_TRY(x)                      \
+  do {                                  \
+    if ((e = (x)) != cudaSuccess) return e; \
+  } while (0)
+  // 1-2: Xr = (X / s) J, A = 2 Xr^T Xr + damping
+  switch (dt) {
+    case kDtF32:
+      AWQ_TRY(launch_pdl(scale_reverse_kernel<float>, grid_for_elems(N * in), 256, 0, st,
+                         static_cast<const float*>(X), N, in, s, Xr));
+      AWQ_TRY(launch_pdl(scale_weights_kernel<float>, grid_for_elems(out * in), 256, 0, st,
+                         static_cast<const float*>(W), out, in, s, Ws));
+      break;
+    case kDtF16:
+      AWQ_TRY(launch_pdl(scale_reverse_kernel<__half>, grid_for_elems(N * in), 256, 0, st,
+                         static_cast<const __half*>(X), N, in, s, Xr));
+      AWQ_TRY(launch_pdl(scale_weights_kernel<__half>, grid_for_elems(out * in), 256, 0, st,
+                         static_cast<const __half*>(W), out, in, s, Ws));
+      break;
+    default:
+      AWQ_TRY(launch_pdl(scale_reverse_kernel<__nv_bfloat16>, grid_for_elems(N * in), 256, 0, st,
+                         static_cast<const __nv_bfloat16*>(X), N, in, s, Xr));
+      AWQ_TRY(launch_pdl(scale_weights_kernel<__nv_bfloat16>, grid_for_elems(out * in), 256, 0,
+                         st, static_cast<const __nv_bfloat16*>(W), out, in, s, Ws));
+      break;
+  }
+  AWQ_TRY(sgemm(st, (int)in, (int)in, (int)N, 2.0f, Xr, in, 1, Xr, in, 0, 0.0f, A, in));
+  AWQ_TRY(launch_pdl(damp_kernel, 1, 1024, 0, st, A, in, damp));
+  // 3: A = M M^T
+  for (int64_t k0 = 0; k0 < in; k0 += kCB) {
+    const int b = (int)std::min<int64_t>(kCB, in - k0);
+    AWQ_TRY(launch_pdl(chol_diag_kernel, 1, kCB * kCB, 0, st, A, in, k0, b, dev_status));
+    const int64_t rest = in - k0 - b;
+    if (rest > 0) {
+      AWQ_TRY(launch_pdl(chol_panel_kernel, (unsigned)((rest + 127) / 128), 128, 0, st, A, in, k0,
+                         b));
+      AWQ_TRY(sgemm(st, (int)rest, (int)rest, b, -1.0f, A + (k0 + b) * in + k0, in, 0,
+                    A + (k0 + b) * in + k0, in, 1, 1.0f, A + (k0 + b) * in + k0 + b, in));
+    }
+  }
+  // 4: Y = M^-1 (Y starts at zero above the diagonal)
+  AWQ_TRY(cudaMemsetAsync(Y, 0, (size_t)in * in * 4, st));
+  for (int64_t i0 = 0; i0 < in; i0 += kCB) {
+    const int b = (int)std::min<int64_t>(kCB, in - i0);
+    AWQ_TRY(launch_pdl(tri_inv_diag_kernel, 1, kCB, 0, st, A, Y, in, i0, b));
+    if (i0 > 0) {
+      AWQ_TRY(sgemm(st, b, (int)i0, (int)i0, 1.0f, A + i0 * in, in, 0, Y, in, 0, 0.0f, T, i0));
+      AWQ_TRY(sgemm(st, b, (int)i0, b, -1.0f, Y + i0 * in + i0, in, 0, T, i0, 0, 0.0f,
+                    Y + i0 * in, in));
+    }
+  }
+  // 5: U = J Y J, into A's storage
+  AWQ_TRY(launch_pdl(reverse_kernel, grid_for_elems(in * in), 256, 0, st, Y, A, in));
+  const float* U = A;
+  // 6: the sweep
+  const size_t smem = (size_t)(kSB * kSB + kSB * kSRows) * 4;
+  AWQ_TRY(cudaFuncSetAttribute(sweep_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem));
+  for (int64_t b0 = 0; b0 < in; b0 += kSB) {
+    const int bw = (int)std::min<int64_t>(kSB, in - b0);
+    AWQ_TRY(launch_pdl(sweep_block_kernel, (unsigned)((out + kSRows - 1) / kSRows), kSRows, smem,
+                       st, Ws, U, out, in, b0, bw, group, bits, sym, codes, scales, zeros, Err));
+    const int64_t rest = in - b0 - bw;
+    if (rest > 0)
+      AWQ_TRY(sgemm(st, (int)out, (int)rest, bw, -1.0f, Err, kSB, 0, U + b0 * in + b0 + bw, in, 0,
+                    1.0f, Ws + b0 + bw, in));
+  }
+  // 7: pack
+  const int64_t nwords = (in * bits + 31) / 32;
+  AWQ_TRY(launch_pdl(pack_codes_kernel, grid_for_elems(out * nwords), 256, 0, st, codes, out, in,
+                     bits, qweight, nwords));
+#undef AWQ_TRY
+  return cudaSuccess;
+}
+
+}  // namespace awq

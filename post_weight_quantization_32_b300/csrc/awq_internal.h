@@ -169,6 +169,23 @@ cudaError_t launch_clip_search(const void* W, const void* X, int dt, int64_t out
                                const ClipFactors& cf, float* H, float* clip, float* errs,
                                int32_t* dev_status, cudaStream_t stream);
 
+// ---- GPTQ rounding after AWQ scaling (awq_gptq.cu)
+// Workspace regions (byte offsets, 256-aligned): X / s reversed (N x in),
+// the Hessian / its factors (in x in twice), a 32 x in scratch, the fp32
+// working weights (out x in), the errors of one sweep block (out x 128) and
+// the byte codes (out x in).
+struct GptqLayout {
+  size_t xr, h, y, t, ws, err, codes, total;
+};
+GptqLayout gptq_layout(int64_t out, int64_t in, int64_t N);
+// s may be null (plain GPTQ).  group in {32, 64, 128}.  Outputs as
+// launch_quantize_pack.  A Hessian that is not positive definite after
+// dampening sets ST_NONFINITE.
+cudaError_t launch_gptq(const void* W, const void* X, int dt, int64_t out, int64_t in, int64_t N,
+                        const float* s, int bits, int group, int sym, float damp, void* workspace,
+                        uint32_t* qweight, float* scales, uint8_t* zeros, int32_t* dev_status,
+                        cudaStream_t st);
+
 // ---- checkpoint export (awq_export.cu)
 // From quantize_pack's row-major outputs (bits divides 32, in % (32/bits) ==
 // 0): qweight_t [in*bits/32][out] (transposed words), scales_h [in/g][out]

@@ -195,3 +195,12 @@ def test_export_and_clipped_pack_reject_bad_arguments_on_host(lib):
                                               vp, vp]
     assert lib.awq_quantize_pack_clipped(f, 2, 4, 8, f, 4, 8, 1, None, f, f, f, None, None) == 1
     assert lib.awq_quantize_pack_clipped(f, 2, 4, 8, f, 4, 3, 1, f, f, f, f, None, None) == 1
+
+
+def test_binding_wrappers_pass_one_label_to_the_status_check():
+    # every wrapper reports a failing C call under its own name
+    import ast
+    src = open(os.path.join(ROOT, "post_weight_quantization_32_b300", "__init__.py")).read()
+    calls = [n for n in ast.walk(ast.parse(src))
+             if isinstance(n, ast.Call) and getattr(n.func, "id", "") == "_check"]
+    assert calls and all(len(c.args) == 2 and isinstance(c.args[1], ast.Constant) for c in calls)

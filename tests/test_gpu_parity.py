@@ -311,6 +311,47 @@ def test_clip_search_matches_oracle(awq, case):
     assert np.array_equal(z.cpu().numpy(), zo)
 
 
+GPTQ_CASES = [
+    # (out, in, N, dtype, bits, group, sym, with AWQ scales)
+    (64, 256, 512, "bf16", 4, 128, True, True),
+    (48, 384, 300, "f16", 3, 64, False, True),
+    (37, 160, 50, "f32", 4, 32, True, False),      # fewer tokens than inputs; partial blocks
+    (96, 512, 2048, "bf16", 2, 128, False, True),
+]
+
+
+@pytest.mark.parametrize("case", GPTQ_CASES, ids=lambda c: "%dx%d_n%d_%s_b%d_g%d_%s_%s" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], "sym" if c[6] else "asym", "awq" if c[7] else "plain"))
+def test_gptq_matches_oracle(awq, case):
+    out, n_in, N, dtype, bits, group, sym, with_s = case
+    W, X = make_random_layer(out, n_in, N, dtype=dtype, seed=out * 7 + n_in,
+                             n_outlier=max(1, n_in // 64))
+    s32 = (np.random.default_rng(n_in).uniform(0.5, 2.0, size=n_in).astype(np.float32)
+           if with_s else None)
+    Wd, Xd = _dev(W, X)
+    qw, sc, z = awq.awq_gptq(Wd, Xd, None if s32 is None else torch.from_numpy(s32).cuda(), bits,
+                             group, sym)
+    r = O.gptq(_np_w(W), _np_x(X), bits, group, sym, s32)
+    u_ref = O.stored_codes(r.q, bits, sym)
+    u = O.unpack_bits(qw.cpu().numpy().view(np.uint32), bits, n_in)
+    # fp32 against float64 running weights: a code may differ where a corrected
+    # weight lies within rounding of a decision boundary
+    assert (u != u_ref).mean() <= 1e-3
+    z_ref = (np.full(r.zero.shape, 1 << (bits - 1)) if sym else r.zero).astype(np.uint8)
+    assert (z.cpu().numpy() != z_ref).mean() <= 1e-3
+    assert np.allclose(sc.cpu().numpy(), r.scale, rtol=1e-4, atol=0)
+    # the layer's output error matches the oracle's
+    g = np.arange(n_in) // group
+    zz = z.cpu().numpy().astype(np.float64)[:, g]
+    w_hat = sc.cpu().numpy().astype(np.float64)[:, g] * (u.astype(np.float64) - zz)
+    s64 = np.ones(n_in) if s32 is None else s32.astype(np.float64)
+    Xn = _np_x(X)
+    ref = Xn @ _np_w(W).astype(np.float64).T
+    e_gpu = O.output_mse(Xn, w_hat / s64[None, :], ref)
+    e_ref = O.output_mse(Xn, r.Wq, ref)
+    assert abs(e_gpu - e_ref) <= ERR_RTOL * e_ref, (e_gpu, e_ref)
+
+
 def test_search_shared_input_group(awq):
     """q/k/v share X and one s: the concatenated rows are searched at once."""
     ws, X = [], None
