@@ -49,6 +49,12 @@ codes are b-bit unsigned, symmetric codes stored offset-binary
 u = q + 2^(b-1) with zero = 2^(b-1); code i of a row sits at bit i*b of that
 row's little-endian uint32 bitstream; scales float32 [out][in/g]; zeros
 uint8 [out][in/g].
+
+Beyond the search itself, each from the page and section it cites:
+output_power / sweep (relative output error, bit-width and group-size
+sweeps), clip_search / quantize_pack_clipped (the per-group clipping
+search), export_checkpoint / dequantize_checkpoint (the checkpoint
+tensors) and gptq (GPTQ's rounding after AWQ's scaling).
 """
 from __future__ import annotations
 

@@ -17,6 +17,17 @@ Entry points (same names as the C ABI):
 * ``awq_search_noalloc(W, X, bits, group, sym, grid)`` -> as ``awq_search``,
   but the library's fixed scratch array (``NOALLOC_SCRATCH_BYTES``) stands
   in for the workspace, for callers that cannot allocate device memory
+* ``awq_output_power(W, X)`` -> mean((X W^T)^2) (float64 [1]), the
+  denominator of the relative output error; ``awq_sweep(W, X, settings)``
+  runs the search over (bits, group) settings and reports RTN beside AWQ,
+  absolute and relative
+* ``awq_clip_search(W, X, s, bits, group, sym)`` -> (clip factors
+  [out, in/group], shares or None); ``awq_quantize_pack_clipped(W, s, clip,
+  ...)`` packs at those factors
+* ``awq_gptq(W, X, s, bits, group, sym, damp)`` -> (qweight, scales, zeros)
+  from GPTQ's rounding of W * diag(s) against X / s
+* ``awq_export_checkpoint(qweight, scales, zeros, in, bits, group)`` ->
+  (qweight [in*b/32, out], fp16 scales [in/g, out], packed zeros)
 """
 from __future__ import annotations
 
