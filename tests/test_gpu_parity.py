@@ -352,6 +352,24 @@ def test_gptq_matches_oracle(awq, case):
     assert abs(e_gpu - e_ref) <= ERR_RTOL * e_ref, (e_gpu, e_ref)
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_search_degenerate_layers(awq, dtype):
+    """All-zero weights: every error is 0 and alpha 0 is kept; all-zero
+    inputs: flat salience, every alpha is RTN, alpha 0 is kept."""
+    W, X = make_random_layer(128, 256, 32, dtype=dtype, seed=21)
+    zw = torch.zeros_like(W)
+    err, best, _ = awq.awq_search(*_dev(zw, X), 4, 128, False, 8)
+    assert int(best.item()) == 0 and torch.all(err == 0)
+    qw, sc, z = awq.awq_quantize_pack(zw.cuda(), torch.ones(256, device="cuda"), 4, 128, True)
+    assert torch.all(sc == torch.tensor(1e-8, dtype=torch.float32, device="cuda"))
+    assert np.all(O.unpack_bits(qw.cpu().numpy().view(np.uint32), 4, 256) == 8)
+    zx = torch.zeros_like(X)
+    err, best, s_best = awq.awq_search(*_dev(W, zx), 4, 128, True, 8)
+    res = O.awq_search(_np_w(W), _np_x(zx), bits=4, group=128, grid=8, sym=True)
+    assert int(best.item()) == 0 and torch.all(s_best == 1.0)
+    assert np.all(err.cpu().numpy() == 0) and np.all(res.errs == 0)
+
+
 def test_search_shared_input_group(awq):
     """q/k/v share X and one s: the concatenated rows are searched at once."""
     ws, X = [], None

@@ -543,3 +543,28 @@ def test_gptq_second_column_is_the_best_code_given_the_first():
         best = int(np.argmin(errs)) - 4
         # the kept code is the best one, unless two codes are within rounding of a tie
         assert r.q[0, 1] == best or errs[int(r.q[0, 1]) + 4] <= errs.min() * (1 + 1e-9), trial
+
+
+# --------------------------------------------------------------------------
+# Degenerate layers
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("sym", [True, False])
+def test_zero_weights_give_zero_error_and_alpha_zero(sym):
+    # every group's range is 0: the step is the 1e-8 floor, every code is the
+    # zero point, the quantized weights are exactly 0 = W
+    X = np.random.default_rng(13).normal(size=(9, 64))
+    r = O.awq_search(np.zeros((4, 64), np.float32), X, bits=4, group=32, grid=6, sym=sym)
+    assert np.all(r.errs == 0.0) and r.best == 0
+    qw, sc, z = O.quantize_pack(np.zeros((4, 64), np.float32), r.s32[0], 4, 32, sym)
+    assert np.all(sc == np.float32(1e-8))
+    u = O.unpack_bits(qw, 4, 64)
+    assert np.all(u == (8 if sym else 0)) and np.all(z == (8 if sym else 0))
+
+
+def test_zero_activations_are_flat_salience():
+    # s_X = 1e-8 for every channel: flat, so every alpha is RTN and alpha 0 wins
+    W = np.random.default_rng(14).normal(0, 0.02, size=(4, 64)).astype(np.float32)
+    r = O.awq_search(W, np.zeros((5, 64)), bits=4, group=32, grid=6, sym=True)
+    assert np.all(r.sx == 1e-8) and r.best == 0
+    assert np.all(r.s32 == np.float32(1.0))
