@@ -119,6 +119,18 @@ class SearchOpts(ctypes.Structure):
                 ("diag", ctypes.c_void_p)]
 
 
+def _env_opts() -> Optional["SearchOpts"]:
+    """Search options from the environment: AWQ_WAIT_LIMIT_MS bounds every
+    device-side wait of the search kernel (the library's default is 2000 ms).
+    None when it is not set."""
+    v = os.environ.get("AWQ_WAIT_LIMIT_MS")
+    if not v:
+        return None
+    o = SearchOpts()
+    o.wait_limit_ns = int(float(v) * 1e6)
+    return o
+
+
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
@@ -196,6 +208,8 @@ def awq_search(W: torch.Tensor, X: torch.Tensor, bits: int = 4, group: Optional[
     args = (_ptr(W), _ptr(X), DTYPE[W.dtype], out, n_in, N, _ptr(sx), bits, g, 1 if sym else 0,
             grid, _ptr(workspace), workspace.numel(), _ptr(err), _ptr(best), _ptr(s_best), _ptr(st),
             _stream(stream))
+    if opts is None:
+        opts = _env_opts()
     if opts is None:
         code = lib.awq_search(*args)
     else:

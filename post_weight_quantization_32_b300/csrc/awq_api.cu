@@ -1,5 +1,9 @@
 // The C ABI of libawq (declared in include/awq.h): argument checks,
 // workspace layout, and the order of launches on the caller's stream.
+// Every entry point is an NVTX range named after it (header-only NVTX: a
+// no-op unless a profiler attaches), so timelines group the launches by call.
+#include <nvtx3/nvToolsExt.h>
+
 #include "awq.h"
 #include "awq_internal.h"
 
@@ -61,6 +65,14 @@ bool dtype_ok(int dt) { return dt == kDtF32 || dt == kDtF16 || dt == kDtBF16; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA; }
 
+// NVTX range for the lifetime of one entry-point call.
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
+
 }  // namespace
 }  // namespace awq
 
@@ -82,6 +94,7 @@ const char* awq_status_string(int status) {
 
 int awq_channel_stats(const void* X, int dtype, int64_t N, int64_t in, double* sx,
                       int32_t* dev_status, awq_stream_t stream) {
+  const Range range("awq_channel_stats");
   (void)dev_status;  // no device-side errors in this kernel
   if (!X || !sx || !dtype_ok(dtype) || N < 1 || in < 1) return AWQ_ERR_INVALID_ARG;
   return cuda_status(
@@ -101,6 +114,7 @@ int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t 
                   const double* sx, int bits, int group, int sym, int grid, void* workspace,
                   size_t workspace_bytes, double* err, int32_t* best, float* s_best,
                   int32_t* dev_status, awq_stream_t stream, const awq_search_opts* opts) {
+  const Range range("awq_search_ex");
   if (!W || !X || !workspace || !err || !best || !s_best || !dtype_ok(dtype))
     return AWQ_ERR_INVALID_ARG;
   if (out < 1 || in < 1 || N < 1 || bits < 2 || bits > 8 || grid < 1 || grid > kMaxGrid ||
@@ -189,6 +203,7 @@ int awq_search(const void* W, const void* X, int dtype, int64_t out, int64_t in,
 int awq_output_power(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
                      void* workspace, size_t workspace_bytes, double* power, int32_t* dev_status,
                      awq_stream_t stream) {
+  const Range range("awq_output_power");
   if (!W || !X || !workspace || !power || !dtype_ok(dtype)) return AWQ_ERR_INVALID_ARG;
   if (out < 1 || in < 1 || N < 1) return AWQ_ERR_INVALID_ARG;
   // the workspace of a one-alpha search with one group per row
@@ -234,6 +249,7 @@ int awq_output_power(const void* W, const void* X, int dtype, int64_t out, int64
 int awq_quantize_pack(const void* W, int dtype, int64_t out, int64_t in, const float* s, int bits,
                       int group, int sym, uint32_t* qweight, float* scales, uint8_t* zeros,
                       int32_t* dev_status, awq_stream_t stream) {
+  const Range range("awq_quantize_pack");
   if (!W || !s || !qweight || !scales || !zeros || !dtype_ok(dtype)) return AWQ_ERR_INVALID_ARG;
   if (out < 1 || in < 1 || bits < 2 || bits > 8 || group < 1 || in % group != 0)
     return AWQ_ERR_INVALID_ARG;
@@ -246,6 +262,7 @@ int awq_quantize_pack_clipped(const void* W, int dtype, int64_t out, int64_t in,
                               int bits, int group, int sym, const float* clip, uint32_t* qweight,
                               float* scales, uint8_t* zeros, int32_t* dev_status,
                               awq_stream_t stream) {
+  const Range range("awq_quantize_pack_clipped");
   if (!W || !s || !clip || !qweight || !scales || !zeros || !dtype_ok(dtype))
     return AWQ_ERR_INVALID_ARG;
   if (out < 1 || in < 1 || bits < 2 || bits > 8 || group < 1 || in % group != 0)
@@ -265,6 +282,7 @@ int awq_clip_search(const void* W, const void* X, int dtype, int64_t out, int64_
                     const float* s, int bits, int group, int sym, int n_grid, int max_shrink_steps,
                     void* workspace, size_t workspace_bytes, float* clip, float* errs,
                     int32_t* dev_status, awq_stream_t stream) {
+  const Range range("awq_clip_search");
   if (!W || !X || !s || !workspace || !clip || !dtype_ok(dtype)) return AWQ_ERR_INVALID_ARG;
   if (out < 1 || in < 1 || N < 1 || bits < 2 || bits > 8 || group < 1 || in % group != 0)
     return AWQ_ERR_INVALID_ARG;
@@ -290,6 +308,7 @@ int awq_gptq(const void* W, const void* X, int dtype, int64_t out, int64_t in, i
              const float* s, int bits, int group, int sym, double damp, void* workspace,
              size_t workspace_bytes, uint32_t* qweight, float* scales, uint8_t* zeros,
              int32_t* dev_status, awq_stream_t stream) {
+  const Range range("awq_gptq");
   if (!W || !X || !workspace || !qweight || !scales || !zeros || !dtype_ok(dtype))
     return AWQ_ERR_INVALID_ARG;
   if (out < 1 || in < 1 || N < 1 || bits < 2 || bits > 8 || group < 1 || in % group != 0 ||
@@ -309,6 +328,7 @@ int awq_export_checkpoint(const uint32_t* qweight, const float* scales, const ui
                           int64_t out, int64_t in, int bits, int group, uint32_t* qweight_t,
                           void* scales_h, uint32_t* qzeros, int32_t* dev_status,
                           awq_stream_t stream) {
+  const Range range("awq_export_checkpoint");
   if (!qweight || !scales || !zeros || !qweight_t || !scales_h || !qzeros)
     return AWQ_ERR_INVALID_ARG;
   if (out < 1 || in < 1 || group < 1 || in % group != 0) return AWQ_ERR_INVALID_ARG;

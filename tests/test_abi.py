@@ -204,3 +204,12 @@ def test_binding_wrappers_pass_one_label_to_the_status_check():
     calls = [n for n in ast.walk(ast.parse(src))
              if isinstance(n, ast.Call) and getattr(n.func, "id", "") == "_check"]
     assert calls and all(len(c.args) == 2 and isinstance(c.args[1], ast.Constant) for c in calls)
+
+
+def test_wait_limit_from_the_environment(monkeypatch):
+    import post_weight_quantization_32_b300 as awq
+    monkeypatch.delenv("AWQ_WAIT_LIMIT_MS", raising=False)
+    assert awq._env_opts() is None
+    monkeypatch.setenv("AWQ_WAIT_LIMIT_MS", "250")
+    o = awq._env_opts()
+    assert o.wait_limit_ns == 250_000_000 and o.test_timeout == 0 and not o.diag
