@@ -1,14 +1,15 @@
 """Parity at the five full-size workloads, in the launch configuration the
 benchmark times (the default persistent grid on all SMs).
 
-The tiny and notebook-shaped layers are checked against the oracle over the
-whole alpha grid.  For the three large layers the oracle evaluates the
-errors one alpha at a time at full size: alpha 0 (plain RTN), the alpha the
-GPU kept and its grid neighbours, which also checks that the kept alpha is a
-minimum of the oracle's errors among those; the final codes are compared
-bit for bit on a sample of rows.  Setting AWQ_FULL_PARITY=1 evaluates every
-alpha of the large layers as well (several minutes of CPU).
+Every alpha of the grid is compared with the oracle on all five layers.  The
+tiny and notebook-shaped layers run the oracle here; for the three large
+layers the oracle's whole-grid errors are stored under tests/golden/ by
+make_config_errs.py (which calls only the oracle and the seeded input
+generator), and this test recomputes the oracle's error at the kept alpha
+live to check that the stored values belong to these inputs.  The final
+codes are compared bit for bit on a sample of rows.
 """
+import json
 import os
 
 import numpy as np
@@ -22,7 +23,7 @@ pytestmark = pytest.mark.gpu
 
 ERR_RTOL = 2e-3
 TIE_RTOL = 1e-3
-FULL = os.environ.get("AWQ_FULL_PARITY", "") == "1"
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
 @pytest.fixture(scope="module")
@@ -68,20 +69,29 @@ def test_small_configs_whole_grid(awq, cfg):
     _check_pack_rows(awq, W, res.s32[b], cfg, np.arange(W.shape[0]))
 
 
+def _golden(cfg):
+    with open(os.path.join(GOLDEN, "config_errs_%s.json" % cfg.name)) as f:
+        rec = json.load(f)
+    assert (rec["seed"], rec["bits"], rec["group"], rec["sym"], rec["grid"]) == \
+        (0, cfg.bits, cfg.group, cfg.sym, cfg.grid)
+    return np.array(rec["errs"], dtype=np.float64), int(rec["best"])
+
+
 @pytest.mark.parametrize("cfg", CONFIGS[2:], ids=lambda c: c.name)
-def test_large_configs_sampled(awq, cfg):
+def test_large_configs_whole_grid(awq, cfg):
     W, X, e, b, sb = _run(awq, cfg)
-    assert np.isfinite(e).all()
-    if FULL:
-        idx = list(range(cfg.n_alpha))
-    else:
-        idx = sorted({0, b, max(b - 1, 0), min(b + 1, cfg.n_alpha - 1)})
-    res = O.awq_search(W.float().numpy(), X.double().numpy(), cfg.bits, cfg.group, cfg.grid, cfg.sym,
-                       alpha_index=set(idx))
-    for k in idx:
-        assert abs(e[k] - res.errs[k]) <= ERR_RTOL * res.errs[k], (k, e[k], res.errs[k])
-    for k in idx:   # the kept alpha is (within the tie tolerance) a minimum of what was evaluated
-        assert res.errs[b] <= res.errs[k] * (1 + TIE_RTOL)
+    errs, obest = _golden(cfg)
+    assert errs.shape == (cfg.n_alpha,) and np.isfinite(e).all()
+    rel = np.abs(e - errs) / errs
+    assert rel.max() <= ERR_RTOL, (int(rel.argmax()), rel.max())
+    # the same alpha, unless the two grid errors are within the tie tolerance
+    if b != obest:
+        assert abs(errs[b] - errs[obest]) <= TIE_RTOL * errs[obest], (b, obest)
+    # the stored errors belong to these inputs: the oracle's error at the kept
+    # alpha, recomputed now
+    Wn, Xn = W.float().numpy(), X.double().numpy()
+    res = O.awq_search(Wn, Xn, cfg.bits, cfg.group, cfg.grid, cfg.sym, alpha_index={b})
+    assert abs(res.errs[b] - errs[b]) <= 1e-9 * errs[b]
     _check_s(sb, res.s32[b])
     rng = np.random.default_rng(0)
     rows = np.sort(rng.choice(W.shape[0], size=64, replace=False))

@@ -480,6 +480,31 @@ def test_clip_search_by_hand_clips_an_outlier():
     assert r.factors[r.best[0, 0]] == np.float32(0.65)
 
 
+def test_asymmetric_clipped_group_by_hand():
+    # one group t = [-1.0, 0.25, 3.0], 2 bits (maxq = 3), factor c = 0.5:
+    #   lo = c * min(min t, 0) = -0.5,  hi = c * max(max t, 0) = 1.5
+    #   step = fl32((hi - lo) / 3) = fl32(2/3),  zero = round(fl32(0.5 / step)) = round(0.74999994) = 1
+    #   codes: -1.0 / step = -1.5 -> -2 + 1 = -1 -> clamped to 0   (either neighbour of the
+    #          tie gives a code <= 0, so the clamp decides)
+    #          0.25 / step = 0.37499998 -> 0 + 1 = 1
+    #          3.0 / step = 4.4999998 -> 4 + 1 = 5 -> clamped to 3
+    #   w_hat = step * (code - zero) = [-step, 0, 2 step]
+    # Shrinking only hi would give step fl32(2.5/3); taking the zero point from
+    # the unclipped lo would give zero 2 and code 2 for 0.25.
+    t = np.array([[-1.0, 0.25, 3.0]], np.float32)
+    g = O.quantize_groups_clipped(t, 2, 3, False, np.array([[0.5]], np.float32))
+    step = np.float32(2.0) / np.float32(3.0)
+    assert g.scale[0, 0] == step and g.zero[0, 0] == 1.0
+    assert g.q.tolist() == [[0.0, 1.0, 3.0]]
+    assert g.w_hat.tolist() == [[float(-step), 0.0, float(np.float32(2) * step)]]
+    # an all-positive group [0.5, 1.0, 2.0] at c = 0.75: lo = c * 0 = 0, hi = 1.5,
+    # step 0.5, zero 0, codes [1, 2, 4 -> 3], w_hat [0.5, 1.0, 1.5]
+    t = np.array([[0.5, 1.0, 2.0]], np.float32)
+    g = O.quantize_groups_clipped(t, 2, 3, False, np.array([[0.75]], np.float32))
+    assert g.scale[0, 0] == np.float32(0.5) and g.zero[0, 0] == 0.0
+    assert g.q.tolist() == [[1.0, 2.0, 3.0]] and g.w_hat.tolist() == [[0.5, 1.0, 1.5]]
+
+
 @pytest.mark.parametrize("sym", [True, False])
 def test_clip_share_of_a_whole_row_group_is_the_row_error(sym):
     # with one group per row the group's share is the row's whole output error
@@ -543,6 +568,33 @@ def test_gptq_second_column_is_the_best_code_given_the_first():
         best = int(np.argmin(errs)) - 4
         # the kept code is the best one, unless two codes are within rounding of a tie
         assert r.q[0, 1] == best or errs[int(r.q[0, 1]) + 4] <= errs.min() * (1 + 1e-9), trial
+
+
+def test_gptq_fits_each_group_on_the_corrected_weights():
+    # "fit on already-corrected weights" ("AWQ vs GPTQ ...", "GPTQ: compensate
+    # the error you just made").  Choose the factor first:
+    #       U = [[1, 0, 2, -1], [0, 1, 6, -8], [0, 0, 1, 1], [0, 0, 0, 1]]
+    # and X = U^-T (4 tokens), so H = 2 X^T X = 2 U^-1 U^-T, H^-1 = U^T U / 2
+    # and the oracle's factor is U / sqrt(2) (damp 0).  The update of column j
+    # by column i uses U[i, j] / U[i, i], in which sqrt(2) cancels.
+    # One row w = [-3, 1.25, 1, 0.25], 3-bit symmetric (L = 3), group 2:
+    #   group 0 at column 0: step max(3, 1.25) / 3 = 1
+    #   column 0: -3 -> code -3, error 0 (nothing passed on)
+    #   column 1: 1.25 -> code 1, error 0.25: column 2 -= 0.25 * 6 -> -0.5,
+    #             column 3 -= 0.25 * (-8) -> 2.25
+    #   group 1 at column 2, fitted on [-0.5, 2.25]: step 2.25 / 3 = 0.75
+    #             (fitted on the original [1, 0.25] it would be 1/3)
+    #   column 2: -0.5 / 0.75 = -0.667 -> code -1, w_hat -0.75, error 0.25:
+    #             column 3 -= 0.25 * 1 -> 2.0
+    #   column 3: 2.0 / 0.75 = 2.667 -> code 3, w_hat 2.25
+    U = np.array([[1, 0, 2, -1], [0, 1, 6, -8], [0, 0, 1, 1], [0, 0, 0, 1]], np.float64)
+    X = np.linalg.inv(U).T
+    W = np.array([[-3.0, 1.25, 1.0, 0.25]], np.float32)
+    r = O.gptq(W, X, 3, 2, True, damp=0.0)
+    assert r.scale.tolist() == [[1.0, 0.75]]
+    assert r.q.tolist() == [[-3.0, 1.0, -1.0, 3.0]]
+    assert r.w_hat.tolist() == [[-3.0, 1.0, -0.75, 2.25]]
+    assert np.allclose(O.inverse_hessian_factor(X, 0.0) * np.sqrt(2.0), U, rtol=0, atol=1e-12)
 
 
 # --------------------------------------------------------------------------
