@@ -16,7 +16,8 @@ every rank searches its own layer (different seed): weak scaling, no
 collective on the data path; the time is the max over ranks.
 
 --impl reference times the CPU oracle (float64 numpy, the pages' algorithm
-as written) on the same layer, each step a bounded sample of the grid.
+as written) on the same layer, each step the whole grid on the tiny and
+notebook-shaped layers (a two-alpha sample on the larger ones).
 """
 from __future__ import annotations
 
@@ -40,11 +41,39 @@ from synthetic import CONFIGS, config_by_name, make_layer  # noqa: E402
 DEFAULT_CONFIG = "nb-4096x4096-n256"
 METRIC = "AWQ search layer-alpha-evals/sec"
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one search-kernel
-# launch, from an ncu capture of this kernel build on that workload; None where
-# no capture of the current kernel exists.  A value far above W + X (each read
-# once) would mean wasted re-reads.
-SEARCH_TRAFFIC_BYTES = {"nb-4096x4096-n256": 36_407_808 + 3_328}
+# The search kernel's DRAM bytes per launch (dram__bytes_read.sum +
+# dram__bytes_write.sum) come from ncu captures summarised under profiles/,
+# one "traffic-record:" line per capture, stamped with a hash of the kernel's
+# sources.  A record counts only while those sources are unchanged; otherwise
+# the line reports null.  Traffic far above W + X (each read once) would mean
+# wasted re-reads.
+SEARCH_SOURCES = ("post_weight_quantization_32_b300/csrc/awq_search.cu",
+                  "post_weight_quantization_32_b300/csrc/awq_device.cuh")
+
+
+def search_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in SEARCH_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def search_traffic(workload):
+    """DRAM bytes of one search-kernel launch on `workload` from a profiles/
+    record of the current kernel sources, else None."""
+    import glob
+    import re
+    want = search_source_hash()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(path) as f:
+            for line in f:
+                m = re.search(r"traffic-record: workload=(\S+) dram_bytes=(\d+) sources-sha256=([0-9a-f]+)",
+                              line)
+                if m and m.group(1) == workload and m.group(3) == want:
+                    return int(m.group(2))
+    return None
 
 
 def _peaks():
@@ -228,14 +257,41 @@ def run_ours(args, cfg, rank, world, dist):
 
 
 def run_oracle_sample(cfg, n_sample, seed=0):
-    """Oracle time for n_sample alphas of the grid (spread over it), seconds."""
+    """Oracle wall time for n_sample alphas of the grid (spread over it; the
+    whole grid when n_sample >= n_alpha), seconds, and the number of alphas.
+    The oracle computes the statistics and the reference output X W^T once
+    per call, as the pages' loop does, so a whole-grid call amortises them
+    over every alpha and a sample does not."""
     from oracle import awq_oracle as O
     W, X = make_layer(cfg, seed=seed)
     Wn, Xn = W.float().numpy(), X.double().numpy()
-    idx = set(np.linspace(0, cfg.n_alpha - 1, n_sample).round().astype(int).tolist())
+    if n_sample >= cfg.n_alpha:
+        idx = None
+        n = cfg.n_alpha
+    else:
+        idx = set(np.linspace(0, cfg.n_alpha - 1, n_sample).round().astype(int).tolist())
+        n = len(idx)
     t0 = time.perf_counter()
     O.awq_search(Wn, Xn, cfg.bits, cfg.group, cfg.grid, cfg.sym, alpha_index=idx)
-    return time.perf_counter() - t0, len(idx)
+    return time.perf_counter() - t0, n
+
+
+def oracle_sample_size(cfg, requested):
+    """Alphas in the oracle's timed sample: the requested count, else the
+    whole grid where the oracle finishes it in seconds (the tiny and
+    notebook-shaped layers), else two alphas."""
+    if requested > 0:
+        return requested
+    return cfg.n_alpha if cfg.out * cfg.in_ * cfg.N <= 4096 * 4096 * 256 else 2
+
+
+def oracle_sample_text(cfg, n):
+    if n >= cfg.n_alpha:
+        return ("the whole %d-alpha grid of the same layer in one oracle call (statistics and "
+                "the reference output X W^T computed once, as the pages' loop does)" % cfg.n_alpha)
+    return ("%d alphas of the %d-alpha grid of the same layer in one oracle call (statistics "
+            "and the reference output X W^T computed once for the sample, so not amortised "
+            "over the grid)" % (n, cfg.n_alpha))
 
 
 def _cores():
@@ -252,7 +308,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=[c.name for c in CONFIGS])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-sample", type=int, default=2, help="alphas in the oracle's timed sample")
+    ap.add_argument("--cpu-sample", type=int, default=0,
+                    help="alphas in the oracle's timed sample (0: the whole grid on the tiny and "
+                         "notebook-shaped layers, two alphas on the larger ones)")
     ap.add_argument("--next-rows", action="store_true",
                     help="also time the clipping search, output power, wide-group searches, GPTQ "
                          "after AWQ and the checkpoint export on the same layer (one extra JSON "
@@ -270,10 +328,11 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
+        n_s = oracle_sample_size(cfg, args.cpu_sample)
         times = []
-        n = 1
+        n = n_s
         for i in range(args.warmup + args.steps):
-            t, n = run_oracle_sample(cfg, 1)
+            t, n = run_oracle_sample(cfg, n_s)
             if i >= args.warmup:
                 times.append(t)
         t = sum(times) / len(times)
@@ -283,8 +342,7 @@ def main():
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": conf,
                 "cpu_baseline": {"value": v, "unit": "layer-alpha-evals/s", "cores": _cores(),
-                                 "kind": "oracle",
-                                 "sample": "one alpha of the grid per step (incl. the reference GEMM X W^T)"},
+                                 "kind": "oracle", "sample": "each step: " + oracle_sample_text(cfg, n)},
                 "e2e": {"value": v, "unit": "layer-alpha-evals/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -297,7 +355,7 @@ def main():
     value = job_throughput(n_alpha, world, r["ms"])
     e2e_v = job_throughput(n_alpha, world, r["e2e_ms"])
     achieved = flops / (r["search_ms"] * 1e-3) / 1e12
-    cpu_t, cpu_n = run_oracle_sample(cfg, args.cpu_sample)
+    cpu_t, cpu_n = run_oracle_sample(cfg, oracle_sample_size(cfg, args.cpu_sample))
     # statistics (with max|W| and the centring), alpha table, search, argmin, pack;
     # a bf16 or fp32 X adds its fp16 copy
     launches_per_step = 5 + (0 if cfg.dtype == "f16" else 1)
@@ -309,11 +367,11 @@ def main():
         "gflops": flops / (r["ms"] * 1e-3) / 1e9,
         "search_kernel_ms": r["search_ms"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
-                     "frac": achieved / tflops_peak, "traffic": SEARCH_TRAFFIC_BYTES.get(cfg.name),
+                     "frac": achieved / tflops_peak, "traffic": search_traffic(cfg.name),
                      "kernel": "awq_search_kernel", "peak_kind": peak_kind + " (bf16 dense = fp16 dense)"},
         "cpu_baseline": {"value": cpu_n / cpu_t, "unit": "layer-alpha-evals/s", "cores": _cores(),
                          "kind": "oracle",
-                         "sample": "%d alphas of the grid on the same layer (incl. the reference GEMM)" % cpu_n},
+                         "sample": oracle_sample_text(cfg, cpu_n)},
         "e2e": {"value": e2e_v, "unit": "layer-alpha-evals/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": launches_per_step * args.steps,
