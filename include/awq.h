@@ -79,11 +79,24 @@ int awq_channel_stats(const void* X, int dtype, int64_t N, int64_t in,
                       double* sx, int32_t* dev_status, awq_stream_t stream);
 
 /*
- * Bytes of device workspace awq_search needs for these sizes (0 on invalid
- * sizes).  The workspace must be 256-byte aligned.
+ * Bytes of device workspace for awq_search's fastest path at these sizes (0
+ * on invalid sizes).  The workspace must be 256-byte aligned.  Where the
+ * problem allows it (more than 128 tokens, group 32, 64 or 128, fp16 or
+ * bf16, and (grid + 1) * N * in * 2 <= 64 MiB) this includes room for
+ * grid + 1 fp16 copies of X / s, which the search then reads instead of
+ * dividing every weight change by s.
  */
 size_t awq_search_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N,
                                   int group, int grid);
+
+/*
+ * The smallest workspace awq_search accepts for these sizes (0 on invalid
+ * sizes): without the copies of X / s.  A workspace between this and
+ * awq_search_workspace_bytes gives the same results within the search's
+ * tolerance, by the other path.
+ */
+size_t awq_search_workspace_min_bytes(int dtype, int64_t out, int64_t in, int64_t N,
+                                      int group, int grid);
 
 /*
  * awq_search - the alpha-grid scale search.
@@ -108,7 +121,8 @@ size_t awq_search_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N,
  *             zero = round(-min/scale), codes in [0, 2^b - 1]
  *             ["AWQ vs GPTQ ...", "The shared problem: one layer, sixteen levels"]
  *   grid   1..4096; the search tries the grid + 1 alphas k/grid, k = 0..grid
- *   workspace, workspace_bytes  >= awq_search_workspace_bytes(...)
+ *   workspace, workspace_bytes  >= awq_search_workspace_min_bytes(...);
+ *          with >= awq_search_workspace_bytes(...) the faster path runs
  *   err    [grid + 1] double      (written) mean((X (Wq - W)^T)^2) per alpha
  *   best   [1] int32              (written) index of the kept alpha; -1 and
  *                                 AWQ_ERR_NONFINITE in *dev_status if every
@@ -119,7 +133,9 @@ size_t awq_search_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N,
  * The error is formed as X (Wq - W)^T, which equals the pages' X Wq^T - X W^T;
  * the GEMM runs on the tensor cores with fp16 operands (X and the weight
  * change each scaled by an exact power of two chosen from max|X| and max|W|)
- * and fp32 accumulation, the per-alpha sum in float64.  Rows, tokens and
+ * and fp32 accumulation, the per-alpha sum in float64.  On the faster path
+ * the same sum is formed as (X / s)(W^ s - W s)^T, with X / s rounded to
+ * fp16 once per alpha.  Rows, tokens and
  * alphas are summed in a fixed order: repeated calls give bit-identical
  * results.  Shared-input layer groups (q/k/v) are searched by passing their
  * weights concatenated along `out` with the common X: one s, one error.
@@ -334,7 +350,7 @@ int awq_export_checkpoint(const uint32_t* qweight, const float* scales, const ui
  * cudaMalloc, cudaFree or other allocating call.
  *
  * Arguments, outputs, numerics and errors are those of awq_search, except:
- *  - the sizes must satisfy awq_search_workspace_bytes(dtype, out, in, N,
+ *  - the sizes must satisfy awq_search_workspace_min_bytes(dtype, out, in, N,
  *    group, grid) <= AWQ_NOALLOC_SCRATCH_BYTES; larger problems return
  *    AWQ_ERR_UNSUPPORTED before anything is enqueued (use awq_search with
  *    your own workspace for those);

@@ -39,7 +39,8 @@ import torch
 
 __all__ = [
     "AWQError", "SearchOpts", "lib", "awq_channel_stats", "awq_search",
-    "awq_search_workspace_bytes", "awq_quantize_pack", "new_status", "check_status", "STATUS",
+    "awq_search_workspace_bytes", "awq_search_workspace_min_bytes", "awq_quantize_pack",
+    "new_status", "check_status", "STATUS",
     "DTYPE", "awq_search_noalloc", "NOALLOC_SCRATCH_BYTES", "awq_output_power", "awq_sweep",
     "awq_export_checkpoint", "awq_clip_search", "awq_clip_search_workspace_bytes",
     "awq_quantize_pack_clipped", "awq_gptq", "awq_gptq_workspace_bytes",
@@ -52,7 +53,8 @@ DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 STATUS = {0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARG", 2: "AWQ_ERR_UNSUPPORTED", 3: "AWQ_ERR_NONFINITE",
           4: "AWQ_ERR_TIMEOUT", 5: "AWQ_ERR_CUDA"}
 
-EXPORTS = ("awq_status_string", "awq_channel_stats", "awq_search_workspace_bytes", "awq_search",
+EXPORTS = ("awq_status_string", "awq_channel_stats", "awq_search_workspace_bytes",
+           "awq_search_workspace_min_bytes", "awq_search",
            "awq_search_ex", "awq_quantize_pack", "awq_search_noalloc", "awq_output_power",
            "awq_export_checkpoint", "awq_clip_search", "awq_clip_search_workspace_bytes",
            "awq_quantize_pack_clipped", "awq_gptq", "awq_gptq_workspace_bytes")
@@ -72,6 +74,8 @@ def _load() -> ctypes.CDLL:
     L.awq_channel_stats.argtypes = [vp, i32, i64, i64, vp, vp, vp]
     L.awq_search_workspace_bytes.restype = sz
     L.awq_search_workspace_bytes.argtypes = [i32, i64, i64, i64, i32, i32]
+    L.awq_search_workspace_min_bytes.restype = sz
+    L.awq_search_workspace_min_bytes.argtypes = [i32, i64, i64, i64, i32, i32]
     L.awq_search.restype = i32
     L.awq_search.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, i32, vp, sz, vp, vp, vp,
                              vp, vp]
@@ -175,7 +179,14 @@ def awq_channel_stats(X: torch.Tensor, sx: Optional[torch.Tensor] = None, stream
 
 def awq_search_workspace_bytes(dtype: torch.dtype, out: int, n_in: int, N: int, group: int,
                                grid: int) -> int:
+    """Workspace bytes for the search's fastest path (see the C header)."""
     return int(lib.awq_search_workspace_bytes(DTYPE[dtype], out, n_in, N, group, grid))
+
+
+def awq_search_workspace_min_bytes(dtype: torch.dtype, out: int, n_in: int, N: int, group: int,
+                                   grid: int) -> int:
+    """The smallest workspace the search accepts."""
+    return int(lib.awq_search_workspace_min_bytes(DTYPE[dtype], out, n_in, N, group, grid))
 
 
 def awq_search(W: torch.Tensor, X: torch.Tensor, bits: int = 4, group: Optional[int] = None,

@@ -72,9 +72,10 @@ __device__ __forceinline__ double pow_int(double r, int k) {
 // max|W| * max(s) / min(s) bounds |dW| for the whole alpha; its
 // power-of-two exponent sets e_k (folded into the 1/s table), and
 // unscale[k] = 2^-2(e_k + m_x) undoes both operand scalings on the squared
-// sums.  pow2_s[k] starts at 1 here.  Threads stride over the alphas; only
+// sums (the pre-divided mode scales the weights and X / s separately, see
+// CentreArgs).  pow2_s[k] starts at 1 here.  Threads stride over the alphas; only
 // products and one reciprocal square root per alpha, no logarithms.
-__device__ __forceinline__ void alpha_centre(const SxExt& x, float wmax, int m_x,
+__device__ __forceinline__ void alpha_centre(const SxExt& x, float wmax, float xmax, int m_x,
                                              const CentreArgs& ca) {
   const int grid = ca.grid;
   for (int k = threadIdx.x; k <= grid; k += blockDim.x) {
@@ -91,9 +92,20 @@ __device__ __forceinline__ void alpha_centre(const SxExt& x, float wmax, int m_x
     const double ic = k == 0 ? 1.0 : rsqrt(smax * smin);
     ca.inv_c[k] = ic;
     const double q = smax * ic;  // sqrt(max / min)
-    const int e = pow2_exponent_for((double)wmax * (q * q));
-    ca.escale[k] = ldexpf(1.0f, e);
-    ca.unscale[k] = ldexp(1.0, -2 * (e + m_x));
+    if (ca.xs) {
+      // pre-divided mode: the weights' rounding errors are at most
+      // max|W| * max(s) = max|W| * q, and |X / s| at most max|X| / min(s) =
+      // max|X| * q
+      const int e = pow2_exponent_for((double)wmax * q);
+      const int m = pow2_exponent_for((double)xmax * q);
+      ca.escale[k] = ldexpf(1.0f, e);
+      ca.xscale[k] = ldexpf(1.0f, m);
+      ca.unscale[k] = ldexp(1.0, -2 * (e + m));
+    } else {
+      const int e = pow2_exponent_for((double)wmax * (q * q));
+      ca.escale[k] = ldexpf(1.0f, e);
+      ca.unscale[k] = ldexp(1.0, -2 * (e + m_x));
+    }
     ca.pow2_s[k] = 1;
   }
 }
@@ -127,9 +139,9 @@ __device__ __forceinline__ void centre_if_last(const CentreArgs& ca, unsigned nc
   x = sext[0];
   for (unsigned w = 1; w < (blockDim.x + 31) / 32; ++w) x.merge(sext[w]);
   const float wmax = __uint_as_float(__ldcg(ca.absmax));
-  const int m_x = ca.x_scaled ? pow2_exponent_for((double)__uint_as_float(__ldcg(ca.absmax + 1)))
-                              : 0;
-  alpha_centre(x, wmax, m_x, ca);
+  const float xmax = __uint_as_float(__ldcg(ca.absmax + 1));
+  const int m_x = ca.x_scaled ? pow2_exponent_for((double)xmax) : 0;
+  alpha_centre(x, wmax, xmax, m_x, ca);
 }
 
 }  // namespace awq

@@ -28,11 +28,14 @@ constexpr int kMaxGrid = 4096;
 
 // Byte offsets of the workspace regions of awq_search (each 256-aligned).
 struct WsLayout {
-  size_t ctl, pow2, unscale, escale, inv_c, sx64, root, minmax, s32, inv_s32, xf16, gext,
-      gext_bytes, partials, total;
+  size_t ctl, pow2, unscale, escale, xscale, inv_c, sx64, root, minmax, s32, inv_s32, ss32, xf16,
+      gext, gext_bytes, partials, total;
 };
 
-WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int group, int grid) {
+// xs: the pre-divided search (search_xs_eligible), which adds the scaled s
+// table and the n_alpha copies of X / s and needs no fp16 copy of X.
+WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int group, int grid,
+                   bool xs = false) {
   WsLayout w{};
   const int64_t n_alpha = grid + 1;
   const int64_t n_tiles = ((out + 127) / 128) * ((N + 255) / 256);
@@ -46,13 +49,16 @@ WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int group, int gr
   w.pow2 = take((size_t)n_alpha * 4);
   w.unscale = take((size_t)n_alpha * 8);
   w.escale = take((size_t)n_alpha * 4);
+  w.xscale = take((size_t)n_alpha * 4);
   w.inv_c = take((size_t)n_alpha * 8);
   w.sx64 = take((size_t)in * 8);
   w.root = take((size_t)in * 8);                   // s_X ^ (1 / grid)
   w.minmax = take(prep_chunks(in) * 32);           // per-chunk extremes of s_X with their roots
   w.s32 = take((size_t)n_alpha * in * 4);
   w.inv_s32 = take((size_t)n_alpha * in * 4);
-  w.xf16 = take(dt == kDtF16 ? 0 : (size_t)N * in * 2);  // fp16 copy of a bf16/fp32 X
+  w.ss32 = take(xs ? (size_t)n_alpha * in * 4 : 0);
+  // fp16 copy of a bf16/fp32 X, or the n_alpha copies of X / s
+  w.xf16 = take(xs ? (size_t)n_alpha * N * in * 2 : (dt == kDtF16 ? 0 : (size_t)N * in * 2));
   // extremes of groups wider than a producer job: two floats per (alpha, row, group)
   w.gext_bytes = search_wide_group(group, in) ? (size_t)n_alpha * out * (in / group) * 8 : 0;
   w.gext = take(w.gext_bytes);
@@ -74,6 +80,15 @@ struct Range {
 };
 
 }  // namespace
+
+size_t search_workspace_min_bytes(int dtype, int64_t out, int64_t in, int64_t N, int group,
+                                  int grid) {
+  if (!dtype_ok(dtype) || out < 1 || in < 1 || N < 1 || grid < 1 || grid > kMaxGrid ||
+      group < 1 || in % group != 0)
+    return 0;
+  return ws_layout(dtype, out, in, N, group, grid).total;
+}
+
 }  // namespace awq
 
 using namespace awq;
@@ -107,7 +122,13 @@ size_t awq_search_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N,
   if (!dtype_ok(dtype) || out < 1 || in < 1 || N < 1 || grid < 1 || grid > kMaxGrid ||
       group < 1 || in % group != 0)
     return 0;
-  return ws_layout(dtype, out, in, N, group, grid).total;
+  return ws_layout(dtype, out, in, N, group, grid,
+                   search_xs_eligible(dtype, in, N, group, grid)).total;
+}
+
+size_t awq_search_workspace_min_bytes(int dtype, int64_t out, int64_t in, int64_t N, int group,
+                                      int grid) {
+  return search_workspace_min_bytes(dtype, out, in, N, group, grid);
 }
 
 int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
@@ -120,7 +141,10 @@ int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t 
   if (out < 1 || in < 1 || N < 1 || bits < 2 || bits > 8 || grid < 1 || grid > kMaxGrid ||
       group < 1 || in % group != 0)
     return AWQ_ERR_INVALID_ARG;
-  const WsLayout ws = ws_layout(dtype, out, in, N, group, grid);
+  // the pre-divided search where it applies and the workspace has room for it
+  const bool xs = search_xs_eligible(dtype, in, N, group, grid) &&
+                  workspace_bytes >= ws_layout(dtype, out, in, N, group, grid, true).total;
+  const WsLayout ws = ws_layout(dtype, out, in, N, group, grid, xs);
   if (workspace_bytes < ws.total || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
     return AWQ_ERR_INVALID_ARG;
   if (!search_supported(dtype, out, in, N, bits, group, grid)) return AWQ_ERR_UNSUPPORTED;
@@ -143,10 +167,14 @@ int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t 
   float* s32 = reinterpret_cast<float*>(wsb + ws.s32);
   float* inv_s32 = reinterpret_cast<float*>(wsb + ws.inv_s32);
   double* unscale = reinterpret_cast<double*>(wsb + ws.unscale);
-  const bool x_copy = dtype != kDtF16;
+  const bool x_copy = dtype != kDtF16 && !xs;
+  const bool need_xmax = x_copy || xs;
+  float* ss32 = xs ? reinterpret_cast<float*>(wsb + ws.ss32) : nullptr;
   CentreArgs ca{};
   ca.grid = grid;
   ca.x_scaled = x_copy ? 1 : 0;
+  ca.xs = xs ? 1 : 0;
+  ca.xscale = reinterpret_cast<float*>(wsb + ws.xscale);
   ca.root = reinterpret_cast<double*>(wsb + ws.root);
   ca.minmax = reinterpret_cast<double*>(wsb + ws.minmax);
   ca.ticket = absmax + 2;
@@ -155,33 +183,40 @@ int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t 
   ca.escale = reinterpret_cast<float*>(wsb + ws.escale);
   ca.unscale = unscale;
   ca.pow2_s = pow2_s;
-  // One launch: channel statistics, max|W| (and max|X| for a bf16 or fp32
-  // X), sx^(1/grid) and, in its last CTA, the per-alpha centring values.
-  // Then a bf16 / fp32 X is copied to fp16 (scaled by a power of two) for
-  // the tensor cores.
+  // One launch: channel statistics, max|W| (and max|X| when it sets a
+  // scaling), sx^(1/grid) and, in its last CTA, the per-alpha centring
+  // values.  Then either a bf16 / fp32 X is copied to fp16 (scaled by a
+  // power of two) for the tensor cores, or, in the pre-divided mode, the
+  // n_alpha fp16 copies of X / s are formed after the tables.
   const double* sxp = sx;
   if (!sxp) {
     e = launch_channel_stats(X, dtype, N, in, reinterpret_cast<double*>(wsb + ws.sx64),
-                             x_copy ? absmax + 1 : nullptr, W, out * in, absmax, ca, s);
+                             need_xmax ? absmax + 1 : nullptr, W, out * in, absmax, ca, s);
     sxp = reinterpret_cast<const double*>(wsb + ws.sx64);
   } else {
     e = launch_absmax(W, dtype, out * in, absmax, s);
-    if (e == cudaSuccess && x_copy) e = launch_absmax(X, dtype, N * in, absmax + 1, s);
+    if (e == cudaSuccess && need_xmax) e = launch_absmax(X, dtype, N * in, absmax + 1, s);
     if (e == cudaSuccess) e = launch_alpha_root(sxp, in, ca, s);
   }
   if (e == cudaSuccess && x_copy) e = launch_to_f16(X, dtype, N * in, absmax + 1, wsb + ws.xf16, s);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess && xs) {
+    e = launch_alpha_table_xs(sxp, ca.root, ca.inv_c, ca.escale, ca.xscale, in, grid, s32, inv_s32,
+                              ss32, pow2_s, s);
+    if (e == cudaSuccess) e = launch_x_over_s(X, dtype, N, in, n_alpha, inv_s32, wsb + ws.xf16, s);
+  } else if (e == cudaSuccess) {
     e = launch_alpha_table(sxp, ca.root, ca.inv_c, ca.escale, in, grid, s32, inv_s32, pow2_s, s);
+  }
   if (e == cudaSuccess && gext)
     e = launch_group_extremes(W, dtype, out, in, s32, n_alpha, group, sym, gext, s);
   if (e != cudaSuccess) return AWQ_ERR_CUDA;
-  const void* xh = x_copy ? static_cast<const void*>(wsb + ws.xf16) : X;
+  const void* xh = (x_copy || xs) ? static_cast<const void*>(wsb + ws.xf16) : X;
 
   const SearchPlan pl =
-      plan_search(dtype, out, in, N, n_alpha, group, gext != nullptr, device_sm_count());
+      plan_search(dtype, out, in, N, n_alpha, group, gext != nullptr, device_sm_count(), xs);
   double* partials = reinterpret_cast<double*>(wsb + ws.partials);
   e = launch_search(W, xh, dtype, out, in, N, bits, group, sym ? 1 : 0, n_alpha, s32, inv_s32,
-                    pow2_s, gext, partials, pl, opts ? opts->wait_limit_ns : 0,
+                    pow2_s, gext, ss32, xs ? ca.escale : nullptr, partials, pl,
+                    opts ? opts->wait_limit_ns : 0,
                     opts ? opts->test_timeout : 0, dev_status, diag, s,
                     opts ? (cudaEvent_t)opts->ev_search_start : nullptr,
                     opts ? (cudaEvent_t)opts->ev_search_stop : nullptr);
@@ -235,8 +270,8 @@ int awq_output_power(const void* W, const void* X, int dtype, int64_t out, int64
   const void* xh = x_copy ? static_cast<const void*>(wsb + ws.xf16) : X;
   const SearchPlan pl = plan_search(dtype, out, in, N, 1, (int)in, true, device_sm_count());
   double* partials = reinterpret_cast<double*>(wsb + ws.partials);
-  e = launch_search(W, xh, dtype, out, in, N, 4, (int)in, 1, 1, s32, inv_s32, pow2_s, ext,
-                    partials, pl, 0, 0, dev_status, ctl + 4, s, nullptr, nullptr);
+  e = launch_search(W, xh, dtype, out, in, N, 4, (int)in, 1, 1, s32, inv_s32, pow2_s, ext, nullptr,
+                    nullptr, partials, pl, 0, 0, dev_status, ctl + 4, s, nullptr, nullptr);
   if (e == cudaErrorInvalidValue) return AWQ_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return AWQ_ERR_CUDA;
   // the reduction's argmin and kept-scale outputs land in scratch words

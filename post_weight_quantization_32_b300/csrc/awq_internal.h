@@ -42,9 +42,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // zeroed counter; absmax = {max|W|, max|X|} as float bits (max|X| is used
 // when x_scaled, i.e. X is copied to fp16 with a power-of-two scaling);
 // inv_c, escale, unscale, pow2_s have grid + 1 entries.
+// With xs != 0 (the pre-divided search mode) the fp16 scalings are split:
+// escale[k] = 2^e_k scales the weights (t = w * s * 2^e_k), xscale[k] =
+// 2^m_k scales X / s, unscale[k] = 2^-2(e_k + m_k), and absmax[1] must hold
+// max|X| whatever X's dtype.
 struct CentreArgs {
   int grid;
   int x_scaled;
+  int xs;
+  float* xscale;
   double* root;
   double* minmax;
   uint32_t* ticket;
@@ -56,7 +62,7 @@ struct CentreArgs {
 };
 
 // sx[j] = sum_n |X[n, j]| / N + 1e-8, float64.  With xmax != nullptr the same
-// pass folds max|X| into *xmax, and with W != nullptr the same launch folds
+// pass folds max|X| into *xmax (any dtype), and with W != nullptr the same launch folds
 // max|W| (nW values) into *wmax (bits of non-negative floats; both words must
 // start at 0; needs in % 8 == 0, nW % 8 == 0 and 16-byte aligned X and W).
 // With ca.grid != 0 the launch also writes ca.root and, once every CTA is
@@ -85,6 +91,18 @@ cudaError_t launch_alpha_root(const double* sx, int64_t in, const CentreArgs& ca
 cudaError_t launch_alpha_table(const double* sx, const double* root, const double* inv_c,
                                const float* escale, int64_t in, int grid, float* s32,
                                float* inv_s32, int32_t* pow2_s, cudaStream_t s);
+// The pre-divided mode's tables: as launch_alpha_table, but inv_s32[k][j] =
+// xscale[k] / s32[k][j] (the factor X is multiplied by) and ss32[k][j] =
+// s32[k][j] * escale[k] (exact: a power of two).
+cudaError_t launch_alpha_table_xs(const double* sx, const double* root, const double* inv_c,
+                                  const float* escale, const float* xscale, int64_t in, int grid,
+                                  float* s32, float* inv_s32, float* ss32, int32_t* pow2_s,
+                                  cudaStream_t s);
+// xs[k][n][j] = fp16(X[n][j] * xinv[k][j]) for k < n_alpha (X of dtype dt,
+// in % 8 == 0, 16-byte aligned): the n_alpha copies of X / s the pre-divided
+// search reads.
+cudaError_t launch_x_over_s(const void* X, int dt, int64_t N, int64_t in, int n_alpha,
+                            const float* xinv, void* xs, cudaStream_t s);
 // Tables for the output power mean((X W^T)^2) run as a one-alpha search:
 // s32 = 1, inv_s32 = 2^e with e from max|W| (absmax[0]), pow2_s[0] = 1,
 // unscale[0] = 2^-2(e + m_x) (m_x from absmax[1] when x_scaled), and a
@@ -120,17 +138,30 @@ struct SearchPlan {
 // job), or one group per row (group == in, any width).  Needs in % 8 == 0.
 bool search_wide_group(int64_t group, int64_t in);
 bool search_supported(int dt, int64_t out, int64_t in, int64_t N, int bits, int group, int grid);
-// gp: the group extremes come precomputed (launch_search with gext).
+// Whether the search may read X already divided by s (launch_search with
+// ss32): one alpha per work unit, group 32, 64 or 128, 16-bit W, and the
+// n_alpha fp16 copies of X / s small enough to stay in L2.
+bool search_xs_eligible(int dt, int64_t in, int64_t N, int group, int grid);
+// The smallest workspace awq_search accepts (without the pre-divided mode's
+// regions); awq_search_workspace_bytes may return more.
+size_t search_workspace_min_bytes(int dtype, int64_t out, int64_t in, int64_t N, int group,
+                                  int grid);
+// gp: the group extremes come precomputed (launch_search with gext); xs: X
+// arrives divided by s (launch_search with ss32).
 SearchPlan plan_search(int dt, int64_t out, int64_t in, int64_t N, int n_alpha, int group,
-                       bool gp, int sms);
+                       bool gp, int sms, bool xs = false);
 // With gext != nullptr the group extremes are read from gext (layout of
 // launch_group_extremes) instead of being formed per job; group must then be
 // in or a multiple of 128 (and must be when search_wide_group holds).
+// With ss32 != nullptr (the pre-divided mode, see search_xs_eligible):
+// Xf16 holds the n_alpha copies X * 2^m_k / s_k ([n_alpha][N][in] fp16),
+// ss32 the table s_k * 2^e_k ([n_alpha][in]) that the weights are scaled
+// by, escale[k] = 2^e_k; inv_s32 is not read.
 cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, int64_t in,
                           int64_t N, int bits, int group, int sym, int n_alpha,
                           const float* s32, const float* inv_s32, const int32_t* pow2_s,
-                          const float* gext, double* partials, const SearchPlan& plan,
-                          int64_t wait_limit_ns,
+                          const float* gext, const float* ss32, const float* escale,
+                          double* partials, const SearchPlan& plan, int64_t wait_limit_ns,
                           int test_timeout, int32_t* dev_status, uint32_t* diag, cudaStream_t s,
                           cudaEvent_t ev0, cudaEvent_t ev1);
 

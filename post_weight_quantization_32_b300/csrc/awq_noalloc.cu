@@ -49,7 +49,7 @@ extern "C" int awq_search_noalloc(const void* W, const void* X, int dtype, int64
                                   int64_t in, int64_t N, const double* sx, int bits, int group,
                                   int sym, int grid, double* err, int32_t* best, float* s_best,
                                   int32_t* dev_status, awq_stream_t stream) {
-  const size_t need = awq_search_workspace_bytes(dtype, out, in, N, group, grid);
+  const size_t need = awq_search_workspace_min_bytes(dtype, out, in, N, group, grid);
   if (need == 0) return AWQ_ERR_INVALID_ARG;               // sizes the search rejects anyway
   if (need > AWQ_NOALLOC_SCRATCH_BYTES) return AWQ_ERR_UNSUPPORTED;  // beyond the fixed array
   cudaError_t e = cudaSuccess;

@@ -66,10 +66,14 @@ __global__ void __launch_bounds__(kPrepChunk) alpha_root_kernel(const double* __
 // alpha in shared memory, applied once per alpha at the end).
 constexpr int kTabCols = 32, kTabSlices = 4;
 
+//
+// With ss32 != nullptr (the pre-divided search): inv_s32[k][j] = xscale[k] /
+// s32 (the factor X is multiplied by) and ss32[k][j] = s32 * escale[k].
 __global__ void __launch_bounds__(kTabCols * kTabSlices) alpha_table_kernel(
     const double* __restrict__ sx, const double* __restrict__ root,
-    const double* __restrict__ inv_c, const float* __restrict__ escale, int64_t in, int grid,
-    float* __restrict__ s32, float* __restrict__ inv_s32, int32_t* __restrict__ pow2_s) {
+    const double* __restrict__ inv_c, const float* __restrict__ escale,
+    const float* __restrict__ xscale, int64_t in, int grid, float* __restrict__ s32,
+    float* __restrict__ inv_s32, float* __restrict__ ss32, int32_t* __restrict__ pow2_s) {
   pdl_wait();
   pdl_trigger();
   __shared__ uint32_t not_pow2[(kMaxGrid + 1 + 31) / 32];
@@ -88,7 +92,12 @@ __global__ void __launch_bounds__(kTabCols * kTabSlices) alpha_table_kernel(
     bool np2 = false;
     if (live) {
       s32[(int64_t)k * in + j] = f;
-      inv_s32[(int64_t)k * in + j] = __frcp_rn(f) * escale[k];
+      if (ss32 != nullptr) {
+        inv_s32[(int64_t)k * in + j] = __frcp_rn(f) * xscale[k];
+        ss32[(int64_t)k * in + j] = f * escale[k];
+      } else {
+        inv_s32[(int64_t)k * in + j] = __frcp_rn(f) * escale[k];
+      }
       np2 = (__float_as_uint(f) & 0x007FFFFFu) != 0u;
     }
     if (__any_sync(0xffffffffu, np2) && lane == 0) atomicOr(&not_pow2[k / 32], 1u << (k % 32));
@@ -216,8 +225,20 @@ cudaError_t launch_alpha_table(const double* sx, const double* root, const doubl
                                float* inv_s32, int32_t* pow2_s, cudaStream_t s) {
   if (grid < 1 || grid > kMaxGrid) return cudaErrorInvalidValue;
   return launch_pdl(alpha_table_kernel, (unsigned)((in + kTabCols - 1) / kTabCols),
-                    kTabCols * kTabSlices, 0, s, sx, root, inv_c, escale, in, grid, s32, inv_s32,
-                    pow2_s);
+                    kTabCols * kTabSlices, 0, s, sx, root, inv_c, escale,
+                    static_cast<const float*>(nullptr), in, grid, s32, inv_s32,
+                    static_cast<float*>(nullptr), pow2_s);
+}
+
+cudaError_t launch_alpha_table_xs(const double* sx, const double* root, const double* inv_c,
+                                  const float* escale, const float* xscale, int64_t in, int grid,
+                                  float* s32, float* inv_s32, float* ss32, int32_t* pow2_s,
+                                  cudaStream_t s) {
+  if (grid < 1 || grid > kMaxGrid || ss32 == nullptr || xscale == nullptr)
+    return cudaErrorInvalidValue;
+  return launch_pdl(alpha_table_kernel, (unsigned)((in + kTabCols - 1) / kTabCols),
+                    kTabCols * kTabSlices, 0, s, sx, root, inv_c, escale, xscale, in, grid, s32,
+                    inv_s32, ss32, pow2_s);
 }
 
 cudaError_t launch_reduce_argmin(const double* partials, const double* unscale, int n_alpha,

@@ -111,10 +111,13 @@ struct SearchArgs {
   int test_timeout;
 };
 
-// Precomputed group ranges, read only by the wide-group instantiations (kept
-// out of SearchArgs, which the other kernels read on every job).
+// Arguments read only by some instantiations (kept out of SearchArgs, which
+// every kernel reads on every job): the precomputed group ranges of the
+// wide-group kernels, and the per-alpha weight scaling of the kernels that
+// read X already divided by s.
 struct WideArgs {
-  const float* gext;  // group extremes [n_alpha][out][ngroups] (x2 asym)
+  const float* gext;    // group extremes [n_alpha][out][ngroups] (x2 asym)
+  const float* escale;  // [n_alpha]: 2^e_k, the power of two folded into the s table
   int group, ngroups;
 };
 
@@ -197,7 +200,10 @@ __device__ __forceinline__ uint32_t pack_f16x2(float2 v) {
 // scale) * (1/scale), q0 = t * (1/scale), then rounds it.
 // With CLAMP the rounded value is also capped at the group's top code
 // (chi = 1.5 * 2^23 + maxq - zero, in the shifted domain).
-template <bool EXACT, bool CLAMP, int G, int JC>
+//
+// With DIV false (X arrives already divided by s) the fp16 pairs are the
+// scaled rounding errors t - q * scale themselves and inv_row is unused.
+template <bool EXACT, bool CLAMP, bool DIV, int G, int JC>
 __device__ __forceinline__ void make_dw(const float (&t)[JC], int kbi, const float* inv_row,
                                         const float (&scl)[JC / G], const float (&rcp)[JC / G],
                                         const float (&chi)[JC / G], uint32_t (&pk)[32]) {
@@ -208,7 +214,7 @@ __device__ __forceinline__ void make_dw(const float (&t)[JC], int kbi, const flo
     const int cgi = kbi * 8 + cc;
     const int g = (cgi * 8) / G;
     float i8[8];
-    lds_f8(inv_row + cc * 8, i8);
+    if (DIV) lds_f8(inv_row + cc * 8, i8);
     const float2 rc2 = make_float2(rcp[g], rcp[g]);
     const float2 ns2 = make_float2(-scl[g], -scl[g]);
 #pragma unroll
@@ -228,12 +234,19 @@ __device__ __forceinline__ void make_dw(const float (&t)[JC], int kbi, const flo
       }
       const float2 qv = __fadd2_rn(av, nm2);
       const float2 ev = __ffma2_rn(qv, ns2, tv);  // t - q * scale
-      pk[cc * 4 + e] = pack_f16x2(__fmul2_rn(ev, make_float2(i8[2 * e], i8[2 * e + 1])));
+      if (DIV)
+        pk[cc * 4 + e] = pack_f16x2(__fmul2_rn(ev, make_float2(i8[2 * e], i8[2 * e + 1])));
+      else
+        pk[cc * 4 + e] = pack_f16x2(ev);
     }
   }
 }
 
-template <typename WT, int G, bool SYM>
+// XS: X arrives as n_alpha fp16 copies X * 2^m_k / s_k (a 3-D tensor map
+// [n_alpha][N][in]); the s table rows in the W stages hold s_k * 2^e_k and
+// the producer writes (t - q * scale) * 2^e_k with no division by s (needs
+// one alpha per unit).
+template <typename WT, int G, bool SYM, bool XS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     awq_search_kernel(const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmX,
@@ -258,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t w_ring = base + kCtrlBytes;
   const uint8_t* w_ring_ptr = gbase + kCtrlBytes;
   const uint32_t W_STAGE = p.w_stage;
-  const uint32_t S_BYTES = 2u * (uint32_t)p.a_per * kKB * 4u;  // s and 2^e/s rows
+  const uint32_t S_BYTES = (XS ? 1u : 2u) * (uint32_t)p.a_per * kKB * 4u;  // s (and 2^e/s) rows
   const uint32_t X_STAGE = (uint32_t)p.T * 128u;
   const uint32_t x_ring = w_ring + (uint32_t)p.sw * W_STAGE;
 
@@ -330,7 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tma_load_2d(dst, &tmW, bar, kb * kKB, rt * kRows);
           }
-          tma_load_3d(dst + W_TILE, &tmS, bar, kb * kKB, ag * p.a_per, 0);
+          if (XS)
+            tma_load_2d(dst + W_TILE, &tmS, bar, kb * kKB, ag);
+          else
+            tma_load_3d(dst + W_TILE, &tmS, bar, kb * kKB, ag * p.a_per, 0);
           if (b) ++wc1; else ++wc0;
         }
       }
@@ -346,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
         const int tt = (u % units_per_rt) % p.n_tt;
+        const int ag = (u % units_per_rt) / p.n_tt;
         for (int kb = 0; kb < p.n_kb; ++kb) {
           const uint32_t st = seq % p.sx, ph = (seq / p.sx) & 1;
           if (!mbar_wait(smem_addr(&c.x_empty[st]), ph ^ 1, abort, lim, p.diag, 3, seq)) {
@@ -354,7 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t bar = smem_addr(&c.x_full[st]);
           mbar_arrive_expect_tx(bar, X_STAGE);
-          tma_load_2d(x_ring + st * X_STAGE, &tmX, bar, kb * kKB, tt * p.T);
+          if (XS)
+            tma_load_3d(x_ring + st * X_STAGE, &tmX, bar, kb * kKB, tt * p.T, ag);
+          else
+            tma_load_2d(x_ring + st * X_STAGE, &tmX, bar, kb * kKB, tt * p.T);
           ++seq;
         }
       }
@@ -435,6 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t exact_mask = 0;
       for (int a = 0; a < na; ++a)
         if (p.pow2_s[ag * p.a_per + a] != 0) exact_mask |= 1u << a;
+      // the step's lower clamp 1e-8, scaled like t (XS: one alpha per unit)
+      const float clampk = XS ? 1e-8f * __ldg(wa.escale + ag) : 1e-8f;
       for (int kg = wg; ok && kg < n_kg; kg += 2) {
         const uint8_t* stg[KBJ];
 #pragma unroll
@@ -497,12 +519,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int g = 0; g < NG; ++g) {
             if (SYM) {
               const float m = fmaxf(fmaxf(r0[g][0], r0[g][1]), fmaxf(r0[g][2], r0[g][3]));
-              scl[g] = fmaxf(__fdiv_rn(m, p.Lf), 1e-8f);
+              scl[g] = fmaxf(__fdiv_rn(m, p.Lf), clampk);
               chi[g] = 0.0f;
             } else {
               const float lo = fminf(fminf(r0[g][0], r0[g][1]), fminf(r0[g][2], r0[g][3]));
               const float hi = fmaxf(fmaxf(r1[g][0], r1[g][1]), fmaxf(r1[g][2], r1[g][3]));
-              scl[g] = fmaxf(__fdiv_rn(__fsub_rn(hi, lo), p.maxqf), 1e-8f);
+              scl[g] = fmaxf(__fdiv_rn(__fsub_rn(hi, lo), p.maxqf), clampk);
               chi[g] = kRoundMagic + p.maxqf - rintf(__fdiv_rn(-lo, scl[g]));
             }
             rcp[g] = __frcp_rn(scl[g]);
@@ -521,9 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reinterpret_cast<const float*>(stg[kbi] + W_TILE) + (p.a_per + a) * kKB;
             uint32_t pk[32];
             if (exact)
-              make_dw<true, !SYM, GE, JC>(t, kbi, inv_row, scl, rcp, chi, pk);
+              make_dw<true, !SYM, !XS, GE, JC>(t, kbi, inv_row, scl, rcp, chi, pk);
             else
-              make_dw<false, false, GE, JC>(t, kbi, inv_row, scl, rcp, chi, pk);
+              make_dw<false, false, !XS, GE, JC>(t, kbi, inv_row, scl, rcp, chi, pk);
             tmem_st32(tmem + lane_addr + kSlotCol0 + ds * 32u, pk);
             tmem_wait_st();
             tc_fence_before();
@@ -657,8 +679,48 @@ bool make_scale_map(CUtensorMap* m, const float* s32, uint64_t in, uint64_t n_al
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over the n_alpha fp16 copies of X / s ([n_alpha][N][in]): boxes of
+// 64 columns x T tokens of one alpha, 128-byte swizzle (the MMA's B layout).
+bool make_xs_map(CUtensorMap* m, const void* xs, uint64_t in, uint64_t N, uint64_t n_alpha,
+                 uint32_t T) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {in, N, n_alpha};
+  cuuint64_t strides[2] = {in * 2, N * in * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kKB, T, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(xs), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D map over the scaled s table ([n_alpha][in] float32): boxes of 64
+// columns of one alpha, unswizzled; out-of-range columns read as zero.
+bool make_s_map(CUtensorMap* m, const float* ss32, uint64_t in, uint64_t n_alpha) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {in, n_alpha};
+  cuuint64_t strides[1] = {in * 4};
+  cuuint32_t box[2] = {(cuuint32_t)kKB, 1};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ss32), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
                           const SearchArgs, const WideArgs);
+
+template <typename WT>
+KernelFn pick_xs(int group, int sym) {
+  switch (group) {
+    case 32: return sym ? &awq_search_kernel<WT, 32, true, true> : &awq_search_kernel<WT, 32, false, true>;
+    case 64: return sym ? &awq_search_kernel<WT, 64, true, true> : &awq_search_kernel<WT, 64, false, true>;
+    case 128:
+      return sym ? &awq_search_kernel<WT, 128, true, true> : &awq_search_kernel<WT, 128, false, true>;
+    default: return nullptr;
+  }
+}
 
 template <typename WT>
 KernelFn pick_g(int group, int sym, bool gp) {
@@ -684,6 +746,14 @@ bool search_wide_group(int64_t group, int64_t in) {
   return in % 8 == 0 && group > 0 && in % group == 0 && (group % 256 == 0 || group == in);
 }
 
+bool search_xs_eligible(int dt, int64_t in, int64_t N, int group, int grid) {
+  // one alpha per unit (more than 128 tokens), a narrow group, 16-bit W, and
+  // all n_alpha copies of X / s small enough to stay in L2 during the search
+  const int64_t n_alpha = (int64_t)grid + 1;
+  return dt != kDtF32 && N > 128 && in % 8 == 0 && (group == 32 || group == 64 || group == 128) &&
+         n_alpha * N * in * 2 <= ((int64_t)64 << 20);
+}
+
 bool search_supported(int dt, int64_t out, int64_t in, int64_t N, int bits, int group, int grid) {
   (void)dt; (void)bits; (void)grid;
   if (group != 32 && group != 64 && group != 128 && !search_wide_group(group, in)) return false;
@@ -693,7 +763,7 @@ bool search_supported(int dt, int64_t out, int64_t in, int64_t N, int bits, int 
 }
 
 SearchPlan plan_search(int dt, int64_t out, int64_t in, int64_t N, int n_alpha, int group,
-                       bool gp, int sms) {
+                       bool gp, int sms, bool xs) {
   SearchPlan pl{};
   pl.n_tt = (int)((N + 255) / 256);
   const int64_t per = (N + pl.n_tt - 1) / pl.n_tt;
@@ -710,7 +780,7 @@ SearchPlan plan_search(int dt, int64_t out, int64_t in, int64_t N, int n_alpha, 
   pl.n_tiles = pl.n_rt * pl.n_tt;
   const int kbj = (group == 128 || gp) ? 2 : 1;
   const size_t w_tile = (size_t)kRows * kKB * dtype_size(dt);
-  pl.w_stage = align_up(w_tile + 2 * (size_t)pl.a_per * kKB * 4, 1024);
+  pl.w_stage = align_up(w_tile + (xs ? 1 : 2) * (size_t)pl.a_per * kKB * 4, 1024);
   const size_t x_stage = (size_t)pl.T * 128;
   const size_t budget = (size_t)max_dyn_smem() - kCtrlBytes - 1024;
   // deepest W ring (two equal banks, each holding at least one job) that
@@ -731,13 +801,15 @@ SearchPlan plan_search(int dt, int64_t out, int64_t in, int64_t N, int n_alpha, 
 cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, int64_t in,
                           int64_t N, int bits, int group, int sym, int n_alpha,
                           const float* s32, const float* inv_s32, const int32_t* pow2_s,
-                          const float* gext, double* partials, const SearchPlan& pl,
-                          int64_t wait_limit_ns,
+                          const float* gext, const float* ss32, const float* escale,
+                          double* partials, const SearchPlan& pl, int64_t wait_limit_ns,
                           int test_timeout, int32_t* dev_status, uint32_t* diag, cudaStream_t s,
                           cudaEvent_t ev0, cudaEvent_t ev1) {
   KernelFn fn = nullptr;
   CUtensorMapDataType wt;
   uint32_t wbox;
+  const bool xs = ss32 != nullptr;
+  if (xs && (gext != nullptr || pl.a_per != 1 || dt == kDtF32)) return cudaErrorInvalidValue;
   switch (dt) {
     case kDtF32:
       fn = pick_g<float>(group, sym, gext != nullptr);
@@ -745,12 +817,12 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
       wbox = 32;
       break;
     case kDtF16:
-      fn = pick_g<__half>(group, sym, gext != nullptr);
+      fn = xs ? pick_xs<__half>(group, sym) : pick_g<__half>(group, sym, gext != nullptr);
       wt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
       wbox = 64;
       break;
     default:
-      fn = pick_g<__nv_bfloat16>(group, sym, gext != nullptr);
+      fn = xs ? pick_xs<__nv_bfloat16>(group, sym) : pick_g<__nv_bfloat16>(group, sym, gext != nullptr);
       wt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
       wbox = 64;
       break;
@@ -759,17 +831,25 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
   if (search_wide_group(group, in) && gext == nullptr) return cudaErrorInvalidValue;
   if (gext != nullptr && (in % 8 != 0 || (group != in && group % (2 * kKB) != 0)))
     return cudaErrorInvalidValue;
-  const uintptr_t tbl = reinterpret_cast<uintptr_t>(inv_s32) - reinterpret_cast<uintptr_t>(s32);
-  if (inv_s32 <= s32 || (tbl & 15) != 0 || (reinterpret_cast<uintptr_t>(s32) & 15) != 0)
-    return cudaErrorInvalidValue;
   CUtensorMap mw, mx, ms;
   if (!make_map(&mw, wt, W, (uint64_t)in, (uint64_t)out, (uint64_t)in * dtype_size(dt), wbox, kRows))
     return cudaErrorInvalidValue;
-  if (!make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xf16, (uint64_t)in, (uint64_t)N,
-                (uint64_t)in * 2, kKB, (uint32_t)pl.T))
-    return cudaErrorInvalidValue;
-  if (!make_scale_map(&ms, s32, (uint64_t)in, (uint64_t)n_alpha, (uint64_t)tbl, (uint32_t)pl.a_per))
-    return cudaErrorInvalidValue;
+  if (xs) {
+    if ((reinterpret_cast<uintptr_t>(ss32) & 15) != 0 || escale == nullptr) return cudaErrorInvalidValue;
+    if (!make_xs_map(&mx, Xf16, (uint64_t)in, (uint64_t)N, (uint64_t)n_alpha, (uint32_t)pl.T))
+      return cudaErrorInvalidValue;
+    if (!make_s_map(&ms, ss32, (uint64_t)in, (uint64_t)n_alpha)) return cudaErrorInvalidValue;
+  } else {
+    const uintptr_t tbl = reinterpret_cast<uintptr_t>(inv_s32) - reinterpret_cast<uintptr_t>(s32);
+    if (inv_s32 <= s32 || (tbl & 15) != 0 || (reinterpret_cast<uintptr_t>(s32) & 15) != 0)
+      return cudaErrorInvalidValue;
+    if (!make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xf16, (uint64_t)in, (uint64_t)N,
+                  (uint64_t)in * 2, kKB, (uint32_t)pl.T))
+      return cudaErrorInvalidValue;
+    if (!make_scale_map(&ms, s32, (uint64_t)in, (uint64_t)n_alpha, (uint64_t)tbl,
+                        (uint32_t)pl.a_per))
+      return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
   SearchArgs a;
@@ -799,6 +879,7 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
   if (ev0 && (e = cudaEventRecord(ev0, s)) != cudaSuccess) return e;
   WideArgs wa;
   wa.gext = gext;
+  wa.escale = escale;
   wa.group = group;
   wa.ngroups = (int)(in / group);
   e = launch_pdl(fn, dim3((unsigned)pl.grid), dim3(kThreads), (size_t)pl.smem, s, mw, mx, ms, a,

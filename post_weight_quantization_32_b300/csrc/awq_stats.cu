@@ -61,6 +61,7 @@ struct ColSum {
   }
   __device__ __forceinline__ Part part(int e) const { return acc[e]; }
   __device__ __forceinline__ void flag_specials(uint32_t*) const {}
+  __device__ __forceinline__ void finish_max(float&) const {}
   static __device__ __forceinline__ double total(Part a, uint32_t) { return a; }
 };
 
@@ -69,12 +70,13 @@ struct ColSum<__half> {
   using Part = unsigned long long;
   unsigned long long acc[8];
   uint32_t special;  // bit e: column e saw an infinity; bit 8 + e: a NaN
+  uint32_t mbits;    // largest |x| seen (NaN excluded) as fp16 bits: their integer order is the value order
   __device__ __forceinline__ void init() {
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0ull;
     special = 0u;
+    mbits = 0u;
   }
-  // (max|X| is not tracked here: an fp16 X needs no copy, so no caller asks)
   __device__ __forceinline__ void add(const __half* p, float&) {
     const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -82,6 +84,7 @@ struct ColSum<__half> {
     for (int e = 0; e < 8; ++e) {
       const uint32_t h = (w[e >> 1] >> ((e & 1) * 16)) & 0x7FFFu;
       const uint32_t ex = h >> 10, mant = h & 0x3FFu;
+      if (!(ex == 31u && mant != 0u)) mbits = max(mbits, h);
       if (ex == 31u) {
         special |= mant ? (1u << (8 + e)) : (1u << e);
       } else {
@@ -91,6 +94,9 @@ struct ColSum<__half> {
     }
   }
   __device__ __forceinline__ Part part(int e) const { return acc[e]; }
+  __device__ __forceinline__ void finish_max(float& m) const {
+    m = __half2float(__ushort_as_half((unsigned short)mbits));
+  }
   // per column of the CTA: bit 0 = an infinity was seen, bit 1 = a NaN
   __device__ __forceinline__ void flag_specials(uint32_t* spec) const {
     if (special == 0u) return;
@@ -172,6 +178,7 @@ __global__ void __launch_bounds__(256) stats_vec_kernel(const T* __restrict__ X,
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[r][c * 8 + e] = cs.part(e);
   cs.flag_specials(spec + c * 8);
+  cs.finish_max(m);
   if (xmax != nullptr) block_absmax(m, xmax);  // contains __syncthreads
   __syncthreads();
   {  // the 64 slices in a fixed two-level order: 8 runs of 8, then the 8 run sums
@@ -277,6 +284,36 @@ __global__ void __launch_bounds__(256) to_f16_kernel(const T* __restrict__ X, in
   }
 }
 
+// xs[k][n][j] = fp16(X[n][j] * xinv[k][j]).  CTA (x, k): lane l of every
+// warp owns the eight columns 8 (32 x + l) .. + 7 (a warp covers 512
+// contiguous bytes of a row), keeps their xinv factors in registers, and
+// the CTA's eight warps walk the rows.
+template <typename T>
+__global__ void __launch_bounds__(256) x_over_s_kernel(const T* __restrict__ X, int N, int in,
+                                                       const float* __restrict__ xinv,
+                                                       uint4* __restrict__ xs) {
+  pdl_wait();
+  pdl_trigger();
+  const int k = blockIdx.y;
+  const int j8 = blockIdx.x * 32 + (threadIdx.x & 31);
+  const int n8 = in / 8;
+  if (j8 >= n8) return;
+  float f[8];
+  load8_f32<float>(xinv + (int64_t)k * in + j8 * 8, f);
+  uint4* dst = xs + (int64_t)k * N * n8 + j8;
+  for (int n = threadIdx.x >> 5; n < N; n += 8) {
+    float v[8];
+    load8_f32<T>(X + (int64_t)n * in + j8 * 8, v);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __half2 h = __floats2half2_rn(v[2 * q] * f[2 * q], v[2 * q + 1] * f[2 * q + 1]);
+      w[q] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    dst[(int64_t)n * n8] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 unsigned grid_for(int64_t work);
 
 template <typename T>
@@ -285,7 +322,6 @@ cudaError_t stats_dispatch(const void* X, int64_t N, int64_t in, double* sx, uin
                            cudaStream_t s) {
   const bool vec = (in % 8 == 0) && ((reinterpret_cast<uintptr_t>(X) & 15) == 0);
   const bool wvec = W != nullptr && nW % 8 == 0 && ((reinterpret_cast<uintptr_t>(W) & 15) == 0);
-  if (std::is_same<T, __half>::value && xmax != nullptr) return cudaErrorInvalidValue;
   if (vec && (W == nullptr || wvec)) {
     const int nx = (int)((in + kStatCols - 1) / kStatCols);
     // max|W| blocks: eight 16-byte loads in flight per thread; at most four
@@ -338,6 +374,26 @@ cudaError_t launch_absmax(const void* p, int dt, int64_t n, uint32_t* out, cudaS
                                                         vec, out);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_x_over_s(const void* X, int dt, int64_t N, int64_t in, int n_alpha,
+                            const float* xinv, void* xs, cudaStream_t s) {
+  if (in % 8 != 0 || (reinterpret_cast<uintptr_t>(X) & 15) != 0 || N > (1 << 24) ||
+      in > (1 << 24) || n_alpha > 65535)
+    return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)((in / 8 + 31) / 32), (unsigned)n_alpha);
+  uint4* d = static_cast<uint4*>(xs);
+  switch (dt) {
+    case kDtF32:
+      return launch_pdl(x_over_s_kernel<float>, grid, 256, 0, s, static_cast<const float*>(X),
+                        (int)N, (int)in, xinv, d);
+    case kDtF16:
+      return launch_pdl(x_over_s_kernel<__half>, grid, 256, 0, s, static_cast<const __half*>(X),
+                        (int)N, (int)in, xinv, d);
+    default:
+      return launch_pdl(x_over_s_kernel<__nv_bfloat16>, grid, 256, 0, s,
+                        static_cast<const __nv_bfloat16*>(X), (int)N, (int)in, xinv, d);
+  }
 }
 
 cudaError_t launch_to_f16(const void* X, int dt, int64_t n, const uint32_t* xmax_bits, void* dst,

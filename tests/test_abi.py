@@ -56,11 +56,12 @@ def test_status_strings(lib):
     assert b"unknown" in lib.awq_status_string(99)
 
 
-def _ws(lib, *a):
-    lib.awq_search_workspace_bytes.restype = ctypes.c_size_t
-    lib.awq_search_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
-                                               ctypes.c_int64, ctypes.c_int, ctypes.c_int]
-    return lib.awq_search_workspace_bytes(*a)
+def _ws(lib, *a, fn="awq_search_workspace_min_bytes"):
+    f = getattr(lib, fn)
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                  ctypes.c_int]
+    return f(*a)
 
 
 def test_workspace_query(lib):
@@ -74,10 +75,24 @@ def test_workspace_query(lib):
     # per alpha, row and group)
     assert _ws(lib, 1, 4096, 4096, 256, 256, 20) >= n + 21 * 4096 * 16 * 8
     assert _ws(lib, 1, 4096, 4096, 256, 4096, 20) >= n + 21 * 4096 * 8
-    assert _ws(lib, 2, 4096, 4096, 256, 100, 20) == 0      # group does not divide in
-    assert _ws(lib, 2, 0, 4096, 256, 128, 20) == 0
-    assert _ws(lib, 7, 16, 16, 16, 16, 20) == 0
-    assert _ws(lib, 2, 16, 16, 16, 16, 5000) == 0
+    for fn in ("awq_search_workspace_min_bytes", "awq_search_workspace_bytes"):
+        assert _ws(lib, 2, 4096, 4096, 256, 100, 20, fn=fn) == 0      # group does not divide in
+        assert _ws(lib, 2, 0, 4096, 256, 128, 20, fn=fn) == 0
+        assert _ws(lib, 7, 16, 16, 16, 16, 20, fn=fn) == 0
+        assert _ws(lib, 2, 16, 16, 16, 16, 5000, fn=fn) == 0
+
+
+def test_workspace_of_the_pre_divided_path(lib):
+    full = lambda *a: _ws(lib, *a, fn="awq_search_workspace_bytes")  # noqa: E731
+    # 16-bit, more than 128 tokens, group 128, 21 copies of X / s within 64 MiB:
+    # the full workspace adds the copies (fp16, N x in each) and the scaled s table
+    for dt in (1, 2):
+        assert full(dt, 4096, 4096, 256, 128, 20) >= (
+            _ws(lib, 1, 4096, 4096, 256, 128, 20) + 21 * 256 * 4096 * 2 + 21 * 4096 * 4)
+    # not eligible: fp32, 128 tokens or fewer, wide groups, or copies beyond 64 MiB
+    for args in ((0, 4096, 4096, 256, 128, 20), (1, 4096, 4096, 128, 128, 20),
+                 (1, 4096, 4096, 256, 256, 20), (2, 8192, 28672, 1024, 128, 40)):
+        assert full(*args) == _ws(lib, *args)
 
 
 def test_search_rejects_bad_arguments_on_host(lib):
