@@ -81,8 +81,8 @@ int awq_channel_stats(const void* X, int dtype, int64_t N, int64_t in,
 /*
  * Bytes of device workspace for awq_search's fastest path at these sizes (0
  * on invalid sizes).  The workspace must be 256-byte aligned.  Where the
- * problem allows it (more than 128 tokens, group 32, 64 or 128, fp16 or
- * bf16, and (grid + 1) * N * in * 2 <= 64 MiB) this includes room for
+ * problem allows it (more than 128 tokens, group 8, 16, 32, 64 or 128, fp16
+ * or bf16, and (grid + 1) * N * in * 2 <= 64 MiB) this includes room for
  * grid + 1 fp16 copies of X / s, which the search then reads instead of
  * dividing every weight change by s.
  */
@@ -110,10 +110,10 @@ size_t awq_search_workspace_min_bytes(int dtype, int64_t out, int64_t in, int64_
  *   bits   2..8                   code width
  *   group  columns per quantization group; divides `in`.  group == in is the
  *          pages' "one group per row".  This build's search handles group
- *          in {32, 64, 128}, any multiple of 256, and group == in (the last
- *          two need in % 8 == 0); others return AWQ_ERR_UNSUPPORTED.  The
- *          last two get their group ranges from a pass over W ahead of the
- *          search.
+ *          in {8, 16, 32, 64, 128}, any other multiple of 8 (24, 48, 96,
+ *          256, ...) and group == in (those need in % 8 == 0); others return
+ *          AWQ_ERR_UNSUPPORTED.  Groups outside {8, ..., 128} get their
+ *          ranges from a pass over W ahead of the search.
  *   sym    1: symmetric, scale = max|w| / (2^(b-1) - 1), codes in
  *             [-2^(b-1), 2^(b-1) - 1]
  *             ["GPTQ and AWQ weight quantisation", "Output MSE vs bit width"]

@@ -60,7 +60,7 @@ WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int group, int gr
   // fp16 copy of a bf16/fp32 X, or the n_alpha copies of X / s
   w.xf16 = take(xs ? (size_t)n_alpha * N * in * 2 : (dt == kDtF16 ? 0 : (size_t)N * in * 2));
   // extremes of groups wider than a producer job: two floats per (alpha, row, group)
-  w.gext_bytes = search_wide_group(group, in) ? (size_t)n_alpha * out * (in / group) * 8 : 0;
+  w.gext_bytes = search_needs_ranges(group, in) ? (size_t)n_alpha * out * (in / group) * 8 : 0;
   w.gext = take(w.gext_bytes);
   w.partials = take((size_t)n_alpha * n_tiles * 8);
   w.total = o;
@@ -212,7 +212,8 @@ int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t 
   const void* xh = (x_copy || xs) ? static_cast<const void*>(wsb + ws.xf16) : X;
 
   const SearchPlan pl =
-      plan_search(dtype, out, in, N, n_alpha, group, gext != nullptr, device_sm_count(), xs);
+      plan_search(dtype, out, in, N, n_alpha, group, gext != nullptr && search_wide_group(group, in),
+                  device_sm_count(), xs);
   double* partials = reinterpret_cast<double*>(wsb + ws.partials);
   e = launch_search(W, xh, dtype, out, in, N, bits, group, sym ? 1 : 0, n_alpha, s32, inv_s32,
                     pow2_s, gext, ss32, xs ? ca.escale : nullptr, partials, pl,

@@ -1,5 +1,7 @@
-// Group ranges computed ahead of the search, for groups wider than one
-// producer job (a multiple of 256 columns, or one group per row).
+// Group ranges computed ahead of the search, for groups that the search
+// kernel's producer jobs do not contain: wider than a job (a multiple of 256
+// columns, or one group per row), or not aligned with the 64-column jobs
+// (another multiple of 8, e.g. 24, 48, 96).
 //
 // For every alpha k, row r and group g the quantizer needs the extremes of
 // t = fl32(w * s_k) over the group ("AWQ vs GPTQ ...", group_params;
@@ -29,11 +31,13 @@ __device__ __forceinline__ void fold_max(float* p, float v) {
   atomicMax(reinterpret_cast<unsigned int*>(p), __float_as_uint(v) & 0x7FFFFFFFu);
 }
 
-// Warp task (row block rb, 256-column chunk ch): the chunk lies inside one
-// group because the group is a multiple of 256 or the whole row.  Each lane
-// keeps its 8 weights of kExtRows rows in registers and runs through the
-// alphas kExtAlphas at a time; per (row, alpha) the lanes' partial extremes
-// are combined by shuffles and lane 0 folds them into ext.
+// Warp task (row block rb, 256-column chunk ch).  Each lane's 8 columns lie
+// in one group (the group is a multiple of 8).  Each lane keeps its 8
+// weights of kExtRows rows in registers and runs through the alphas
+// kExtAlphas at a time; per (row, alpha) the partial extremes of the lanes
+// of one group are combined (a max over the lanes with the same group, on
+// the bit patterns of the non-negative values) and the group's first lane
+// folds them into ext.
 template <typename WT, bool SYM>
 __global__ void __launch_bounds__(256) group_extremes_kernel(const WT* __restrict__ W, int64_t out,
                                                              int64_t in, const float* __restrict__ s32,
@@ -51,7 +55,10 @@ __global__ void __launch_bounds__(256) group_extremes_kernel(const WT* __restric
     const int64_t rb = task / nchunk, ch = task % nchunk;
     const int64_t c0 = ch * kExtChunk + lane * 8;
     const bool live = c0 < in;  // in % 8 == 0, so all 8 columns are live
-    const int64_t g = (ch * kExtChunk) / group;
+    // lanes past the last column join the last lane's group with zeros
+    const int64_t g = (live ? c0 : in - 8) / group;
+    const unsigned same = __match_any_sync(0xffffffffu, (unsigned long long)g);
+    const bool leader = (int)(__ffs(same) - 1) == lane;
     float w[kExtRows][8];
 #pragma unroll
     for (int r = 0; r < kExtRows; ++r) {
@@ -94,16 +101,20 @@ __global__ void __launch_bounds__(256) group_extremes_kernel(const WT* __restric
           hi[r][a] = h;
           nlo[r][a] = -l;
         }
+      // (hi and nlo are >= 0 or -0 and never NaN: the running max ignores
+      // NaN and starts at 0; with the sign bit cleared the bit patterns order
+      // like the values)
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
+      for (int r = 0; r < kExtRows; ++r)
 #pragma unroll
-        for (int r = 0; r < kExtRows; ++r)
-#pragma unroll
-          for (int a = 0; a < kExtAlphas; ++a) {
-            hi[r][a] = fmaxf(hi[r][a], __shfl_xor_sync(0xffffffffu, hi[r][a], o));
-            if (!SYM) nlo[r][a] = fmaxf(nlo[r][a], __shfl_xor_sync(0xffffffffu, nlo[r][a], o));
-          }
-      if (lane == 0) {
+        for (int a = 0; a < kExtAlphas; ++a) {
+          hi[r][a] = __uint_as_float(
+              __reduce_max_sync(same, __float_as_uint(hi[r][a]) & 0x7FFFFFFFu));
+          if (!SYM)
+            nlo[r][a] = __uint_as_float(
+                __reduce_max_sync(same, __float_as_uint(nlo[r][a]) & 0x7FFFFFFFu));
+        }
+      if (leader) {
 #pragma unroll
         for (int r = 0; r < kExtRows; ++r)
 #pragma unroll
@@ -141,7 +152,8 @@ cudaError_t launch_ext(const void* W, int64_t out, int64_t in, const float* s32,
 cudaError_t launch_group_extremes(const void* W, int dt, int64_t out, int64_t in,
                                   const float* s32, int n_alpha, int64_t group, int sym,
                                   float* ext, cudaStream_t s) {
-  if (in % 8 != 0 || (group % kExtChunk != 0 && group != in)) return cudaErrorInvalidValue;
+  if (in % 8 != 0 || group < 8 || in % group != 0 || (group % 8 != 0 && group != in))
+    return cudaErrorInvalidValue;
   switch (dt) {
     case kDtF32: return launch_ext<float>(W, out, in, s32, n_alpha, group, sym, ext, s);
     case kDtF16: return launch_ext<__half>(W, out, in, s32, n_alpha, group, sym, ext, s);

@@ -137,10 +137,14 @@ struct SearchPlan {
 // search: a multiple of 256 columns (wider than one 128-column producer
 // job), or one group per row (group == in, any width).  Needs in % 8 == 0.
 bool search_wide_group(int64_t group, int64_t in);
+// Group widths whose ranges come from launch_group_extremes: the wide ones,
+// and any other multiple of 8 outside {8, 16, 32, 64, 128} (e.g. 24, 48,
+// 96), which 64-column producer jobs do not align with.  Needs in % 8 == 0.
+bool search_needs_ranges(int64_t group, int64_t in);
 bool search_supported(int dt, int64_t out, int64_t in, int64_t N, int bits, int group, int grid);
 // Whether the search may read X already divided by s (launch_search with
-// ss32): one alpha per work unit, group 32, 64 or 128, 16-bit W, and the
-// n_alpha fp16 copies of X / s small enough to stay in L2.
+// ss32): one alpha per work unit, group 8, 16, 32, 64 or 128, 16-bit W, and
+// the n_alpha fp16 copies of X / s small enough to stay in L2.
 bool search_xs_eligible(int dt, int64_t in, int64_t N, int group, int grid);
 // The smallest workspace awq_search accepts (without the pre-divided mode's
 // regions); awq_search_workspace_bytes may return more.
@@ -170,7 +174,7 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
 // t = fl32(W[row][j] * s32[k][j]) over the group's columns, folded into ext
 // (zeroed by the caller): symmetric ext[(k*out + row)*ngroups + g] = max|t|;
 // asymmetric ext[2i] = -min(min t, 0), ext[2i + 1] = max(max t, 0).
-// group is a multiple of 256 or equal to in; in % 8 == 0; W 16-byte aligned.
+// group is a multiple of 8 (or equal to in); in % 8 == 0; W 16-byte aligned.
 cudaError_t launch_group_extremes(const void* W, int dt, int64_t out, int64_t in,
                                   const float* s32, int n_alpha, int64_t group, int sym,
                                   float* ext, cudaStream_t s);

@@ -88,6 +88,7 @@ constexpr int kMaxSW = 8, kMaxSX = 8, kMaxAPer = 8;
 constexpr uint32_t kSlotCol0 = 256;
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: fma(x, r, M) - M = rint(x * r)
 constexpr uint32_t kCtrlBytes = 1024;
+constexpr int kMaxJobGroups = 4;  // groups a 64-column job can touch when they are >= 24 wide
 // Register split after setmaxnreg: 128 * 48 + 256 * 200 + 128 * 56 = 64512
 // must not exceed the 512 * 128 = 65536 registers the block is launched
 // with (the build checks that every search kernel is compiled to 128
@@ -254,12 +255,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const WideArgs wa) {
   // G == 0: groups wider than a job (a multiple of 256 columns or the whole
   // row) whose extremes come precomputed in p.gext
+  // G < 0: any other group width that is a multiple of 8 (24, 48, 96, ...):
+  // the extremes come precomputed as for G == 0, a 64-column job touches at
+  // most kMaxJobGroups groups, and every 8-column chunk takes its group's
+  // step
   constexpr bool GP = (G == 0);
+  constexpr bool GV = (G < 0);
   constexpr int KBJ = (G == 128 || GP) ? 2 : 1;  // K blocks per producer job
   constexpr int JC = KBJ * kKB;                  // columns per producer job
-  constexpr int NG = GP ? 1 : JC / G;            // groups per job
-  constexpr int CPG = GP ? JC / 8 : G / 8;       // 8-column chunks per group
-  constexpr int GE = GP ? JC : G;                // group width as one job sees it
+  constexpr int NG = GP ? 1 : (GV ? JC / 8 : JC / G);  // groups (GV: chunks) per job
+  constexpr int CPG = GP ? JC / 8 : (GV ? 1 : G / 8);  // 8-column chunks per group
+  constexpr int GE = GP ? JC : (GV ? 8 : G);           // group width as one job sees it
   constexpr uint32_t W_TILE = w_tile_bytes<WT>();
   constexpr uint32_t FULL = 0xffffffffu;
 
@@ -491,6 +497,29 @@ __global__ void __launch_bounds__(kThreads, 1)
               r1[0][0] = __ldg(wa.gext + 2 * gi + 1);
             }
           }
+          // GV: the extremes of the (at most kMaxJobGroups) groups the job touches
+          float vlo[kMaxJobGroups], vhi[kMaxJobGroups];
+          int vg0 = 0, vgn = 1;
+          if constexpr (GV) {
+            const int col0 = kg * JC;
+            vg0 = col0 / wa.group;
+            vgn = min((col0 + JC - 1) / wa.group, wa.ngroups - 1) - vg0 + 1;
+            const int64_t grow =
+                min((int64_t)(u / units_per_rt) * kRows + row, (int64_t)p.out - 1);
+            const int64_t gi0 = ((int64_t)(ag * p.a_per + a) * p.out + grow) * wa.ngroups + vg0;
+#pragma unroll
+            for (int i = 0; i < kMaxJobGroups; ++i) {
+              vlo[i] = vhi[i] = 0.0f;
+              if (i < vgn) {
+                if (SYM) {
+                  vhi[i] = __ldg(wa.gext + gi0 + i);
+                } else {
+                  vlo[i] = -__ldg(wa.gext + 2 * (gi0 + i));
+                  vhi[i] = __ldg(wa.gext + 2 * (gi0 + i) + 1);
+                }
+              }
+            }
+          }
 #pragma unroll
           for (int cgi = 0; cgi < JC / 8; ++cgi) {
             const int kbi = cgi >> 3, cc = cgi & 7, g = cgi / CPG;
@@ -503,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   __fmul2_rn(make_float2(w8[2 * e], w8[2 * e + 1]), make_float2(s8[2 * e], s8[2 * e + 1]));
               t[cgi * 8 + 2 * e] = tv.x;
               t[cgi * 8 + 2 * e + 1] = tv.y;
-              if constexpr (!GP) {
+              if constexpr (!GP && !GV) {
                 if (SYM) {
                   r0[g][e] = fmax3f(r0[g][e], fabsf(tv.x), fabsf(tv.y));
                 } else {
@@ -515,8 +544,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // group steps
           float scl[NG], rcp[NG], chi[NG];
+          if constexpr (GV) {
+            // each group's step once, then every chunk takes its group's
+            float vs[kMaxJobGroups], vr[kMaxJobGroups], vc[kMaxJobGroups];
 #pragma unroll
-          for (int g = 0; g < NG; ++g) {
+            for (int i = 0; i < kMaxJobGroups; ++i) {
+              if (SYM) {
+                vs[i] = fmaxf(__fdiv_rn(vhi[i], p.Lf), clampk);
+                vc[i] = 0.0f;
+              } else {
+                vs[i] = fmaxf(__fdiv_rn(__fsub_rn(vhi[i], vlo[i]), p.maxqf), clampk);
+                vc[i] = kRoundMagic + p.maxqf - rintf(__fdiv_rn(-vlo[i], vs[i]));
+              }
+              vr[i] = __frcp_rn(vs[i]);
+            }
+            const int b1 = (vg0 + 1) * wa.group, b2 = b1 + wa.group, b3 = b2 + wa.group;
+#pragma unroll
+            for (int cgi = 0; cgi < NG; ++cgi) {
+              const int col = kg * JC + cgi * 8;
+              const int i = (col >= b1) + (col >= b2) + (col >= b3);
+              scl[cgi] = i == 0 ? vs[0] : i == 1 ? vs[1] : i == 2 ? vs[2] : vs[3];
+              rcp[cgi] = i == 0 ? vr[0] : i == 1 ? vr[1] : i == 2 ? vr[2] : vr[3];
+              chi[cgi] = i == 0 ? vc[0] : i == 1 ? vc[1] : i == 2 ? vc[2] : vc[3];
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < (GV ? 0 : NG); ++g) {
             if (SYM) {
               const float m = fmaxf(fmaxf(r0[g][0], r0[g][1]), fmaxf(r0[g][2], r0[g][3]));
               scl[g] = fmaxf(__fdiv_rn(m, p.Lf), clampk);
@@ -714,6 +767,8 @@ using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMa
 template <typename WT>
 KernelFn pick_xs(int group, int sym) {
   switch (group) {
+    case 8: return sym ? &awq_search_kernel<WT, 8, true, true> : &awq_search_kernel<WT, 8, false, true>;
+    case 16: return sym ? &awq_search_kernel<WT, 16, true, true> : &awq_search_kernel<WT, 16, false, true>;
     case 32: return sym ? &awq_search_kernel<WT, 32, true, true> : &awq_search_kernel<WT, 32, false, true>;
     case 64: return sym ? &awq_search_kernel<WT, 64, true, true> : &awq_search_kernel<WT, 64, false, true>;
     case 128:
@@ -723,9 +778,13 @@ KernelFn pick_xs(int group, int sym) {
 }
 
 template <typename WT>
-KernelFn pick_g(int group, int sym, bool gp) {
-  if (gp) return sym ? &awq_search_kernel<WT, 0, true> : &awq_search_kernel<WT, 0, false>;
+KernelFn pick_g(int group, int sym, int64_t in, bool gp) {
+  if (gp && search_wide_group(group, in))
+    return sym ? &awq_search_kernel<WT, 0, true> : &awq_search_kernel<WT, 0, false>;
+  if (gp) return sym ? &awq_search_kernel<WT, -1, true> : &awq_search_kernel<WT, -1, false>;
   switch (group) {
+    case 8: return sym ? &awq_search_kernel<WT, 8, true> : &awq_search_kernel<WT, 8, false>;
+    case 16: return sym ? &awq_search_kernel<WT, 16, true> : &awq_search_kernel<WT, 16, false>;
     case 32: return sym ? &awq_search_kernel<WT, 32, true> : &awq_search_kernel<WT, 32, false>;
     case 64: return sym ? &awq_search_kernel<WT, 64, true> : &awq_search_kernel<WT, 64, false>;
     case 128: return sym ? &awq_search_kernel<WT, 128, true> : &awq_search_kernel<WT, 128, false>;
@@ -746,17 +805,29 @@ bool search_wide_group(int64_t group, int64_t in) {
   return in % 8 == 0 && group > 0 && in % group == 0 && (group % 256 == 0 || group == in);
 }
 
+namespace {
+bool in_job_group(int64_t group) {
+  return group == 8 || group == 16 || group == 32 || group == 64 || group == 128;
+}
+}  // namespace
+
+bool search_needs_ranges(int64_t group, int64_t in) {
+  if (search_wide_group(group, in)) return true;  // (one group per row included)
+  return !in_job_group(group) && group > 0 && in % group == 0 && group % 8 == 0 && in % 8 == 0;
+}
+
 bool search_xs_eligible(int dt, int64_t in, int64_t N, int group, int grid) {
-  // one alpha per unit (more than 128 tokens), a narrow group, 16-bit W, and
+  // one alpha per unit (more than 128 tokens), a group inside one producer
+  // job (8, 16, 32, 64 or 128 columns), 16-bit W, and
   // all n_alpha copies of X / s small enough to stay in L2 during the search
   const int64_t n_alpha = (int64_t)grid + 1;
-  return dt != kDtF32 && N > 128 && in % 8 == 0 && (group == 32 || group == 64 || group == 128) &&
+  return dt != kDtF32 && N > 128 && in % 8 == 0 && in_job_group(group) &&
          n_alpha * N * in * 2 <= ((int64_t)64 << 20);
 }
 
 bool search_supported(int dt, int64_t out, int64_t in, int64_t N, int bits, int group, int grid) {
   (void)dt; (void)bits; (void)grid;
-  if (group != 32 && group != 64 && group != 128 && !search_wide_group(group, in)) return false;
+  if (!in_job_group(group) && !search_needs_ranges(group, in)) return false;
   if (in % group != 0) return false;
   if (out > (1 << 24) || N > (1 << 24) || in > (1 << 24)) return false;
   return true;
@@ -812,25 +883,24 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
   if (xs && (gext != nullptr || pl.a_per != 1 || dt == kDtF32)) return cudaErrorInvalidValue;
   switch (dt) {
     case kDtF32:
-      fn = pick_g<float>(group, sym, gext != nullptr);
+      fn = pick_g<float>(group, sym, in, gext != nullptr);
       wt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
       wbox = 32;
       break;
     case kDtF16:
-      fn = xs ? pick_xs<__half>(group, sym) : pick_g<__half>(group, sym, gext != nullptr);
+      fn = xs ? pick_xs<__half>(group, sym) : pick_g<__half>(group, sym, in, gext != nullptr);
       wt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
       wbox = 64;
       break;
     default:
-      fn = xs ? pick_xs<__nv_bfloat16>(group, sym) : pick_g<__nv_bfloat16>(group, sym, gext != nullptr);
+      fn = xs ? pick_xs<__nv_bfloat16>(group, sym)
+              : pick_g<__nv_bfloat16>(group, sym, in, gext != nullptr);
       wt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
       wbox = 64;
       break;
   }
   if (!fn || pl.sw < 2 || pl.sx < 3) return cudaErrorInvalidValue;
-  if (search_wide_group(group, in) && gext == nullptr) return cudaErrorInvalidValue;
-  if (gext != nullptr && (in % 8 != 0 || (group != in && group % (2 * kKB) != 0)))
-    return cudaErrorInvalidValue;
+  if (search_needs_ranges(group, in) != (gext != nullptr)) return cudaErrorInvalidValue;
   CUtensorMap mw, mx, ms;
   if (!make_map(&mw, wt, W, (uint64_t)in, (uint64_t)out, (uint64_t)in * dtype_size(dt), wbox, kRows))
     return cudaErrorInvalidValue;

@@ -118,8 +118,11 @@ def test_search_rejects_bad_arguments_on_host(lib):
     assert call(group=100) == 1          # does not divide in
     assert call(wsb=16) == 1             # workspace too small
     assert call(ws=fake + 8) == 1        # workspace not 256-byte aligned
-    assert call(group=384, n_in=768) == 2  # valid for the method, not handled by the search kernels
-    assert call(group=16) == 2
+    # valid for the method, not handled by the search kernels: a group that is
+    # not a multiple of 8 columns, or range-pass groups with in % 8 != 0
+    assert call(group=12, n_in=768) == 2
+    assert call(group=12, n_in=516) == 2
+    assert call(group=516, n_in=516) == 2
     assert call(W=fake + 4) == 2         # TMA needs 16-byte aligned rows
 
 

@@ -182,6 +182,16 @@ SEARCH_CASES = [
     (96, 1024, 20, "bf16", 4, 128, False, 20),     # 8 alphas per unit over 8 K groups
     (256, 384, 48, "bf16", 4, 128, True, 20),      # odd number of K groups
     (160, 512, 40, "f32", 4, 64, False, 12),
+    # narrow groups inside a 64-column job: eight or four per job
+    (130, 768, 40, "f16", 3, 8, True, 6),
+    (200, 768, 64, "bf16", 4, 16, False, 8),       # the AWQ guide's "a scale per 16"
+    (96, 256, 300, "f16", 3, 16, True, 20),        # two token tiles, X pre-divided by s
+    # groups the 64-column jobs do not align with: ranges from a pass over W,
+    # each 8-column chunk takes its group's step
+    (256, 768, 300, "bf16", 4, 96, False, 10),     # two token tiles
+    (96, 768, 50, "f16", 4, 48, True, 12),
+    (70, 1536, 20, "bf16", 4, 24, False, 8),       # up to four groups in one job
+    (33, 240, 9, "f32", 3, 40, True, 5),           # ragged K block
 ]
 
 
@@ -447,7 +457,9 @@ def test_search_wait_timeout_reports_and_recovers(awq):
 
 
 def test_search_rejects_unsupported_group(awq):
+    # groups of 4 columns divide in but are not a multiple of 8: the method
+    # allows them, the search kernels do not (the pack does)
     W, X = make_random_layer(64, 256, 16, dtype="bf16", seed=1)
     with pytest.raises(awq.AWQError) as ei:
-        awq.awq_search(W.cuda(), X.cuda(), 4, 16, True, 20)
+        awq.awq_search(W.cuda(), X.cuda(), 4, 4, True, 20)
     assert ei.value.code == 2
