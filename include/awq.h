@@ -170,6 +170,26 @@ int awq_output_power(const void* W, const void* X, int dtype,
                      void* workspace, size_t workspace_bytes,
                      double* power, int32_t* dev_status, awq_stream_t stream);
 
+/*
+ * awq_sweep_summary - one row of a bit-width / group-size sweep
+ * ["AWQ (activation-aware weight quantization)", "What the simulations
+ * show": RTN beside AWQ at each setting, as relative output errors;
+ * "GPTQ and AWQ weight quantisation", "Output MSE vs bit width"].
+ *
+ *   err    [grid + 1] double (read)  awq_search's per-alpha errors
+ *   best   [1] int32 (read)          awq_search's kept index
+ *   power  [1] double (read)         awq_output_power of the same W and X
+ *   grid   the search's grid (1..4096)
+ *   row    [5] double (written): the kept alpha's value on the grid
+ *          (linspace(0, 1, grid + 1)[best]), RTN's error err[0] (alpha = 0,
+ *          which is plain round-to-nearest), AWQ's error err[best], and the
+ *          two relative errors err[0] / power and err[best] / power.  With
+ *          best = -1 (no finite error) the alpha and AWQ entries are NaN.
+ * All pointers are device memory; the call enqueues one small kernel.
+ */
+int awq_sweep_summary(const double* err, const int32_t* best, const double* power, int grid,
+                      double* row, awq_stream_t stream);
+
 /* Options for awq_search_ex; zero-initialise, then set what you need. */
 typedef struct {
     awq_event_t ev_search_start;  /* recorded on `stream` right before the fused search kernel */

@@ -20,7 +20,7 @@ Entry points (same names as the C ABI):
 * ``awq_output_power(W, X)`` -> mean((X W^T)^2) (float64 [1]), the
   denominator of the relative output error; ``awq_sweep(W, X, settings)``
   runs the search over (bits, group) settings and reports RTN beside AWQ,
-  absolute and relative
+  absolute and relative (each row from ``awq_sweep_summary`` on the device)
 * ``awq_clip_search(W, X, s, bits, group, sym)`` -> (clip factors
   [out, in/group], shares or None); ``awq_quantize_pack_clipped(W, s, clip,
   ...)`` packs at those factors
@@ -43,7 +43,7 @@ __all__ = [
     "new_status", "check_status", "STATUS",
     "DTYPE", "awq_search_noalloc", "NOALLOC_SCRATCH_BYTES", "awq_output_power", "awq_sweep",
     "awq_export_checkpoint", "awq_clip_search", "awq_clip_search_workspace_bytes",
-    "awq_quantize_pack_clipped", "awq_gptq", "awq_gptq_workspace_bytes",
+    "awq_quantize_pack_clipped", "awq_gptq", "awq_gptq_workspace_bytes", "awq_sweep_summary",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -57,7 +57,8 @@ EXPORTS = ("awq_status_string", "awq_channel_stats", "awq_search_workspace_bytes
            "awq_search_workspace_min_bytes", "awq_search",
            "awq_search_ex", "awq_quantize_pack", "awq_search_noalloc", "awq_output_power",
            "awq_export_checkpoint", "awq_clip_search", "awq_clip_search_workspace_bytes",
-           "awq_quantize_pack_clipped", "awq_gptq", "awq_gptq_workspace_bytes")
+           "awq_quantize_pack_clipped", "awq_gptq", "awq_gptq_workspace_bytes",
+           "awq_sweep_summary")
 
 # Size of the library's fixed scratch array used by awq_search_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -74,6 +75,8 @@ def _load() -> ctypes.CDLL:
     L.awq_channel_stats.argtypes = [vp, i32, i64, i64, vp, vp, vp]
     L.awq_search_workspace_bytes.restype = sz
     L.awq_search_workspace_bytes.argtypes = [i32, i64, i64, i64, i32, i32]
+    L.awq_sweep_summary.restype = i32
+    L.awq_sweep_summary.argtypes = [vp, vp, vp, i32, vp, vp]
     L.awq_search_workspace_min_bytes.restype = sz
     L.awq_search_workspace_min_bytes.argtypes = [i32, i64, i64, i64, i32, i32]
     L.awq_search.restype = i32
@@ -152,6 +155,13 @@ def _check(code: int, where: str) -> None:
 def _need(t: torch.Tensor, name: str, ndim: int) -> None:
     if not t.is_cuda or not t.is_contiguous() or t.dim() != ndim:
         raise ValueError("%s must be a contiguous %d-D CUDA tensor" % (name, ndim))
+    # the library launches on the current device (and awq_search_noalloc uses
+    # that device's scratch array): tensors elsewhere would be read through
+    # pointers of another device
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError("%s is on %s but the current CUDA device is %d: call under "
+                         "torch.cuda.device(%s)" % (name, t.device, torch.cuda.current_device(),
+                                                    t.device))
 
 
 def new_status(device=None) -> torch.Tensor:
@@ -264,8 +274,9 @@ def awq_search_noalloc(W: torch.Tensor, X: torch.Tensor, bits: int = 4, group: O
     """``awq_search`` without a workspace: the library's fixed scratch array
     is used instead, so the C call allocates nothing.  Output tensors are
     still the caller's (pass ``out_tensors`` to reuse preallocated ones).
-    Problems whose workspace would exceed ``NOALLOC_SCRATCH_BYTES`` raise
-    AWQError with AWQ_ERR_UNSUPPORTED."""
+    Problems whose smallest workspace (``awq_search_workspace_min_bytes``)
+    would exceed ``NOALLOC_SCRATCH_BYTES`` raise AWQError with
+    AWQ_ERR_UNSUPPORTED."""
     _need(W, "W", 2)
     _need(X, "X", 2)
     if W.dtype != X.dtype or W.shape[1] != X.shape[1]:
@@ -312,20 +323,30 @@ def awq_output_power(W: torch.Tensor, X: torch.Tensor, workspace: Optional[torch
     return power
 
 
+def awq_sweep_summary(err: torch.Tensor, best: torch.Tensor, power: torch.Tensor, grid: int,
+                      stream=None) -> torch.Tensor:
+    """One sweep row from a search's (err, best) and the layer's output power:
+    float64 [5] = (alpha value, RTN error, AWQ error, RTN relative error, AWQ
+    relative error), computed on the device."""
+    row = torch.empty(5, dtype=torch.float64, device=err.device)
+    _check(lib.awq_sweep_summary(_ptr(err), _ptr(best), _ptr(power), grid, _ptr(row),
+                                 _stream(stream)), "awq_sweep_summary")
+    return row
+
+
 def awq_sweep(W: torch.Tensor, X: torch.Tensor, settings, sym: bool = True, grid: int = 20):
     """The search at several (bits, group) settings of one layer, with RTN
     (alpha = 0, the first grid point) beside AWQ and both errors also relative
     to mean((X W^T)^2).  ``group=None`` means one group per row.  Returns one
     dict per setting: bits, group, best (alpha index), alpha, err_rtn,
     err_awq, rel_rtn, rel_awq."""
-    power = float(awq_output_power(W, X).item())
+    power = awq_output_power(W, X)
     rows = []
     for bits, group in settings:
         err, best, _ = awq_search(W, X, bits=bits, group=group, sym=sym, grid=grid)
-        e = err.cpu().tolist()
-        b = int(best.item())
-        rows.append(dict(bits=bits, group=group, best=b, alpha=b / grid, err_rtn=e[0],
-                         err_awq=e[b], rel_rtn=e[0] / power, rel_awq=e[b] / power))
+        r = awq_sweep_summary(err, best, power, grid).cpu().tolist()
+        rows.append(dict(bits=bits, group=group, best=int(best.item()), alpha=r[0], err_rtn=r[1],
+                         err_awq=r[2], rel_rtn=r[3], rel_awq=r[4]))
     return rows
 
 

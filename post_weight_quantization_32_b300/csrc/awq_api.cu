@@ -282,6 +282,13 @@ int awq_output_power(const void* W, const void* X, int dtype, int64_t out, int64
   return cuda_status(e);
 }
 
+int awq_sweep_summary(const double* err, const int32_t* best, const double* power, int grid,
+                      double* row, awq_stream_t stream) {
+  const Range range("awq_sweep_summary");
+  if (!err || !best || !power || !row || grid < 1 || grid > kMaxGrid) return AWQ_ERR_INVALID_ARG;
+  return cuda_status(launch_sweep_summary(err, best, power, grid, row, (cudaStream_t)stream));
+}
+
 int awq_quantize_pack(const void* W, int dtype, int64_t out, int64_t in, const float* s, int bits,
                       int group, int sym, uint32_t* qweight, float* scales, uint8_t* zeros,
                       int32_t* dev_status, awq_stream_t stream) {

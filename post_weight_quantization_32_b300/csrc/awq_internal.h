@@ -118,6 +118,11 @@ cudaError_t launch_reduce_argmin(const double* partials, const double* unscale, 
                                  double* err, int32_t* best, float* s_best, int32_t* dev_status,
                                  cudaStream_t s);
 
+// row[0..4] = alpha value of best, err[0], err[best], err[0] / *power,
+// err[best] / *power (NaN where best < 0); one thread.
+cudaError_t launch_sweep_summary(const double* err, const int32_t* best, const double* power,
+                                 int grid, double* row, cudaStream_t s);
+
 // ---- the fused search (awq_search.cu)
 struct SearchPlan {
   int T;        // token tile (multiple of 32, <= 256) = MMA N

@@ -201,7 +201,31 @@ __global__ void __launch_bounds__(256) power_tables_kernel(int64_t out, int64_t 
   }
 }
 
+// One row of a bit-width / group-size sweep (one thread): the kept alpha's
+// value on the grid (linspace(0, 1, grid + 1)[best], R2 of the readings),
+// RTN's error (alpha = 0), AWQ's error, and both relative to the output power.
+__global__ void sweep_summary_kernel(const double* __restrict__ err, const int32_t* __restrict__ best,
+                                     const double* __restrict__ power, int grid,
+                                     double* __restrict__ row) {
+  pdl_wait();
+  const int b = *best;
+  const double nan = __longlong_as_double(0x7FF8000000000000ll);
+  const double p = *power;
+  const double e0 = err[0];
+  const double eb = b >= 0 ? err[b] : nan;
+  row[0] = b < 0 ? nan : (b == grid ? 1.0 : (double)b * (1.0 / (double)grid));
+  row[1] = e0;
+  row[2] = eb;
+  row[3] = e0 / p;
+  row[4] = eb / p;
+}
+
 }  // namespace
+
+cudaError_t launch_sweep_summary(const double* err, const int32_t* best, const double* power,
+                                 int grid, double* row, cudaStream_t s) {
+  return launch_pdl(sweep_summary_kernel, 1, 1, 0, s, err, best, power, grid, row);
+}
 
 cudaError_t launch_power_tables(int64_t out, int64_t in, const uint32_t* absmax, int x_scaled,
                                 float* s32, float* inv_s32, int32_t* pow2_s, double* unscale,

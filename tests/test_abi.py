@@ -231,3 +231,14 @@ def test_wait_limit_from_the_environment(monkeypatch):
     monkeypatch.setenv("AWQ_WAIT_LIMIT_MS", "250")
     o = awq._env_opts()
     assert o.wait_limit_ns == 250_000_000 and o.test_timeout == 0 and not o.diag
+
+
+def test_sweep_summary_rejects_bad_arguments_on_host(lib):
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    lib.awq_sweep_summary.restype = i32
+    lib.awq_sweep_summary.argtypes = [vp, vp, vp, i32, vp, vp]
+    fake = 1 << 20  # never dereferenced
+    assert lib.awq_sweep_summary(None, fake, fake, 20, fake, None) == 1
+    assert lib.awq_sweep_summary(fake, fake, fake, 0, fake, None) == 1
+    assert lib.awq_sweep_summary(fake, fake, fake, 5000, fake, None) == 1
+    assert lib.awq_sweep_summary(fake, fake, None, 20, fake, None) == 1

@@ -251,6 +251,8 @@ def test_sweep_matches_oracle(awq):
         label = (g["bits"], g["group"])
         if g["best"] != r["best"]:
             assert abs(r["errs"][g["best"]] - r["err_awq"]) <= TIE_RTOL * r["err_awq"], label
+        else:
+            assert g["alpha"] == r["alpha"], label
         for key in ("err_rtn", "rel_rtn"):
             assert abs(g[key] - r[key]) <= ERR_RTOL * r[key], (label, key, g[key], r[key])
         assert abs(g["rel_awq"] - r["rel_awq"]) <= (ERR_RTOL + TIE_RTOL) * r["rel_awq"], label

@@ -59,12 +59,29 @@ def test_noalloc_matches_workspace_search_twice(awq):
     _compare(awq, W2, X2, 4, 128, True, 20)
 
 
+def test_noalloc_at_the_edge_of_its_scratch(awq):
+    # 256 x 4096 bf16 with N = 4002 needs a workspace of just under the fixed
+    # array's 32 MiB (the fp16 copy of X dominates it); one token more is
+    # just over.  The first runs and matches the workspace search, the
+    # second is refused before anything is enqueued.
+    out, n_in, grid = 256, 4096, 20
+    need = awq.awq_search_workspace_min_bytes(torch.bfloat16, out, n_in, 4002, 128, grid)
+    assert awq.NOALLOC_SCRATCH_BYTES - 8192 < need <= awq.NOALLOC_SCRATCH_BYTES
+    assert awq.awq_search_workspace_min_bytes(torch.bfloat16, out, n_in, 4003, 128,
+                                              grid) > awq.NOALLOC_SCRATCH_BYTES
+    W, X = make_random_layer(out, n_in, 4003, dtype="bf16", seed=903, n_outlier=40)
+    _compare(awq, W, X[:4002].contiguous(), 4, 128, False, grid)
+    with pytest.raises(awq.AWQError) as ei:
+        awq.awq_search_noalloc(W.cuda(), X.cuda(), 4, 128, False, grid)
+    assert ei.value.code == 2   # AWQ_ERR_UNSUPPORTED
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch(awq):
     # 8192 x 28672 bf16 with N = 1024 needs far more than the fixed array;
     # the size check returns before anything is enqueued, so the tensors
     # passed here are never read.
     out, n_in, N, grid = 8192, 28672, 1024, 40
-    need = awq.awq_search_workspace_bytes(torch.bfloat16, out, n_in, N, 128, grid)
+    need = awq.awq_search_workspace_min_bytes(torch.bfloat16, out, n_in, N, 128, grid)
     assert need > awq.NOALLOC_SCRATCH_BYTES
     dummy = torch.empty(64, dtype=torch.uint8, device="cuda")
     p = dummy.data_ptr()
