@@ -171,6 +171,43 @@ int awq_output_power(const void* W, const void* X, int dtype,
                      double* power, int32_t* dev_status, awq_stream_t stream);
 
 /*
+ * awq_search_rows / awq_search_finish - the search split by output rows
+ * ["AWQ (activation-aware weight quantization)", "Source code": the error
+ * is a mean over every output entry, so it splits into sums over slices of
+ * the output rows; s depends on X alone, so every slice sees the same s].
+ *
+ * awq_search_rows runs the search on `rows` consecutive rows of a layer
+ * (W points at the first of them, [rows][in]); arguments as awq_search
+ * (workspace sized by awq_search_workspace_bytes(dtype, rows, in, N, group,
+ * grid)), except:
+ *   sums    [grid + 1] double (written)  per alpha, the sum over these rows
+ *           and all N tokens of (X (Wq - W)^T)^2, not divided by anything
+ *   s_table [grid + 1][in] float or NULL (written)  the centred scale
+ *           vector of every alpha, rounded to float32 (the same on every
+ *           slice: it depends on X only)
+ * awq_search_finish combines the slices' sums:
+ *   sums    [n_parts][grid + 1] double (read)  the slices' sums, in slice
+ *           order; they are added in that order, so the result does not
+ *           depend on which device or process produced which slice
+ *   N, out  tokens, and rows of the whole layer (the sum of the slices' rows)
+ *   s_table [grid + 1][in] float (read)  any slice's s_table
+ *   err, best, s_best  as awq_search's outputs for the whole layer
+ * A layer can be searched slice by slice on several devices: gather the
+ * slices' sums (every device the same, in slice order) and finish anywhere.
+ */
+int awq_search_rows(const void* W, const void* X, int dtype,
+                    int64_t rows, int64_t in, int64_t N,
+                    const double* sx, int bits, int group, int sym, int grid,
+                    void* workspace, size_t workspace_bytes,
+                    double* sums, float* s_table,
+                    int32_t* dev_status, awq_stream_t stream);
+
+int awq_search_finish(const double* sums, int n_parts, int grid, int64_t N, int64_t out,
+                      const float* s_table, int64_t in,
+                      double* err, int32_t* best, float* s_best,
+                      int32_t* dev_status, awq_stream_t stream);
+
+/*
  * awq_sweep_summary - one row of a bit-width / group-size sweep
  * ["AWQ (activation-aware weight quantization)", "What the simulations
  * show": RTN beside AWQ at each setting, as relative output errors;

@@ -44,6 +44,7 @@ __all__ = [
     "DTYPE", "awq_search_noalloc", "NOALLOC_SCRATCH_BYTES", "awq_output_power", "awq_sweep",
     "awq_export_checkpoint", "awq_clip_search", "awq_clip_search_workspace_bytes",
     "awq_quantize_pack_clipped", "awq_gptq", "awq_gptq_workspace_bytes", "awq_sweep_summary",
+    "awq_search_rows", "awq_search_finish", "gather_row_sums",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -58,7 +59,7 @@ EXPORTS = ("awq_status_string", "awq_channel_stats", "awq_search_workspace_bytes
            "awq_search_ex", "awq_quantize_pack", "awq_search_noalloc", "awq_output_power",
            "awq_export_checkpoint", "awq_clip_search", "awq_clip_search_workspace_bytes",
            "awq_quantize_pack_clipped", "awq_gptq", "awq_gptq_workspace_bytes",
-           "awq_sweep_summary")
+           "awq_sweep_summary", "awq_search_rows", "awq_search_finish")
 
 # Size of the library's fixed scratch array used by awq_search_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -75,6 +76,11 @@ def _load() -> ctypes.CDLL:
     L.awq_channel_stats.argtypes = [vp, i32, i64, i64, vp, vp, vp]
     L.awq_search_workspace_bytes.restype = sz
     L.awq_search_workspace_bytes.argtypes = [i32, i64, i64, i64, i32, i32]
+    L.awq_search_rows.restype = i32
+    L.awq_search_rows.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, i32, vp, sz, vp,
+                                  vp, vp, vp]
+    L.awq_search_finish.restype = i32
+    L.awq_search_finish.argtypes = [vp, i32, i32, i64, i64, vp, i64, vp, vp, vp, vp, vp]
     L.awq_sweep_summary.restype = i32
     L.awq_sweep_summary.argtypes = [vp, vp, vp, i32, vp, vp]
     L.awq_search_workspace_min_bytes.restype = sz
@@ -239,6 +245,68 @@ def awq_search(W: torch.Tensor, X: torch.Tensor, bits: int = 4, group: Optional[
     if check:
         check_status(st, "awq_search")
     return err, best, s_best
+
+
+def awq_search_rows(W_rows: torch.Tensor, X: torch.Tensor, bits: int = 4,
+                    group: Optional[int] = None, sym: bool = True, grid: int = 20,
+                    sx: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    stream=None, dev_status: Optional[torch.Tensor] = None, check: bool = True):
+    """The search on a slice of a layer's output rows; returns (sums [grid+1]
+    f64: per alpha the unnormalised sum of squared output errors over these
+    rows, s_table [grid+1, in] f32: every alpha's scale vector)."""
+    _need(W_rows, "W_rows", 2)
+    _need(X, "X", 2)
+    if W_rows.dtype != X.dtype or W_rows.shape[1] != X.shape[1]:
+        raise ValueError("W_rows and X must share dtype and the input dimension")
+    rows, n_in = W_rows.shape
+    N = X.shape[0]
+    g = n_in if group is None else int(group)
+    if workspace is None:
+        need = awq_search_workspace_bytes(W_rows.dtype, rows, n_in, N, g, grid)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=W_rows.device)
+    sums = torch.empty(grid + 1, dtype=torch.float64, device=W_rows.device)
+    s_table = torch.empty((grid + 1, n_in), dtype=torch.float32, device=W_rows.device)
+    st = dev_status if dev_status is not None else new_status(W_rows.device)
+    _check(lib.awq_search_rows(_ptr(W_rows), _ptr(X), DTYPE[W_rows.dtype], rows, n_in, N, _ptr(sx),
+                               bits, g, 1 if sym else 0, grid, _ptr(workspace), workspace.numel(),
+                               _ptr(sums), _ptr(s_table), _ptr(st), _stream(stream)),
+           "awq_search_rows")
+    if check:
+        check_status(st, "awq_search_rows")
+    return sums, s_table
+
+
+def awq_search_finish(sums: torch.Tensor, N: int, out: int, s_table: torch.Tensor,
+                      stream=None, dev_status: Optional[torch.Tensor] = None, check: bool = True):
+    """Whole-layer (err, best, s_best) from the slices' sums ([n_parts,
+    grid+1] f64, slice order), the layer's N and out, and any slice's s_table."""
+    _need(sums, "sums", 2)
+    _need(s_table, "s_table", 2)
+    n_parts, n_alpha = sums.shape
+    n_in = s_table.shape[1]
+    err = torch.empty(n_alpha, dtype=torch.float64, device=sums.device)
+    best = torch.empty(1, dtype=torch.int32, device=sums.device)
+    s_best = torch.empty(n_in, dtype=torch.float32, device=sums.device)
+    st = dev_status if dev_status is not None else new_status(sums.device)
+    _check(lib.awq_search_finish(_ptr(sums), n_parts, n_alpha - 1, N, out, _ptr(s_table), n_in,
+                                 _ptr(err), _ptr(best), _ptr(s_best), _ptr(st), _stream(stream)),
+           "awq_search_finish")
+    if check:
+        check_status(st, "awq_search_finish")
+    return err, best, s_best
+
+
+def gather_row_sums(sums: torch.Tensor, group=None) -> torch.Tensor:
+    """Every rank's row-slice sums ([grid+1] f64), stacked in rank order on
+    every rank ([world, grid+1]): the input of awq_search_finish when rank r
+    searched slice r.  Only moves data (torch.distributed.all_gather); the
+    sums are added in awq_search_finish, in rank order, so every rank gets
+    the same answer."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    parts = [torch.empty_like(sums) for _ in range(world)]
+    dist.all_gather(parts, sums.contiguous(), group=group)
+    return torch.stack(parts, 0)
 
 
 def awq_quantize_pack(W: torch.Tensor, s: torch.Tensor, bits: int = 4, group: Optional[int] = None,

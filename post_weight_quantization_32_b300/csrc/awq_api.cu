@@ -29,7 +29,7 @@ constexpr int kMaxGrid = 4096;
 // Byte offsets of the workspace regions of awq_search (each 256-aligned).
 struct WsLayout {
   size_t ctl, pow2, unscale, escale, xscale, inv_c, sx64, root, minmax, s32, inv_s32, ss32, xf16,
-      gext, gext_bytes, partials, total;
+      gext, gext_bytes, partials, sbest, total;
 };
 
 // xs: the pre-divided search (search_xs_eligible), which adds the scaled s
@@ -63,6 +63,7 @@ WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int group, int gr
   w.gext_bytes = search_needs_ranges(group, in) ? (size_t)n_alpha * out * (in / group) * 8 : 0;
   w.gext = take(w.gext_bytes);
   w.partials = take((size_t)n_alpha * n_tiles * 8);
+  w.sbest = take((size_t)in * 4);  // awq_search_rows: the reduction's kept-scale output
   w.total = o;
   return w;
 }
@@ -131,12 +132,19 @@ size_t awq_search_workspace_min_bytes(int dtype, int64_t out, int64_t in, int64_
   return search_workspace_min_bytes(dtype, out, in, N, group, grid);
 }
 
-int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
-                  const double* sx, int bits, int group, int sym, int grid, void* workspace,
-                  size_t workspace_bytes, double* err, int32_t* best, float* s_best,
-                  int32_t* dev_status, awq_stream_t stream, const awq_search_opts* opts) {
-  const Range range("awq_search_ex");
-  if (!W || !X || !workspace || !err || !best || !s_best || !dtype_ok(dtype))
+}  // extern "C"
+
+namespace {
+
+// The search; rows_mode: err receives the per-alpha sums over these rows,
+// unnormalised (denominator 1), best and s_best go to workspace scratch, and
+// s_table (if given) receives the per-alpha scale table.
+int search_impl(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
+                const double* sx, int bits, int group, int sym, int grid, void* workspace,
+                size_t workspace_bytes, double* err, int32_t* best, float* s_best,
+                int32_t* dev_status, awq_stream_t stream, const awq_search_opts* opts,
+                bool rows_mode, float* s_table) {
+  if (!W || !X || !workspace || !err || (!rows_mode && (!best || !s_best)) || !dtype_ok(dtype))
     return AWQ_ERR_INVALID_ARG;
   if (out < 1 || in < 1 || N < 1 || bits < 2 || bits > 8 || grid < 1 || grid > kMaxGrid ||
       group < 1 || in % group != 0)
@@ -223,9 +231,52 @@ int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t 
                     opts ? (cudaEvent_t)opts->ev_search_stop : nullptr);
   if (e == cudaErrorInvalidValue) return AWQ_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return AWQ_ERR_CUDA;
-  e = launch_reduce_argmin(partials, unscale, n_alpha, pl.n_tiles, (double)N * (double)out, s32,
-                           in, err, best, s_best, dev_status, s);
+  if (rows_mode) {
+    best = reinterpret_cast<int32_t*>(absmax + 3);
+    s_best = reinterpret_cast<float*>(wsb + ws.sbest);
+  }
+  e = launch_reduce_argmin(partials, unscale, n_alpha, pl.n_tiles,
+                           rows_mode ? 1.0 : (double)N * (double)out, s32, in, err, best, s_best,
+                           dev_status, s);
+  if (e == cudaSuccess && s_table)
+    e = cudaMemcpyAsync(s_table, s32, (size_t)n_alpha * in * sizeof(float),
+                        cudaMemcpyDeviceToDevice, s);
   return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int awq_search_ex(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
+                  const double* sx, int bits, int group, int sym, int grid, void* workspace,
+                  size_t workspace_bytes, double* err, int32_t* best, float* s_best,
+                  int32_t* dev_status, awq_stream_t stream, const awq_search_opts* opts) {
+  const Range range("awq_search_ex");
+  return search_impl(W, X, dtype, out, in, N, sx, bits, group, sym, grid, workspace,
+                     workspace_bytes, err, best, s_best, dev_status, stream, opts, false, nullptr);
+}
+
+int awq_search_rows(const void* W, const void* X, int dtype, int64_t rows, int64_t in, int64_t N,
+                    const double* sx, int bits, int group, int sym, int grid, void* workspace,
+                    size_t workspace_bytes, double* sums, float* s_table, int32_t* dev_status,
+                    awq_stream_t stream) {
+  const Range range("awq_search_rows");
+  return search_impl(W, X, dtype, rows, in, N, sx, bits, group, sym, grid, workspace,
+                     workspace_bytes, sums, nullptr, nullptr, dev_status, stream, nullptr, true,
+                     s_table);
+}
+
+int awq_search_finish(const double* sums, int n_parts, int grid, int64_t N, int64_t out,
+                      const float* s_table, int64_t in, double* err, int32_t* best, float* s_best,
+                      int32_t* dev_status, awq_stream_t stream) {
+  const Range range("awq_search_finish");
+  if (!sums || !s_table || !err || !best || !s_best || n_parts < 1 || grid < 1 ||
+      grid > kMaxGrid || N < 1 || out < 1 || in < 1)
+    return AWQ_ERR_INVALID_ARG;
+  return cuda_status(launch_search_finish(sums, n_parts, grid + 1, (double)N * (double)out, s_table,
+                                          in, err, best, s_best, dev_status,
+                                          (cudaStream_t)stream));
 }
 
 int awq_search(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,

@@ -123,6 +123,13 @@ cudaError_t launch_reduce_argmin(const double* partials, const double* unscale, 
 cudaError_t launch_sweep_summary(const double* err, const int32_t* best, const double* power,
                                  int grid, double* row, cudaStream_t s);
 
+// The finish of a row-split search: err[k] = (sum over parts p, in order,
+// of sums[p][k]) / denom, then best and s_best = s_table[best] as
+// launch_reduce_argmin.
+cudaError_t launch_search_finish(const double* sums, int parts, int n_alpha, double denom,
+                                 const float* s_table, int64_t in, double* err, int32_t* best,
+                                 float* s_best, int32_t* dev_status, cudaStream_t s);
+
 // ---- the fused search (awq_search.cu)
 struct SearchPlan {
   int T;        // token tile (multiple of 32, <= 256) = MMA N

@@ -109,6 +109,9 @@ __global__ void __launch_bounds__(kTabCols * kTabSlices) alpha_table_kernel(
 }
 
 // One CTA: per-alpha fixed-order sums, strict argmin, copy of the kept scales.
+// With parts > 0 (the finish of a row-split search) err_k is instead
+// sum_{p < parts} partials[p][k] / denom, added in part order, and unscale
+// is not read.
 __global__ void __launch_bounds__(1024) reduce_argmin_kernel(const double* __restrict__ partials,
                                                             const double* __restrict__ unscale,
                                                             int n_alpha, int n_tiles, double denom,
@@ -116,20 +119,30 @@ __global__ void __launch_bounds__(1024) reduce_argmin_kernel(const double* __res
                                                             int64_t in, double* __restrict__ err,
                                                             int32_t* __restrict__ best_out,
                                                             float* __restrict__ s_best,
-                                                            int32_t* dev_status) {
+                                                            int32_t* dev_status, int parts) {
   pdl_wait();
   pdl_trigger();
   __shared__ int best_sh;
   __shared__ double err_sh[kMaxGrid + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int k = warp; k < n_alpha; k += blockDim.x >> 5) {
-    double s = 0.0;
-    for (int t = lane; t < n_tiles; t += 32) s += __ldcg(partials + (int64_t)k * n_tiles + t);
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) {
-      const double e = s * unscale[k] / denom;
+  if (parts > 0) {
+    for (int k = threadIdx.x; k < n_alpha; k += blockDim.x) {
+      double s = 0.0;
+      for (int q = 0; q < parts; ++q) s += partials[(int64_t)q * n_alpha + k];
+      const double e = s / denom;
       err[k] = e;
       err_sh[k] = e;
+    }
+  } else {
+    for (int k = warp; k < n_alpha; k += blockDim.x >> 5) {
+      double s = 0.0;
+      for (int t = lane; t < n_tiles; t += 32) s += __ldcg(partials + (int64_t)k * n_tiles + t);
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) {
+        const double e = s * unscale[k] / denom;
+        err[k] = e;
+        err_sh[k] = e;
+      }
     }
   }
   __syncthreads();
@@ -270,7 +283,15 @@ cudaError_t launch_reduce_argmin(const double* partials, const double* unscale, 
                                  double* err, int32_t* best, float* s_best, int32_t* dev_status,
                                  cudaStream_t s) {
   return launch_pdl(reduce_argmin_kernel, 1, 1024, 0, s, partials, unscale, n_alpha, n_tiles, denom,
-                    s32, in, err, best, s_best, dev_status);
+                    s32, in, err, best, s_best, dev_status, 0);
+}
+
+cudaError_t launch_search_finish(const double* sums, int parts, int n_alpha, double denom,
+                                 const float* s_table, int64_t in, double* err, int32_t* best,
+                                 float* s_best, int32_t* dev_status, cudaStream_t s) {
+  if (n_alpha < 1 || n_alpha > kMaxGrid + 1 || parts < 1) return cudaErrorInvalidValue;
+  return launch_pdl(reduce_argmin_kernel, 1, 1024, 0, s, sums, static_cast<const double*>(nullptr),
+                    n_alpha, 0, denom, s_table, in, err, best, s_best, dev_status, parts);
 }
 
 }  // namespace awq

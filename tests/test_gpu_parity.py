@@ -465,3 +465,35 @@ def test_search_rejects_unsupported_group(awq):
     with pytest.raises(awq.AWQError) as ei:
         awq.awq_search(W.cuda(), X.cuda(), 4, 4, True, 20)
     assert ei.value.code == 2
+
+
+# ---------------------------------------------------------------- row split
+
+@pytest.mark.parametrize("cuts", [(128,), (64, 200), (1, 299)])
+def test_row_split_matches_whole_search(awq, cuts):
+    """The search run slice by slice over the output rows, then finished from
+    the slices' sums, gives the whole layer's errors, alpha and scales."""
+    out, n_in, N = 300, 512, 96
+    W, X = make_random_layer(out, n_in, N, dtype="bf16", seed=77, n_outlier=8)
+    Wd, Xd = _dev(W, X)
+    e_full, b_full, s_full = awq.awq_search(Wd, Xd, 4, 128, False, 20)
+    bounds = (0,) + tuple(cuts) + (out,)
+    parts, tables = [], []
+    for r0, r1 in zip(bounds[:-1], bounds[1:]):
+        sums, tab = awq.awq_search_rows(Wd[r0:r1].contiguous(), Xd, 4, 128, False, 20)
+        parts.append(sums)
+        tables.append(tab)
+    for tab in tables[1:]:
+        assert torch.equal(tab, tables[0])     # s depends on X alone
+    e, b, sb = awq.awq_search_finish(torch.stack(parts, 0), N, out, tables[0])
+    torch.cuda.synchronize()
+    e, e_full = e.cpu().numpy(), e_full.cpu().numpy()
+    # each slice scales its weight changes into fp16 by a power of two from
+    # its own max|W|, which moves the fp16 rounding of the smallest entries:
+    # the sums agree to about 1e-8, far inside the search's 2e-3
+    assert (np.abs(e - e_full) / e_full).max() <= 1e-6
+    b, bf = int(b.item()), int(b_full.item())
+    if b != bf:
+        assert abs(e_full[b] - e_full[bf]) <= TIE_RTOL * e_full[bf]
+    else:
+        assert torch.equal(sb, s_full)

@@ -597,6 +597,23 @@ def test_gptq_fits_each_group_on_the_corrected_weights():
     assert np.allclose(O.inverse_hessian_factor(X, 0.0) * np.sqrt(2.0), U, rtol=0, atol=1e-12)
 
 
+def test_error_splits_into_row_slices():
+    # err is a mean over every (token, output row) entry and s depends on X
+    # alone, so the search over slices of the output rows sums back to the
+    # whole layer's search: N out err = sum over slices of N rows_p err_p
+    rng = np.random.default_rng(15)
+    W = rng.normal(0, 0.02, size=(10, 64)).astype(np.float32)
+    X = rng.normal(size=(7, 64))
+    X[:, 5] *= 20.0
+    full = O.awq_search(W, X, bits=3, group=32, grid=8, sym=False)
+    parts = [O.awq_search(W[a:b], X, bits=3, group=32, grid=8, sym=False)
+             for a, b in ((0, 3), (3, 4), (4, 10))]
+    total = sum(p.errs * (b - a) for p, (a, b) in zip(parts, ((0, 3), (3, 4), (4, 10))))
+    assert np.allclose(total / 10, full.errs, rtol=1e-12, atol=0)
+    for p in parts:
+        assert np.array_equal(p.s32, full.s32)
+
+
 # --------------------------------------------------------------------------
 # Degenerate layers
 # --------------------------------------------------------------------------

@@ -60,17 +60,27 @@ def test_noalloc_matches_workspace_search_twice(awq):
 
 
 def test_noalloc_at_the_edge_of_its_scratch(awq):
-    # 256 x 4096 bf16 with N = 4002 needs a workspace of just under the fixed
-    # array's 32 MiB (the fp16 copy of X dominates it); one token more is
-    # just over.  The first runs and matches the workspace search, the
-    # second is refused before anything is enqueued.
+    # 256 x 4096 bf16 with the largest N whose workspace still fits the fixed
+    # array's 32 MiB (the fp16 copy of X dominates it; about 4000 tokens):
+    # it runs and matches the workspace search; one token more is refused
+    # before anything is enqueued.
     out, n_in, grid = 256, 4096, 20
-    need = awq.awq_search_workspace_min_bytes(torch.bfloat16, out, n_in, 4002, 128, grid)
-    assert awq.NOALLOC_SCRATCH_BYTES - 8192 < need <= awq.NOALLOC_SCRATCH_BYTES
-    assert awq.awq_search_workspace_min_bytes(torch.bfloat16, out, n_in, 4003, 128,
-                                              grid) > awq.NOALLOC_SCRATCH_BYTES
-    W, X = make_random_layer(out, n_in, 4003, dtype="bf16", seed=903, n_outlier=40)
-    _compare(awq, W, X[:4002].contiguous(), 4, 128, False, grid)
+
+    def need(N):
+        return awq.awq_search_workspace_min_bytes(torch.bfloat16, out, n_in, N, 128, grid)
+
+    lo, hi = 1, 1 << 16
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if need(mid) <= awq.NOALLOC_SCRATCH_BYTES:
+            lo = mid
+        else:
+            hi = mid - 1
+    n_edge = lo
+    assert awq.NOALLOC_SCRATCH_BYTES - 16384 < need(n_edge) <= awq.NOALLOC_SCRATCH_BYTES
+    assert need(n_edge + 1) > awq.NOALLOC_SCRATCH_BYTES
+    W, X = make_random_layer(out, n_in, n_edge + 1, dtype="bf16", seed=903, n_outlier=40)
+    _compare(awq, W, X[:n_edge].contiguous(), 4, 128, False, grid)
     with pytest.raises(awq.AWQError) as ei:
         awq.awq_search_noalloc(W.cuda(), X.cuda(), 4, 128, False, grid)
     assert ei.value.code == 2   # AWQ_ERR_UNSUPPORTED
