@@ -89,7 +89,8 @@ def build(verbose: bool = False, force: bool = False) -> str:
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             list(ex.map(lambda j: _compile(j[0], j[1], log), jobs))
     if jobs or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        cmd = [_nvcc()] + ARCH + ["-shared", "--cudart", "static", "-o", LIB] + objs
+        # cuBLAS serves GPTQ's plain GEMMs (dynamic: the CUDA toolkit's libcublas)
+        cmd = [_nvcc()] + ARCH + ["-shared", "--cudart", "static", "-o", LIB] + objs + ["-lcublas"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stdout + r.stderr)

@@ -9,7 +9,8 @@
 //   group's step and zero on the corrected weights; round column i with the
 //   float32 quantizer; err = (w - w_hat) / U[i][i]; w[:, j>i] -= err U[i][j]
 //
-// Everything runs in fp32 on the CUDA cores, in this order:
+// Everything runs in fp32 (the GEMMs in cuBLAS, float32 emulated on the
+// tensor cores; the rest on the CUDA cores), in this order:
 //  1. Xr = X / s with its columns reversed (Xr = Xs J, J the exchange matrix).
 //  2. A = 2 Xr^T Xr = J H J (a GEMM), dampened on its diagonal.
 //  3. A = M M^T, M lower (blocked right-looking Cholesky: a one-CTA factor of
@@ -25,6 +26,9 @@
 //     then applies the block's errors to all later columns.
 //  7. The codes are packed as awq_quantize_pack packs them.
 #include <algorithm>
+#include <mutex>
+
+#include <cublas_v2.h>
 
 #include "awq_device.cuh"
 #include "awq_internal.h"
@@ -34,69 +38,38 @@ namespace awq {
 namespace {
 
 // ---------------------------------------------------------------- fp32 GEMM
-// C[m][n] = alpha * sum_k A(m, k) B(k, n) + beta * C[m][n]; A(m, k) is
-// A[m * lda + k] (or A[k * lda + m] when ta), B(k, n) is B[k * ldb + n] (or
-// B[n * ldb + k] when tb).  64 x 64 tiles, 16-deep k steps, 4 x 4 outputs a
-// thread.
-constexpr int kGT = 64, kGK = 16;
+// C[m][n] = alpha * sum_k A(m, k) B(k, n) + beta * C[m][n] (row-major); A(m,
+// k) is A[m * lda + k] (or A[k * lda + m] when ta), B(k, n) is B[k * ldb + n]
+// (or B[n * ldb + k] when tb).  These are plain GEMMs, so they go to cuBLAS
+// with its float32 result emulated on the bf16 tensor cores (each float32
+// operand split into three bf16 parts, products accumulated in float32):
+// float32 accuracy at tensor-core speed.  cuBLAS is column-major: the
+// row-major product is computed as C^T = B^T A^T.
+std::mutex g_blas_mu;
+cublasHandle_t g_blas[64] = {nullptr};
 
-__global__ void __launch_bounds__(256) sgemm_kernel(int m, int n, int k, float alpha,
-                                                    const float* __restrict__ A, int64_t lda,
-                                                    int ta, const float* __restrict__ B,
-                                                    int64_t ldb, int tb, float beta,
-                                                    float* __restrict__ C, int64_t ldc) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ float as[kGK][kGT + 4], bs[kGK][kGT + 4];
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  const int m0 = blockIdx.y * kGT, n0 = blockIdx.x * kGT;
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < k; k0 += kGK) {
-    for (int i = threadIdx.x; i < kGK * kGT; i += 256) {
-      const int kk = i / kGT, mm = i % kGT;
-      const int gm = m0 + mm, gk = k0 + kk;
-      float a = 0.0f;
-      if (gm < m && gk < k) a = ta ? A[(int64_t)gk * lda + gm] : A[(int64_t)gm * lda + gk];
-      as[kk][mm] = a;
-      const int gn = n0 + mm;
-      float b = 0.0f;
-      if (gn < n && gk < k) b = tb ? B[(int64_t)gn * ldb + gk] : B[(int64_t)gk * ldb + gn];
-      bs[kk][mm] = b;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < kGK; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        a[r] = as[kk][ty * 4 + r];
-        b[r] = bs[kk][tx * 4 + r];
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
-    }
-    __syncthreads();
+cublasHandle_t blas_handle() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_blas_mu);
+  if (g_blas[dev] == nullptr) {
+    cublasHandle_t h = nullptr;
+    if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return nullptr;
+    g_blas[dev] = h;
   }
-#pragma unroll
-  for (int r = 0; r < 4; ++r)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int gm = m0 + ty * 4 + r, gn = n0 + tx * 4 + c;
-      if (gm < m && gn < n) {
-        float* p = C + (int64_t)gm * ldc + gn;
-        *p = beta == 0.0f ? alpha * acc[r][c] : fmaf(alpha, acc[r][c], beta * *p);
-      }
-    }
+  return g_blas[dev];
 }
 
 cudaError_t sgemm(cudaStream_t s, int m, int n, int k, float alpha, const float* A, int64_t lda,
                   int ta, const float* B, int64_t ldb, int tb, float beta, float* C, int64_t ldc) {
   if (m <= 0 || n <= 0 || k <= 0) return cudaSuccess;
-  const dim3 grid((unsigned)((n + kGT - 1) / kGT), (unsigned)((m + kGT - 1) / kGT));
-  return launch_pdl(sgemm_kernel, grid, dim3(256), 0, s, m, n, k, alpha, A, lda, ta, B, ldb, tb,
-                    beta, C, ldc);
+  cublasHandle_t h = blas_handle();
+  if (h == nullptr || cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+  const cublasStatus_t r =
+      cublasGemmEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, n, m, k,
+                   &alpha, B, CUDA_R_32F, (int)ldb, A, CUDA_R_32F, (int)lda, &beta, C, CUDA_R_32F,
+                   (int)ldc, CUBLAS_COMPUTE_32F_EMULATED_16BFX9, CUBLAS_GEMM_DEFAULT);
+  return r == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
 }
 
 // ------------------------------------------------------- inputs and Hessian
