@@ -158,13 +158,17 @@ int awq_search(const void* W, const void* X, int dtype,
  * entries), err / power is that ratio.
  *
  *   W, X, dtype, out, in, N   as for awq_search
- *   workspace, workspace_bytes >= awq_search_workspace_bytes(dtype, out,
- *                               in, N, in, 1) (one alpha, one group per row)
+ *   workspace, workspace_bytes >= awq_output_power_workspace_bytes(dtype,
+ *                               out, in, N) (256-byte aligned)
  *   power  [1] double (written)
- * The GEMM runs on the same tensor-core path as the search (fp16 operands
- * scaled by exact powers of two, fp32 accumulation, float64 sums in a fixed
- * order).  Requirements: in % 8 == 0, W and X 16-byte aligned.
+ * X W^T is a plain GEMM (cuBLAS on the tensor cores: 16-bit operands with
+ * float32 accumulation, float32 operands emulated to float32 accuracy)
+ * written to the workspace as float32; its squares are summed in float64 in
+ * a fixed order, so repeated calls give identical results.  dev_status is
+ * not written (a NaN or infinite product shows in power).
  */
+size_t awq_output_power_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N);
+
 int awq_output_power(const void* W, const void* X, int dtype,
                      int64_t out, int64_t in, int64_t N,
                      void* workspace, size_t workspace_bytes,

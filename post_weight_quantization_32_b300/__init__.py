@@ -59,7 +59,8 @@ EXPORTS = ("awq_status_string", "awq_channel_stats", "awq_search_workspace_bytes
            "awq_search_ex", "awq_quantize_pack", "awq_search_noalloc", "awq_output_power",
            "awq_export_checkpoint", "awq_clip_search", "awq_clip_search_workspace_bytes",
            "awq_quantize_pack_clipped", "awq_gptq", "awq_gptq_workspace_bytes",
-           "awq_sweep_summary", "awq_search_rows", "awq_search_finish")
+           "awq_sweep_summary", "awq_search_rows", "awq_search_finish",
+           "awq_output_power_workspace_bytes")
 
 # Size of the library's fixed scratch array used by awq_search_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -81,6 +82,8 @@ def _load() -> ctypes.CDLL:
                                   vp, vp, vp]
     L.awq_search_finish.restype = i32
     L.awq_search_finish.argtypes = [vp, i32, i32, i64, i64, vp, i64, vp, vp, vp, vp, vp]
+    L.awq_output_power_workspace_bytes.restype = sz
+    L.awq_output_power_workspace_bytes.argtypes = [i32, i64, i64, i64]
     L.awq_sweep_summary.restype = i32
     L.awq_sweep_summary.argtypes = [vp, vp, vp, i32, vp, vp]
     L.awq_search_workspace_min_bytes.restype = sz
@@ -379,7 +382,7 @@ def awq_output_power(W: torch.Tensor, X: torch.Tensor, workspace: Optional[torch
     n_out, n_in = W.shape
     N = X.shape[0]
     if workspace is None:
-        need = awq_search_workspace_bytes(W.dtype, n_out, n_in, N, n_in, 1)
+        need = int(lib.awq_output_power_workspace_bytes(DTYPE[W.dtype], n_out, n_in, N))
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=W.device)
     power = out if out is not None else torch.empty(1, dtype=torch.float64, device=W.device)
     st = dev_status if dev_status is not None else new_status(W.device)

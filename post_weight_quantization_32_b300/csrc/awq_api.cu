@@ -287,49 +287,32 @@ int awq_search(const void* W, const void* X, int dtype, int64_t out, int64_t in,
                        workspace_bytes, err, best, s_best, dev_status, stream, nullptr);
 }
 
+size_t awq_output_power_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N) {
+  if (!dtype_ok(dtype) || out < 1 || in < 1 || N < 1) return 0;
+  return align_up((size_t)N * out * sizeof(float), 256) + align_up(power_reduce_scratch_bytes(), 256);
+}
+
 int awq_output_power(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
                      void* workspace, size_t workspace_bytes, double* power, int32_t* dev_status,
                      awq_stream_t stream) {
   const Range range("awq_output_power");
+  (void)dev_status;  // no device-side errors: a NaN or infinite product shows in *power
   if (!W || !X || !workspace || !power || !dtype_ok(dtype)) return AWQ_ERR_INVALID_ARG;
   if (out < 1 || in < 1 || N < 1) return AWQ_ERR_INVALID_ARG;
-  // the workspace of a one-alpha search with one group per row
-  const WsLayout ws = ws_layout(dtype, out, in, N, (int)in, 1);
-  if (workspace_bytes < ws.total || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+  if (workspace_bytes < awq_output_power_workspace_bytes(dtype, out, in, N) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
     return AWQ_ERR_INVALID_ARG;
-  if (in % 8 != 0 || out > (1 << 24) || N > (1 << 24) || in > (1 << 24))
-    return AWQ_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(W) & 15) != 0 || (reinterpret_cast<uintptr_t>(X) & 15) != 0)
-    return AWQ_ERR_UNSUPPORTED;
+  if (out >= (1ll << 31) || N >= (1ll << 31) || in >= (1ll << 31)) return AWQ_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  uint32_t* ctl = reinterpret_cast<uint32_t*>(wsb + ws.ctl);
-  cudaError_t e = cudaMemsetAsync(ctl, 0, 8 * sizeof(uint32_t), s);
-  // max|W| (and max|X| for a bf16 / fp32 X) set the fp16 operand scalings
-  if (e == cudaSuccess) e = launch_absmax(W, dtype, out * in, ctl, s);
-  const bool x_copy = dtype != kDtF16;
-  if (e == cudaSuccess && x_copy) e = launch_absmax(X, dtype, N * in, ctl + 1, s);
-  if (e == cudaSuccess && x_copy) e = launch_to_f16(X, dtype, N * in, ctl + 1, wsb + ws.xf16, s);
-  float* s32 = reinterpret_cast<float*>(wsb + ws.s32);
-  float* inv_s32 = reinterpret_cast<float*>(wsb + ws.inv_s32);
-  int32_t* pow2_s = reinterpret_cast<int32_t*>(wsb + ws.pow2);
-  double* unscale = reinterpret_cast<double*>(wsb + ws.unscale);
-  // one float per row for the symmetric group maximum (the region holds two)
-  float* ext = reinterpret_cast<float*>(wsb + ws.gext);
+  // D = X W^T ([N][out] float32, a plain GEMM), then mean(D^2) in float64
+  float* D = reinterpret_cast<float*>(wsb);
+  void* scratch = wsb + align_up((size_t)N * out * sizeof(float), 256);
+  cudaError_t e = cudaMemsetAsync(scratch, 0, 256, s);
   if (e == cudaSuccess)
-    e = launch_power_tables(out, in, ctl, x_copy ? 1 : 0, s32, inv_s32, pow2_s, unscale, ext, s);
-  if (e != cudaSuccess) return AWQ_ERR_CUDA;
-  const void* xh = x_copy ? static_cast<const void*>(wsb + ws.xf16) : X;
-  const SearchPlan pl = plan_search(dtype, out, in, N, 1, (int)in, true, device_sm_count());
-  double* partials = reinterpret_cast<double*>(wsb + ws.partials);
-  e = launch_search(W, xh, dtype, out, in, N, 4, (int)in, 1, 1, s32, inv_s32, pow2_s, ext, nullptr,
-                    nullptr, partials, pl, 0, 0, dev_status, ctl + 4, s, nullptr, nullptr);
-  if (e == cudaErrorInvalidValue) return AWQ_ERR_UNSUPPORTED;
-  if (e != cudaSuccess) return AWQ_ERR_CUDA;
-  // the reduction's argmin and kept-scale outputs land in scratch words
-  e = launch_reduce_argmin(partials, unscale, 1, pl.n_tiles, (double)N * (double)out, s32, in,
-                           power, reinterpret_cast<int32_t*>(ctl + 3),
-                           reinterpret_cast<float*>(wsb + ws.sx64), dev_status, s);
+    e = blas_gemm(s, (int)N, (int)out, (int)in, 1.0f, X, in, 0, W, in, 1, 0.0f, D, out, dtype);
+  if (e == cudaSuccess)
+    e = launch_power_reduce(D, N * out, (double)N * (double)out, scratch, power, s);
   return cuda_status(e);
 }
 

@@ -45,6 +45,9 @@ namespace {
 // operand split into three bf16 parts, products accumulated in float32):
 // float32 accuracy at tensor-core speed.  cuBLAS is column-major: the
 // row-major product is computed as C^T = B^T A^T.
+}  // namespace
+
+namespace {
 std::mutex g_blas_mu;
 cublasHandle_t g_blas[64] = {nullptr};
 
@@ -59,17 +62,32 @@ cublasHandle_t blas_handle() {
   }
   return g_blas[dev];
 }
+}  // namespace
 
-cudaError_t sgemm(cudaStream_t s, int m, int n, int k, float alpha, const float* A, int64_t lda,
-                  int ta, const float* B, int64_t ldb, int tb, float beta, float* C, int64_t ldc) {
+cudaError_t blas_gemm(cudaStream_t s, int m, int n, int k, float alpha, const void* A, int64_t lda,
+                      int ta, const void* B, int64_t ldb, int tb, float beta, float* C, int64_t ldc,
+                      int dt) {
   if (m <= 0 || n <= 0 || k <= 0) return cudaSuccess;
   cublasHandle_t h = blas_handle();
   if (h == nullptr || cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+  const cudaDataType_t t = dt == kDtF16 ? CUDA_R_16F : (dt == kDtBF16 ? CUDA_R_16BF : CUDA_R_32F);
+  // 16-bit operands: their products are exact in float32 and accumulate in
+  // float32; float32 operands: float32 emulated on the bf16 tensor cores
+  const cublasComputeType_t ct =
+      dt == kDtF32 ? CUBLAS_COMPUTE_32F_EMULATED_16BFX9 : CUBLAS_COMPUTE_32F;
   const cublasStatus_t r =
       cublasGemmEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, n, m, k,
-                   &alpha, B, CUDA_R_32F, (int)ldb, A, CUDA_R_32F, (int)lda, &beta, C, CUDA_R_32F,
-                   (int)ldc, CUBLAS_COMPUTE_32F_EMULATED_16BFX9, CUBLAS_GEMM_DEFAULT);
+                   &alpha, B, t, (int)ldb, A, t, (int)lda, &beta, C, CUDA_R_32F, (int)ldc, ct,
+                   CUBLAS_GEMM_DEFAULT);
   return r == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
+namespace {
+
+
+cudaError_t sgemm(cudaStream_t s, int m, int n, int k, float alpha, const float* A, int64_t lda,
+                  int ta, const float* B, int64_t ldb, int tb, float beta, float* C, int64_t ldc) {
+  return blas_gemm(s, m, n, k, alpha, A, lda, ta, B, ldb, tb, beta, C, ldc, kDtF32);
 }
 
 // ------------------------------------------------------- inputs and Hessian

@@ -103,14 +103,6 @@ cudaError_t launch_alpha_table_xs(const double* sx, const double* root, const do
 // search reads.
 cudaError_t launch_x_over_s(const void* X, int dt, int64_t N, int64_t in, int n_alpha,
                             const float* xinv, void* xs, cudaStream_t s);
-// Tables for the output power mean((X W^T)^2) run as a one-alpha search:
-// s32 = 1, inv_s32 = 2^e with e from max|W| (absmax[0]), pow2_s[0] = 1,
-// unscale[0] = 2^-2(e + m_x) (m_x from absmax[1] when x_scaled), and a
-// symmetric group maximum of 2^120 for every row (ext[out]), so that every
-// code rounds to zero and the weight change is -W itself.
-cudaError_t launch_power_tables(int64_t out, int64_t in, const uint32_t* absmax, int x_scaled,
-                                float* s32, float* inv_s32, int32_t* pow2_s, double* unscale,
-                                float* ext, cudaStream_t s);
 // err[k] = unscale[k] * sum_t partials[k][t] / denom (fixed order),
 // best = strict-< argmin, s_best = s32[best].
 cudaError_t launch_reduce_argmin(const double* partials, const double* unscale, int n_alpha,
@@ -232,6 +224,23 @@ cudaError_t launch_gptq(const void* W, const void* X, int dt, int64_t out, int64
                         const float* s, int bits, int group, int sym, float damp, void* workspace,
                         uint32_t* qweight, float* scales, uint8_t* zeros, int32_t* dev_status,
                         cudaStream_t st);
+
+// ---- plain GEMMs (cuBLAS; awq_gptq.cu)
+// Row-major C[m][n] (float32) = alpha * A(m, k) B(k, n) + beta * C, A(m, k) =
+// A[m * lda + k] (or A[k * lda + m] when ta), B(k, n) = B[k * ldb + n] (or
+// B[n * ldb + k] when tb); A and B of dtype dt.  16-bit operands accumulate
+// in float32; float32 operands use float32 emulated on the bf16 tensor cores.
+cudaError_t blas_gemm(cudaStream_t s, int m, int n, int k, float alpha, const void* A, int64_t lda,
+                      int ta, const void* B, int64_t ldb, int tb, float beta, float* C, int64_t ldc,
+                      int dt);
+
+// ---- output power (awq_prep.cu)
+// *power = sum over the n floats of D of D^2 (float64, a fixed order: the
+// grid's threads' strided sums, each CTA's tree, then the CTAs in order) /
+// denom.  scratch: power_reduce_scratch_bytes(n), its first word zeroed.
+size_t power_reduce_scratch_bytes();
+cudaError_t launch_power_reduce(const float* D, int64_t n, double denom, void* scratch,
+                                double* power, cudaStream_t s);
 
 // ---- checkpoint export (awq_export.cu)
 // From quantize_pack's row-major outputs (bits divides 32, in % (32/bits) ==

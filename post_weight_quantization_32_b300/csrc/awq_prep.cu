@@ -188,32 +188,6 @@ __global__ void __launch_bounds__(1024) reduce_argmin_kernel(const double* __res
   }
 }
 
-// Tables of the output-power pass (see launch_power_tables).
-__global__ void __launch_bounds__(256) power_tables_kernel(int64_t out, int64_t in,
-                                                           const uint32_t* __restrict__ absmax,
-                                                           int x_scaled, float* __restrict__ s32,
-                                                           float* __restrict__ inv_s32,
-                                                           int32_t* __restrict__ pow2_s,
-                                                           double* __restrict__ unscale,
-                                                           float* __restrict__ ext) {
-  pdl_wait();
-  pdl_trigger();
-  const int e = pow2_exponent_for((double)__uint_as_float(absmax[0]));
-  const float es = ldexpf(1.0f, e);
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (int64_t j = i0; j < in; j += stride) {
-    s32[j] = 1.0f;
-    inv_s32[j] = es;
-  }
-  for (int64_t r = i0; r < out; r += stride) ext[r] = 0x1p120f;
-  if (i0 == 0) {
-    const int m_x = x_scaled ? pow2_exponent_for((double)__uint_as_float(absmax[1])) : 0;
-    pow2_s[0] = 1;
-    unscale[0] = ldexp(1.0, -2 * (e + m_x));
-  }
-}
-
 // One row of a bit-width / group-size sweep (one thread): the kept alpha's
 // value on the grid (linspace(0, 1, grid + 1)[best], R2 of the readings),
 // RTN's error (alpha = 0), AWQ's error, and both relative to the output power.
@@ -233,20 +207,58 @@ __global__ void sweep_summary_kernel(const double* __restrict__ err, const int32
   row[4] = eb / p;
 }
 
+// Sum of squares of D in a fixed order: each thread of a fixed grid adds
+// the entries it strides over, the CTA adds its threads in a tree, and the
+// last CTA to finish (a ticket) adds the CTAs' sums in order.
+constexpr int kPowBlocks = 512;
+__global__ void __launch_bounds__(256) power_reduce_kernel(const float* __restrict__ D, int64_t n,
+                                                           double denom, uint32_t* ticket,
+                                                           double* __restrict__ part,
+                                                           double* __restrict__ power) {
+  pdl_wait();
+  pdl_trigger();
+  double acc = 0.0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const double v = (double)D[i];
+    acc = fma(v, v, acc);
+  }
+  __shared__ double red[256];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  __shared__ bool last;
+  if (threadIdx.x == 0) {
+    part[blockIdx.x] = red[0];
+    __threadfence();
+    last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (last && threadIdx.x == 0) {
+    __threadfence();
+    double s = 0.0;
+    for (unsigned b = 0; b < gridDim.x; ++b) s += __ldcg(part + b);
+    *power = s / denom;
+  }
+}
+
 }  // namespace
+
+size_t power_reduce_scratch_bytes() { return 256 + (size_t)kPowBlocks * 8; }
+
+cudaError_t launch_power_reduce(const float* D, int64_t n, double denom, void* scratch,
+                                double* power, cudaStream_t s) {
+  uint8_t* b = static_cast<uint8_t*>(scratch);
+  return launch_pdl(power_reduce_kernel, kPowBlocks, 256, 0, s, D, n, denom,
+                    reinterpret_cast<uint32_t*>(b), reinterpret_cast<double*>(b + 256), power);
+}
 
 cudaError_t launch_sweep_summary(const double* err, const int32_t* best, const double* power,
                                  int grid, double* row, cudaStream_t s) {
   return launch_pdl(sweep_summary_kernel, 1, 1, 0, s, err, best, power, grid, row);
-}
-
-cudaError_t launch_power_tables(int64_t out, int64_t in, const uint32_t* absmax, int x_scaled,
-                                float* s32, float* inv_s32, int32_t* pow2_s, double* unscale,
-                                float* ext, cudaStream_t s) {
-  const int64_t n = std::max(out, in);
-  const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 1024);
-  return launch_pdl(power_tables_kernel, grid, 256, 0, s, out, in, absmax, x_scaled, s32, inv_s32,
-                    pow2_s, unscale, ext);
 }
 
 size_t prep_chunks(int64_t in) { return (size_t)((in + 31) / 32); }  // the finer of the two chunkings

@@ -152,8 +152,11 @@ def test_output_power_rejects_bad_arguments_on_host(lib):
     lib.awq_output_power.restype = i32
     lib.awq_output_power.argtypes = [vp, vp, i32, i64, i64, i64, vp, sz, vp, vp, vp]
     f = 1 << 20   # never dereferenced
-    need = _ws(lib, 2, 64, 256, 16, 256, 1)
-    assert need > 0
+    lib.awq_output_power_workspace_bytes.restype = sz
+    lib.awq_output_power_workspace_bytes.argtypes = [i32, i64, i64, i64]
+    need = lib.awq_output_power_workspace_bytes(2, 64, 256, 16)
+    assert need >= 16 * 64 * 4 and need % 256 == 0   # the float32 product X W^T and a scratch
+    assert lib.awq_output_power_workspace_bytes(7, 64, 256, 16) == 0
     ok = dict(W=f, X=f, dt=2, out=64, n_in=256, N=16, ws=f, wsb=need, p=f)
 
     def call(**kw):
@@ -165,8 +168,6 @@ def test_output_power_rejects_bad_arguments_on_host(lib):
     assert call(W=None) == 1 and call(p=None) == 1
     assert call(N=0) == 1 and call(out=0) == 1 and call(dt=7) == 1
     assert call(wsb=need - 1) == 1 and call(ws=f + 16) == 1
-    assert call(n_in=252, wsb=1 << 30) == 2     # in % 8 != 0: no tensor-map rows
-    assert call(X=f + 8) == 2                    # TMA needs 16-byte aligned rows
 
 
 def test_clip_search_rejects_bad_arguments_on_host(lib):
