@@ -542,6 +542,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
+          if constexpr (XS) {
+            // pass 2 reads no table: with one alpha per unit the stages are
+            // free once pass 1 has read the weights and s
+            __syncwarp();
+            if (lane == 0)
+              for (int kbi = 0; kbi < KBJ; ++kbi)
+                mbar_arrive(smem_addr(&c.w_empty[wg * hw + (wm + kbi) % hw]));
+          }
           // group steps
           float scl[NG], rcp[NG], chi[NG];
           if constexpr (GV) {
@@ -609,10 +617,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         // every alpha of the job is done with these stages (weights and tables)
-        __syncwarp();
-        if (lane == 0)
-          for (int kbi = 0; kbi < KBJ; ++kbi)
-            mbar_arrive(smem_addr(&c.w_empty[wg * hw + (wm + kbi) % hw]));
+        if constexpr (!XS) {
+          __syncwarp();
+          if (lane == 0)
+            for (int kbi = 0; kbi < KBJ; ++kbi)
+              mbar_arrive(smem_addr(&c.w_empty[wg * hw + (wm + kbi) % hw]));
+        }
         wm += KBJ;
       }
     }
