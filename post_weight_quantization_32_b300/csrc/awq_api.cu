@@ -24,11 +24,10 @@ int device_sm_count() {
 
 namespace {
 
-constexpr int kMaxGrid = 4096;
 
 // Byte offsets of the workspace regions of awq_search (each 256-aligned).
 struct WsLayout {
-  size_t ctl, pow2, unscale, escale, xscale, inv_c, sx64, root, minmax, s32, inv_s32, ss32, xf16,
+  size_t ctl, pow2, unscale, escale, qk, sx64, u64, minmax, s32, inv_s32, ss32, xf16,
       gext, gext_bytes, partials, sbest, total;
 };
 
@@ -45,14 +44,15 @@ WsLayout ws_layout(int dt, int64_t out, int64_t in, int64_t N, int group, int gr
     o = align_up(o + bytes, 256);
     return at;
   };
-  w.ctl = take(8 * sizeof(uint32_t));  // max|W|, max|X| bits, a ticket; 4 words of wait diagnostics
+  // max|W|, max|X| bits, a ticket, the kept alpha (row split), 4 words of
+  // wait diagnostics
+  w.ctl = take(8 * sizeof(uint32_t));
   w.pow2 = take((size_t)n_alpha * 4);
   w.unscale = take((size_t)n_alpha * 8);
   w.escale = take((size_t)n_alpha * 4);
-  w.xscale = take((size_t)n_alpha * 4);
-  w.inv_c = take((size_t)n_alpha * 8);
+  w.qk = take((size_t)n_alpha * 8);
   w.sx64 = take((size_t)in * 8);
-  w.root = take((size_t)in * 8);                   // s_X ^ (1 / grid)
+  w.u64 = take((size_t)n_alpha * in * 8);          // s_X ^ (k / grid)
   w.minmax = take(prep_chunks(in) * 32);           // per-chunk extremes of s_X with their roots
   w.s32 = take((size_t)n_alpha * in * 4);
   w.inv_s32 = take((size_t)n_alpha * in * 4);
@@ -114,8 +114,7 @@ int awq_channel_stats(const void* X, int dtype, int64_t N, int64_t in, double* s
   (void)dev_status;  // no device-side errors in this kernel
   if (!X || !sx || !dtype_ok(dtype) || N < 1 || in < 1) return AWQ_ERR_INVALID_ARG;
   return cuda_status(
-      launch_channel_stats(X, dtype, N, in, sx, nullptr, nullptr, 0, nullptr, CentreArgs{},
-                           (cudaStream_t)stream));
+      launch_channel_stats(X, dtype, N, in, sx, nullptr, CentreArgs{}, (cudaStream_t)stream));
 }
 
 size_t awq_search_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N, int group,
@@ -178,42 +177,38 @@ int search_impl(const void* W, const void* X, int dtype, int64_t out, int64_t in
   const bool x_copy = dtype != kDtF16 && !xs;
   const bool need_xmax = x_copy || xs;
   float* ss32 = xs ? reinterpret_cast<float*>(wsb + ws.ss32) : nullptr;
+  float* escale = reinterpret_cast<float*>(wsb + ws.escale);
+  double* qk = reinterpret_cast<double*>(wsb + ws.qk);
   CentreArgs ca{};
   ca.grid = grid;
-  ca.x_scaled = x_copy ? 1 : 0;
-  ca.xs = xs ? 1 : 0;
-  ca.xscale = reinterpret_cast<float*>(wsb + ws.xscale);
-  ca.root = reinterpret_cast<double*>(wsb + ws.root);
+  ca.u = reinterpret_cast<double*>(wsb + ws.u64);
   ca.minmax = reinterpret_cast<double*>(wsb + ws.minmax);
-  ca.ticket = absmax + 2;
-  ca.absmax = absmax;
-  ca.inv_c = reinterpret_cast<double*>(wsb + ws.inv_c);
-  ca.escale = reinterpret_cast<float*>(wsb + ws.escale);
-  ca.unscale = unscale;
   ca.pow2_s = pow2_s;
-  // One launch: channel statistics, max|W| (and max|X| when it sets a
-  // scaling), sx^(1/grid) and, in its last CTA, the per-alpha centring
-  // values.  Then either a bf16 / fp32 X is copied to fp16 (scaled by a
-  // power of two) for the tensor cores, or, in the pre-divided mode, the
-  // n_alpha fp16 copies of X / s are formed after the tables.
+  // The statistics launch: s_X (unless given), max|X| where it sets a
+  // scaling, every column's powers s_X^(k / grid) and the chunk extremes of
+  // s_X.  Then one launch streams W for max|W| -- in the pre-divided mode
+  // forming the s table and the n_alpha fp16 copies of X / s meanwhile --
+  // and a table launch folds max|W| and max|X| into the power-of-two
+  // scalings.  A bf16 / fp32 X is copied to fp16 (scaled by a power of two)
+  // for the tensor cores.
   const double* sxp = sx;
   if (!sxp) {
     e = launch_channel_stats(X, dtype, N, in, reinterpret_cast<double*>(wsb + ws.sx64),
-                             need_xmax ? absmax + 1 : nullptr, W, out * in, absmax, ca, s);
+                             need_xmax ? absmax + 1 : nullptr, ca, s);
     sxp = reinterpret_cast<const double*>(wsb + ws.sx64);
   } else {
-    e = launch_absmax(W, dtype, out * in, absmax, s);
-    if (e == cudaSuccess && need_xmax) e = launch_absmax(X, dtype, N * in, absmax + 1, s);
+    if (need_xmax) e = launch_absmax(X, dtype, N * in, absmax + 1, s);
     if (e == cudaSuccess) e = launch_alpha_root(sxp, in, ca, s);
   }
+  if (e == cudaSuccess)
+    e = launch_wmax_xs(W, dtype, out * in, absmax, X, N, in, grid, ca.u, ca.minmax, absmax + 1, s32,
+                       qk, pow2_s, xs ? wsb + ws.xf16 : nullptr, s);
   if (e == cudaSuccess && x_copy) e = launch_to_f16(X, dtype, N * in, absmax + 1, wsb + ws.xf16, s);
-  if (e == cudaSuccess && xs) {
-    e = launch_alpha_table_xs(sxp, ca.root, ca.inv_c, ca.escale, ca.xscale, in, grid, s32, inv_s32,
-                              ss32, pow2_s, s);
-    if (e == cudaSuccess) e = launch_x_over_s(X, dtype, N, in, n_alpha, inv_s32, wsb + ws.xf16, s);
-  } else if (e == cudaSuccess) {
-    e = launch_alpha_table(sxp, ca.root, ca.inv_c, ca.escale, in, grid, s32, inv_s32, pow2_s, s);
-  }
+  if (e == cudaSuccess && xs)
+    e = launch_scale_table_xs(s32, qk, absmax, in, grid, ss32, escale, unscale, s);
+  else if (e == cudaSuccess)
+    e = launch_alpha_table(ca.u, ca.minmax, absmax, x_copy ? 1 : 0, in, grid, s32, inv_s32, escale,
+                           unscale, pow2_s, s);
   if (e == cudaSuccess && gext)
     e = launch_group_extremes(W, dtype, out, in, s32, n_alpha, group, sym, gext, s);
   if (e != cudaSuccess) return AWQ_ERR_CUDA;
@@ -224,7 +219,7 @@ int search_impl(const void* W, const void* X, int dtype, int64_t out, int64_t in
                   device_sm_count(), xs);
   double* partials = reinterpret_cast<double*>(wsb + ws.partials);
   e = launch_search(W, xh, dtype, out, in, N, bits, group, sym ? 1 : 0, n_alpha, s32, inv_s32,
-                    pow2_s, gext, ss32, xs ? ca.escale : nullptr, partials, pl,
+                    pow2_s, gext, ss32, xs ? escale : nullptr, partials, pl,
                     opts ? opts->wait_limit_ns : 0,
                     opts ? opts->test_timeout : 0, dev_status, diag, s,
                     opts ? (cudaEvent_t)opts->ev_search_start : nullptr,

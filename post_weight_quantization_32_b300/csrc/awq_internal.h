@@ -34,42 +34,43 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// Largest alpha grid (grid + 1 alphas) the C ABI accepts.
+constexpr int kMaxGrid = 4096;
+
 // ---- statistics and conversions (awq_stats.cu)
-// Where the per-alpha centring values go, for a launch that also forms them
-// (grid == 0: none).  root[j] = sx[j] ^ (1 / grid); minmax holds each CTA
-// chunk's max and min of sx with their roots (4 doubles per chunk,
-// prep_chunks(in) chunks at most); ticket is a
-// zeroed counter; absmax = {max|W|, max|X|} as float bits (max|X| is used
-// when x_scaled, i.e. X is copied to fp16 with a power-of-two scaling);
-// inv_c, escale, unscale, pow2_s have grid + 1 entries.
-// With xs != 0 (the pre-divided search mode) the fp16 scalings are split:
-// escale[k] = 2^e_k scales the weights (t = w * s * 2^e_k), xscale[k] =
-// 2^m_k scales X / s, unscale[k] = 2^-2(e_k + m_k), and absmax[1] must hold
-// max|X| whatever X's dtype.
+// Where a statistics (or root) launch puts what the table launches need
+// (grid == 0: nothing).  u[k][j] = s_X[j]^(k / grid) for k = 0..grid
+// (float64, [grid + 1][in]; exactly 1 at k = 0 and s_X at k = grid);
+// minmax holds each 32-column chunk's max and min of s_X with their roots
+// s_X^(1 / grid) (4 words per chunk, prep_chunks(in) chunks); pow2_s[k] is
+// set to 1 for k = 0..grid (the table launches clear it).
 struct CentreArgs {
   int grid;
-  int x_scaled;
-  int xs;
-  float* xscale;
-  double* root;
+  double* u;
   double* minmax;
-  uint32_t* ticket;
-  const uint32_t* absmax;
-  double* inv_c;
-  float* escale;
-  double* unscale;
   int32_t* pow2_s;
 };
 
 // sx[j] = sum_n |X[n, j]| / N + 1e-8, float64.  With xmax != nullptr the same
-// pass folds max|X| into *xmax (any dtype), and with W != nullptr the same launch folds
-// max|W| (nW values) into *wmax (bits of non-negative floats; both words must
-// start at 0; needs in % 8 == 0, nW % 8 == 0 and 16-byte aligned X and W).
-// With ca.grid != 0 the launch also writes ca.root and, once every CTA is
-// done, the centring values (needs the same vector conditions).
+// pass folds max|X| into *xmax (bits of a non-negative float; must start at
+// 0).  With ca.grid != 0 the launch also writes the powers and chunk
+// extremes of CentreArgs (needs in % 8 == 0 and a 16-byte aligned X, as
+// does xmax).  The launch lets the next one in the stream start
+// (programmatic dependent launch) as soon as its CTAs have read X.
 cudaError_t launch_channel_stats(const void* X, int dt, int64_t N, int64_t in, double* sx,
-                                 uint32_t* xmax, const void* W, int64_t nW, uint32_t* wmax,
-                                 const CentreArgs& ca, cudaStream_t s);
+                                 uint32_t* xmax, const CentreArgs& ca, cudaStream_t s);
+// Fold max|W| (nW values, nW % 8 == 0, 16-byte aligned) into *wmax, and
+// finish only after the launch before it in the stream.  With xs != nullptr
+// the same launch forms the pre-divided search's table and X copies once
+// that earlier launch is done: for k = 0..grid, s32[k][j] = fp32(u[k][j] *
+// ic_k) (ic_k the centring of alpha k from the chunk extremes), qk[k] (see
+// launch_alpha_table), and xs[k][n][j] = fp16(X[n][j] * 2^m_k / s32[k][j])
+// (m_k from max|X| in xmax_bits; X of dtype dt, in % 8 == 0, 16-byte
+// aligned); pow2_s[k] is cleared when some s32[k][j] is not a power of two.
+cudaError_t launch_wmax_xs(const void* W, int dt, int64_t nW, uint32_t* wmax, const void* X,
+                           int64_t N, int64_t in, int grid, const double* u,
+                           const double* minmax, const uint32_t* xmax_bits, float* s32,
+                           double* qk, int32_t* pow2_s, void* xs, cudaStream_t s);
 // *out = max(*out, bits of max_i |p[i]|); *out must start at 0.
 cudaError_t launch_absmax(const void* p, int dt, int64_t n, uint32_t* out, cudaStream_t s);
 // dst = fp16(X * 2^m) with m = pow2_exponent_for(max|X|) read from *xmax_bits;
@@ -78,31 +79,27 @@ cudaError_t launch_to_f16(const void* X, int dt, int64_t n, const uint32_t* xmax
                           cudaStream_t s);
 
 // ---- alpha tables, reduction and argmin (awq_prep.cu)
-// Column chunks of the statistics / root launches: minmax needs
-// 4 * prep_chunks(in) doubles.
+// Column chunks of the statistics / root launches (32 columns each):
+// minmax needs 4 * prep_chunks(in) words.
 size_t prep_chunks(int64_t in);
-// ca.root and the centring values (see CentreArgs) from a given sx.
+// The powers and chunk extremes of CentreArgs from a given sx.
 cudaError_t launch_alpha_root(const double* sx, int64_t in, const CentreArgs& ca, cudaStream_t s);
-// For k = 0..grid: s = sx^alpha_k * inv_c[k], as the running product of
-// root = sx^(1/grid) (exactly sx at k = grid), written as float32 s32[k][j],
-// and inv_s32[k][j] = escale[k] / s32[k][j], where escale[k] = 2^e_k scales
-// the weight changes of alpha k into the fp16 range of the error GEMM.
+// For k = 0..grid: s32[k][j] = fp32(u[k][j] * ic_k), where ic_k = 1 /
+// sqrt(max(s_k) * min(s_k)) comes from the chunk extremes, and inv_s32[k][j]
+// = escale[k] / s32[k][j]; escale[k] = 2^e_k (which scales the weight
+// changes of alpha k into the fp16 range of the error GEMM) and unscale[k]
+// are formed from qk = sqrt(max(s_k) / min(s_k)) and the max|W|, max|X|
+// bits in absmax (X copied to fp16 with a scaling when x_scaled).
 // pow2_s[k] (1 on entry) ends nonzero iff every s32[k][j] is a power of two.
-cudaError_t launch_alpha_table(const double* sx, const double* root, const double* inv_c,
-                               const float* escale, int64_t in, int grid, float* s32,
-                               float* inv_s32, int32_t* pow2_s, cudaStream_t s);
-// The pre-divided mode's tables: as launch_alpha_table, but inv_s32[k][j] =
-// xscale[k] / s32[k][j] (the factor X is multiplied by) and ss32[k][j] =
-// s32[k][j] * escale[k] (exact: a power of two).
-cudaError_t launch_alpha_table_xs(const double* sx, const double* root, const double* inv_c,
-                                  const float* escale, const float* xscale, int64_t in, int grid,
-                                  float* s32, float* inv_s32, float* ss32, int32_t* pow2_s,
-                                  cudaStream_t s);
-// xs[k][n][j] = fp16(X[n][j] * xinv[k][j]) for k < n_alpha (X of dtype dt,
-// in % 8 == 0, 16-byte aligned): the n_alpha copies of X / s the pre-divided
-// search reads.
-cudaError_t launch_x_over_s(const void* X, int dt, int64_t N, int64_t in, int n_alpha,
-                            const float* xinv, void* xs, cudaStream_t s);
+cudaError_t launch_alpha_table(const double* u, const double* minmax, const uint32_t* absmax,
+                               int x_scaled, int64_t in, int grid, float* s32, float* inv_s32,
+                               float* escale, double* unscale, int32_t* pow2_s, cudaStream_t s);
+// The pre-divided mode's scalings, after launch_wmax_xs: ss32[k][j] =
+// s32[k][j] * escale[k] (exact: a power of two), and escale[k], unscale[k]
+// from qk[k] and the max|W|, max|X| bits in absmax.
+cudaError_t launch_scale_table_xs(const float* s32, const double* qk, const uint32_t* absmax,
+                                  int64_t in, int grid, float* ss32, float* escale,
+                                  double* unscale, cudaStream_t s);
 // err[k] = unscale[k] * sum_t partials[k][t] / denom (fixed order),
 // best = strict-< argmin, s_best = s32[best].
 cudaError_t launch_reduce_argmin(const double* partials, const double* unscale, int n_alpha,

@@ -5,8 +5,8 @@
 // ("AWQ (activation-aware weight quantization)", "The code, line by line",
 //  bullets on the grid and on centring), all in float64, then rounded to
 // float32 for the quantizer.  Float64 transcendentals are costly on this
-// GPU, so the table entries are running products of s_X^(1/grid): one
-// float64 multiplication per entry, within a few float64 ulps of the power,
+// GPU, so the powers are running products of s_X^(1/grid) (write_powers):
+// one float64 product per entry, within a few float64 ulps of the power,
 // far below the float32 rounding that follows.
 //
 // err_k = sum of the search's per-tile partial sums / (N * out), times the
@@ -25,87 +25,93 @@ namespace awq {
 
 namespace {
 
-constexpr int kPrepChunk = 64;   // columns per CTA of the per-column kernels
-constexpr int kMaxGrid = 4096;   // largest grid the C ABI accepts
+constexpr int kPrepChunk = kChunkCols;  // columns per CTA of the root launch (one chunk)
 
-// grid = chunks: root[j] = sx[j] ^ (1 / grid) in float64 and each chunk's
-// max and min of sx; the last CTA to finish reduces the chunk extremes and
-// forms the per-alpha centring values.  (The statistics launch does the same
-// when it computes sx itself; this kernel serves a caller-given sx.)
-__global__ void __launch_bounds__(kPrepChunk) alpha_root_kernel(const double* __restrict__ sx,
-                                                               int64_t in, CentreArgs ca) {
+// CTA b: root r = sx^(1 / grid) in float64 of the 32 columns 32 b .. 32 b +
+// 31 (warp 0), the chunk's max and min of sx with their roots, and the
+// columns' powers u[k][j] = sx^(k / grid) (write_powers, warps 0..3); CTA 0
+// sets pow2_s[k] = 1.  (The statistics launch does the same when it
+// computes sx itself; this kernel serves a caller-given sx.)
+__global__ void __launch_bounds__(128) alpha_root_kernel(const double* __restrict__ sx, int64_t in,
+                                                        CentreArgs ca) {
   pdl_wait();
   pdl_trigger();
-  SxExt x;
-  x.init();
-  const int64_t j = (int64_t)blockIdx.x * kPrepChunk + threadIdx.x;
-  if (j < in) {
-    const double v = sx[j];
-    const double r = exp(log(v) / (double)ca.grid);
-    ca.root[j] = r;
-    x.take(v, r);
+  __shared__ double sh_v[kPrepChunk], sh_r[kPrepChunk];
+  if (blockIdx.x == 0)
+    for (int k = threadIdx.x; k <= ca.grid; k += blockDim.x) ca.pow2_s[k] = 1;
+  if (threadIdx.x < kPrepChunk) {
+    SxExt x;
+    x.init();
+    const int64_t j = (int64_t)blockIdx.x * kPrepChunk + threadIdx.x;
+    if (j < in) {
+      const double v = sx[j];
+      const double r = exp(log(v) / (double)ca.grid);
+      sh_v[threadIdx.x] = v;
+      sh_r[threadIdx.x] = r;
+      x.take(v, r);
+    }
+    x.warp_merge();
+    if (threadIdx.x == 0) x.store(ca.minmax + 4 * blockIdx.x);
   }
-  __shared__ SxExt sext[kPrepChunk / 32];
-  x.warp_merge();
-  if ((threadIdx.x & 31) == 0) sext[threadIdx.x >> 5] = x;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < kPrepChunk / 32; ++w) x.merge(sext[w]);
-    x.store(ca.minmax + 4 * blockIdx.x);
-  }
-  centre_if_last(ca, gridDim.x);
+  write_powers(sh_v, sh_r, (int64_t)blockIdx.x * kPrepChunk, in, ca.grid, ca.u);
 }
 
-// One CTA per kTabCols columns; warp q of the CTA takes the alphas k = q,
-// q + kTabSlices, q + 2 kTabSlices, ... of every column, so the float64
-// product chains are kTabSlices times shorter than one chain per column.
-// s_k = sx ^ (k / grid) = root^k: root^q by binary powering, then running
-// products by root^kTabSlices (exactly 1 at k = 0 and exactly sx at
-// k = grid), centred, rounded to float32; inv_s32 = 2^e_k / s.  pow2_s[k]
-// is cleared when some entry of the chunk is not a power of two (a bit per
-// alpha in shared memory, applied once per alpha at the end).
-constexpr int kTabCols = 32, kTabSlices = 4;
-
-//
-// With ss32 != nullptr (the pre-divided search): inv_s32[k][j] = xscale[k] /
-// s32 (the factor X is multiplied by) and ss32[k][j] = s32 * escale[k].
-__global__ void __launch_bounds__(kTabCols * kTabSlices) alpha_table_kernel(
-    const double* __restrict__ sx, const double* __restrict__ root,
-    const double* __restrict__ inv_c, const float* __restrict__ escale,
-    const float* __restrict__ xscale, int64_t in, int grid, float* __restrict__ s32,
-    float* __restrict__ inv_s32, float* __restrict__ ss32, int32_t* __restrict__ pow2_s) {
+// CTA (x, k): alpha k of the 256 columns 256 x .. 256 x + 255, one column
+// a thread.  Each CTA reduces the chunk extremes and centres alpha k
+// (centre_alpha), forms its scalings from q and the max|W| / max|X| bits
+// (alpha_scalings; CTA x = 0 stores escale[k] and unscale[k]), then
+// s32[k][j] = f = fp32(u[k][j] * ic) and inv_s32[k][j] = 2^e_k / f;
+// pow2_s[k] is cleared when some entry is not a power of two.
+constexpr int kTabCols = 256;
+__global__ void __launch_bounds__(kTabCols) alpha_table_kernel(
+    const double* __restrict__ u, const double* __restrict__ minmax,
+    const uint32_t* __restrict__ absmax, int x_scaled, int64_t in, int grid,
+    float* __restrict__ s32, float* __restrict__ inv_s32, float* __restrict__ escale,
+    double* __restrict__ unscale, int32_t* __restrict__ pow2_s) {
   pdl_wait();
   pdl_trigger();
-  __shared__ uint32_t not_pow2[(kMaxGrid + 1 + 31) / 32];
-  const int nwords = (grid + 1 + 31) / 32;
-  for (int i = threadIdx.x; i < nwords; i += blockDim.x) not_pow2[i] = 0u;
-  __syncthreads();
-  const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
-  const int64_t j = (int64_t)blockIdx.x * kTabCols + lane;
-  const bool live = j < in;
-  const double sxj = live ? sx[j] : 1.0, r = live ? root[j] : 1.0;
-  const double step = pow_int(r, kTabSlices);
-  double v = pow_int(r, q);
-  for (int k = q; k <= grid; k += kTabSlices) {
-    const double sk = k == grid ? sxj : v;
-    const float f = __double2float_rn(sk * inv_c[k]);
-    bool np2 = false;
-    if (live) {
-      s32[(int64_t)k * in + j] = f;
-      if (ss32 != nullptr) {
-        inv_s32[(int64_t)k * in + j] = __frcp_rn(f) * xscale[k];
-        ss32[(int64_t)k * in + j] = f * escale[k];
-      } else {
-        inv_s32[(int64_t)k * in + j] = __frcp_rn(f) * escale[k];
-      }
-      np2 = (__float_as_uint(f) & 0x007FFFFFu) != 0u;
-    }
-    if (__any_sync(0xffffffffu, np2) && lane == 0) atomicOr(&not_pow2[k / 32], 1u << (k % 32));
-    v *= step;
+  const int k = blockIdx.y;
+  const int64_t j = (int64_t)blockIdx.x * kTabCols + threadIdx.x;
+  const double uk = j < in ? u[(int64_t)k * in + j] : 1.0;
+  double ic, q;
+  centre_alpha(minmax, chunk_count(in), k, grid, ic, q);
+  int e, m;
+  alpha_scalings(q, __uint_as_float(absmax[0]), __uint_as_float(absmax[1]), false, x_scaled != 0,
+                 e, m);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    escale[k] = exp2i_f32(e);
+    unscale[k] = exp2i_f64(-2 * (e + m));
   }
-  __syncthreads();
-  for (int k = threadIdx.x; k <= grid; k += blockDim.x)
-    if ((not_pow2[k / 32] >> (k % 32)) & 1u) atomicAnd(&pow2_s[k], 0);
+  bool np2 = false;
+  if (j < in) {
+    const float f = __double2float_rn(uk * ic);
+    s32[(int64_t)k * in + j] = f;
+    inv_s32[(int64_t)k * in + j] = __frcp_rn(f) * exp2i_f32(e);
+    np2 = (__float_as_uint(f) & 0x007FFFFFu) != 0u;
+  }
+  if (__syncthreads_or(np2) && threadIdx.x == 0) atomicAnd(&pow2_s[k], 0);
+}
+
+// The pre-divided mode's scalings, CTA (x, k) as alpha_table_kernel:
+// ss32[k][j] = s32[k][j] * 2^e_k (exact), escale[k] = 2^e_k and
+// unscale[k] = 2^-2(e_k + m_k) from qk[k], max|W| and max|X|.
+__global__ void __launch_bounds__(kTabCols) scale_table_xs_kernel(
+    const float* __restrict__ s32, const double* __restrict__ qk,
+    const uint32_t* __restrict__ absmax, int64_t in, float* __restrict__ ss32,
+    float* __restrict__ escale, double* __restrict__ unscale) {
+  pdl_wait();
+  pdl_trigger();
+  const int k = blockIdx.y;
+  int e, m;
+  alpha_scalings(qk[k], __uint_as_float(absmax[0]), __uint_as_float(absmax[1]), true, false, e, m);
+  const float es = exp2i_f32(e);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    escale[k] = es;
+    unscale[k] = exp2i_f64(-2 * (e + m));
+  }
+  const int64_t j = (int64_t)blockIdx.x * kTabCols + threadIdx.x;
+  if (j < in) ss32[(int64_t)k * in + j] = s32[(int64_t)k * in + j] * es;
 }
 
 // One CTA: per-alpha fixed-order sums, strict argmin, copy of the kept scales.
@@ -149,21 +155,26 @@ __global__ void __launch_bounds__(1024) reduce_argmin_kernel(const double* __res
   if (warp == 0) {
     // first index of the smallest error under strict <, starting from +inf:
     // each lane scans its own alphas in order, then lanes merge preferring
-    // the smaller error and, on equal errors, the smaller index
+    // the smaller error and, on equal errors, the smaller index.  The
+    // comparisons run on total-order keys of the errors (integer compares;
+    // float64 ones are slow here): NaN is never kept, -0 counts as +0.
+    const unsigned long long kinf = f64_key(INFINITY);
     int best = -1;
-    double be = INFINITY;
+    unsigned long long bk = kinf;
     for (int k = lane; k < n_alpha; k += 32) {
       const double e = err_sh[k];
-      if (e < be) {
-        be = e;
+      if (f64_is_nan(e)) continue;
+      const unsigned long long ek = f64_key(f64_drop_sign_of_zero(e));
+      if (ek < bk) {
+        bk = ek;
         best = k;
       }
     }
     for (int o = 16; o > 0; o >>= 1) {
-      const double oe = __shfl_xor_sync(0xffffffffu, be, o);
+      const unsigned long long ok = __shfl_xor_sync(0xffffffffu, bk, o);
       const int ob = __shfl_xor_sync(0xffffffffu, best, o);
-      if (ob >= 0 && (best < 0 || oe < be || (oe == be && ob < best))) {
-        be = oe;
+      if (ob >= 0 && (best < 0 || ok < bk || (ok == bk && ob < best))) {
+        bk = ok;
         best = ob;
       }
     }
@@ -261,33 +272,30 @@ cudaError_t launch_sweep_summary(const double* err, const int32_t* best, const d
   return launch_pdl(sweep_summary_kernel, 1, 1, 0, s, err, best, power, grid, row);
 }
 
-size_t prep_chunks(int64_t in) { return (size_t)((in + 31) / 32); }  // the finer of the two chunkings
+size_t prep_chunks(int64_t in) { return (size_t)((in + kPrepChunk - 1) / kPrepChunk); }
 
 cudaError_t launch_alpha_root(const double* sx, int64_t in, const CentreArgs& ca, cudaStream_t s) {
   if (ca.grid < 1 || ca.grid > kMaxGrid) return cudaErrorInvalidValue;
-  return launch_pdl(alpha_root_kernel, (unsigned)((in + kPrepChunk - 1) / kPrepChunk), kPrepChunk,
-                    0, s, sx, in, ca);
+  return launch_pdl(alpha_root_kernel, (unsigned)((in + kPrepChunk - 1) / kPrepChunk), 128, 0, s,
+                    sx, in, ca);
 }
 
-cudaError_t launch_alpha_table(const double* sx, const double* root, const double* inv_c,
-                               const float* escale, int64_t in, int grid, float* s32,
-                               float* inv_s32, int32_t* pow2_s, cudaStream_t s) {
+cudaError_t launch_alpha_table(const double* u, const double* minmax, const uint32_t* absmax,
+                               int x_scaled, int64_t in, int grid, float* s32, float* inv_s32,
+                               float* escale, double* unscale, int32_t* pow2_s, cudaStream_t s) {
   if (grid < 1 || grid > kMaxGrid) return cudaErrorInvalidValue;
-  return launch_pdl(alpha_table_kernel, (unsigned)((in + kTabCols - 1) / kTabCols),
-                    kTabCols * kTabSlices, 0, s, sx, root, inv_c, escale,
-                    static_cast<const float*>(nullptr), in, grid, s32, inv_s32,
-                    static_cast<float*>(nullptr), pow2_s);
+  const dim3 g((unsigned)((in + kTabCols - 1) / kTabCols), (unsigned)(grid + 1));
+  return launch_pdl(alpha_table_kernel, g, kTabCols, 0, s, u, minmax, absmax, x_scaled, in, grid,
+                    s32, inv_s32, escale, unscale, pow2_s);
 }
 
-cudaError_t launch_alpha_table_xs(const double* sx, const double* root, const double* inv_c,
-                                  const float* escale, const float* xscale, int64_t in, int grid,
-                                  float* s32, float* inv_s32, float* ss32, int32_t* pow2_s,
-                                  cudaStream_t s) {
-  if (grid < 1 || grid > kMaxGrid || ss32 == nullptr || xscale == nullptr)
-    return cudaErrorInvalidValue;
-  return launch_pdl(alpha_table_kernel, (unsigned)((in + kTabCols - 1) / kTabCols),
-                    kTabCols * kTabSlices, 0, s, sx, root, inv_c, escale, xscale, in, grid, s32,
-                    inv_s32, ss32, pow2_s);
+cudaError_t launch_scale_table_xs(const float* s32, const double* qk, const uint32_t* absmax,
+                                  int64_t in, int grid, float* ss32, float* escale,
+                                  double* unscale, cudaStream_t s) {
+  if (grid < 1 || grid > kMaxGrid) return cudaErrorInvalidValue;
+  const dim3 g((unsigned)((in + kTabCols - 1) / kTabCols), (unsigned)(grid + 1));
+  return launch_pdl(scale_table_xs_kernel, g, kTabCols, 0, s, s32, qk, absmax, in, ss32, escale,
+                    unscale);
 }
 
 cudaError_t launch_reduce_argmin(const double* partials, const double* unscale, int n_alpha,

@@ -7,6 +7,7 @@
 // (exactly, as an integer, for fp16 X), so repeated calls give identical
 // results.
 #include <algorithm>
+#include <climits>
 #include <type_traits>
 
 #include "awq_alpha.cuh"
@@ -17,7 +18,7 @@ namespace awq {
 
 namespace {
 
-constexpr int kStatCols = 32;    // columns per CTA of the vector path (4 lanes x 8 columns)
+constexpr int kStatCols = kChunkCols;  // columns per CTA of the vector path (4 lanes x 8 columns)
 constexpr int kStatSlices = 64;  // row slices per CTA of the vector path
 constexpr int kScalarCols = 64;  // columns per CTA of the scalar path
 
@@ -109,58 +110,32 @@ struct ColSum<__half> {
   static __device__ __forceinline__ double total(Part a, uint32_t spec) {
     if (spec & 2u) return __longlong_as_double(0x7FF8000000000000ll);
     if (spec & 1u) return INFINITY;
-    return ldexp((double)a, -24);
+    return (double)a * 0x1p-24;  // exact: a power of two
   }
 };
 
-// Vector path: in % 8 == 0 and 16-byte aligned rows.  Blocks [0, nx) do the
-// statistics: thread (c, r) sums the 8 columns c*8..c*8+7 of the CTA's 32
-// over rows r, r+64, r+128, ..., four 16-byte loads in flight at a time; the
-// 64 slices are then added in a fixed order.  With xmax != nullptr the pass
-// also folds max|X| into *xmax.  Blocks [nx, gridDim.x) fold max|W| (nW
-// values) into *wmax in the same launch.  With ca.grid != 0 the statistics
-// blocks also write root = sx^(1/grid) and their chunk's extremes of sx, and
-// the last block to finish forms the per-alpha centring values.
+// Vector path: in % 8 == 0 and 16-byte aligned rows.  Thread (c, r) of CTA
+// b sums the 8 columns c*8..c*8+7 of the CTA's 32 over rows r, r+64,
+// r+128, ..., four 16-byte loads in flight at a time; the 64 slices are
+// then added in a fixed order.  With xmax != nullptr the pass also folds
+// max|X| into *xmax.  With ca.grid != 0 the CTA also writes its columns'
+// powers s_X^(k / grid) and its chunk's extremes of s_X with their roots
+// (CentreArgs; no step crosses CTAs).  Each CTA lets the next launch start
+// once it has read its part of X: that launch streams W, and X's loads
+// would otherwise queue behind W's.
 template <typename T>
 __global__ void __launch_bounds__(256) stats_vec_kernel(const T* __restrict__ X, int64_t N,
                                                         int64_t in, double* __restrict__ sx,
                                                         uint32_t* __restrict__ xmax,
-                                                        const T* __restrict__ W, int64_t nW,
-                                                        uint32_t* __restrict__ wmax, int nx,
                                                         CentreArgs ca) {
-  pdl_trigger();
-  if ((int)blockIdx.x >= nx) {
-    // ------------------------------------------------------------- max|W|
-    float m = 0.0f;
-    const int64_t n8 = nW / 8;
-    const int64_t stride = (int64_t)(gridDim.x - nx) * blockDim.x;
-    int64_t i = (int64_t)(blockIdx.x - nx) * blockDim.x + threadIdx.x;
-    for (; i < n8; i += 8 * stride) {  // eight 16-byte loads in flight
-      float v[8][8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (i + u * stride < n8) {
-          load8_f32<T>(W + (i + u * stride) * 8, v[u]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[u][e] = 0.0f;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[u][e]));
-    }
-    block_absmax(m, wmax);
-    if (ca.grid != 0) centre_if_last(ca, (unsigned)nx);
-    return;
-  }
-  // --------------------------------------------------------------- statistics
   using Part = typename ColSum<T>::Part;
   __shared__ Part red[kStatSlices][kStatCols + 1];
   __shared__ Part red2[kStatSlices / 8][kStatCols + 1];
   __shared__ uint32_t spec[kStatCols];
+  __shared__ double sh_v[kStatCols], sh_r[kStatCols];
   if (threadIdx.x < kStatCols) spec[threadIdx.x] = 0u;
+  if (ca.grid != 0 && blockIdx.x == 0)
+    for (int k = threadIdx.x; k <= ca.grid; k += blockDim.x) ca.pow2_s[k] = 1;
   __syncthreads();
   const int c = threadIdx.x % 4, r = threadIdx.x / 4;
   const int64_t col0 = (int64_t)blockIdx.x * kStatCols + c * 8;
@@ -175,6 +150,7 @@ __global__ void __launch_bounds__(256) stats_vec_kernel(const T* __restrict__ X,
     }
     for (; n < N; n += kStatSlices) cs.add(X + n * in + col0, m);
   }
+  pdl_trigger();
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[r][c * 8 + e] = cs.part(e);
   cs.flag_specials(spec + c * 8);
@@ -200,9 +176,10 @@ __global__ void __launch_bounds__(256) stats_vec_kernel(const T* __restrict__ X,
       const double v = ColSum<T>::total(a, spec[threadIdx.x]) / (double)N + 1e-8;
       sx[j] = v;
       if (ca.grid != 0) {
-        const double r = exp(log(v) / (double)ca.grid);
-        ca.root[j] = r;
-        x.take(v, r);
+        const double rt = exp(log(v) / (double)ca.grid);
+        sh_v[threadIdx.x] = v;
+        sh_r[threadIdx.x] = rt;
+        x.take(v, rt);
       }
     }
     if (ca.grid != 0) {
@@ -210,7 +187,119 @@ __global__ void __launch_bounds__(256) stats_vec_kernel(const T* __restrict__ X,
       if (threadIdx.x == 0) x.store(ca.minmax + 4 * blockIdx.x);
     }
   }
-  if (ca.grid != 0) centre_if_last(ca, (unsigned)nx);
+  if (ca.grid == 0) return;
+  __syncthreads();
+  write_powers(sh_v, sh_r, (int64_t)blockIdx.x * kStatCols, in, ca.grid, ca.u);
+}
+
+// fp16(v[i] * f[i]) for i < 8, packed into 16 bytes.
+__device__ __forceinline__ uint4 scaled_f16x8(const float (&v)[8], const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    __half2 h = __floats2half2_rn(v[2 * p] * f[2 * p], v[2 * p + 1] * f[2 * p + 1]);
+    w[p] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// max|W| (CTAs [0, nw)) and, with xs != nullptr, the pre-divided search's
+// table and X copies (CTAs [nw, gridDim.x)) in one launch, so that the
+// copies are formed while the weights stream.
+//
+// A max|W| CTA: eight 16-byte loads in flight per thread, folded into *wmax.
+//
+// A copy CTA (x, k) (x fastest) owns columns 256 x .. 256 x + 255 and alpha
+// k.  Once the statistics launch is done it reduces the chunk extremes and
+// centres alpha k (centre_alpha; CTA x = 0 stores qk[k]); thread i forms
+// the table entry f = fp32(u[k][j] * ic) of column j = 256 x + i, writes
+// s32[k][j] = f and leaves the factor 2^m_k / f that X is multiplied by in
+// shared memory; pow2_s[k] is cleared when some entry is not a power of
+// two.  Lane l of every warp then owns the eight columns 8 (32 x + l) .. + 7
+// (a warp covers 512 contiguous bytes of a row) and the eight warps walk
+// the rows, four rows in flight: xs[k][n][j] = fp16(X[n][j] * factor[j]).
+//
+// Every CTA waits for the launch before it before finishing, so this launch
+// ends after the statistics launch whatever it does.
+template <typename T>
+__global__ void __launch_bounds__(256, 5) wmax_xs_kernel(
+    const T* __restrict__ W, int64_t nW, uint32_t* __restrict__ wmax, int nw,
+    const T* __restrict__ X, int N, int in, int grid, const double* __restrict__ u,
+    const double* __restrict__ minmax, const uint32_t* __restrict__ xmax_bits,
+    float* __restrict__ s32, double* __restrict__ qk, int32_t* __restrict__ pow2_s,
+    uint4* __restrict__ xs) {
+  pdl_trigger();
+  if ((int)blockIdx.x < nw) {
+    float m = 0.0f;
+    const int64_t n8 = nW / 8;
+    const int64_t stride = (int64_t)nw * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i < n8; i += 8 * stride) {  // eight 16-byte loads in flight
+      float v[8][8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (i + q * stride < n8) {
+          load8_f32<T>(W + (i + q * stride) * 8, v[q]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[q][e] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[q][e]));
+    }
+    block_absmax(m, wmax);
+    pdl_wait();
+    return;
+  }
+  pdl_wait();
+  __shared__ __align__(16) float fac[256];
+  const int b = (int)blockIdx.x - nw;
+  const int nxb = (in + 255) / 256;
+  const int k = b / nxb, xb = b % nxb;
+  const int j = xb * 256 + (int)threadIdx.x;
+  const double uk = j < in ? u[(int64_t)k * in + j] : 1.0;
+  double ic, q;
+  centre_alpha(minmax, chunk_count(in), k, grid, ic, q);
+  if (xb == 0 && threadIdx.x == 0) qk[k] = q;
+  int e, mexp;
+  alpha_scalings(q, 0.0f, __uint_as_float(*xmax_bits), true, false, e, mexp);
+  bool np2 = false;
+  if (j < in) {
+    const float f = __double2float_rn(uk * ic);
+    s32[(int64_t)k * in + j] = f;
+    fac[threadIdx.x] = __frcp_rn(f) * exp2i_f32(mexp);
+    np2 = (__float_as_uint(f) & 0x007FFFFFu) != 0u;
+  }
+  if (__syncthreads_or(np2) && threadIdx.x == 0) atomicAnd(&pow2_s[k], 0);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int j8 = xb * 32 + lane;
+  const int n8 = in / 8;
+  if (j8 >= n8) return;
+  float f[8];
+  {
+    const float4 a = reinterpret_cast<const float4*>(fac + lane * 8)[0];
+    const float4 c4 = reinterpret_cast<const float4*>(fac + lane * 8)[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = c4.x; f[5] = c4.y; f[6] = c4.z; f[7] = c4.w;
+  }
+  const T* src = X + (int64_t)j8 * 8;
+  uint4* dst = xs + (int64_t)k * N * n8 + j8;
+  int n = warp;
+  for (; n + 24 < N; n += 32) {  // rows n, n + 8, n + 16, n + 24: four loads in flight
+    float v[4][8];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) load8_f32<T>(src + (int64_t)(n + 8 * p) * in, v[p]);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) dst[(int64_t)(n + 8 * p) * n8] = scaled_f16x8(v[p], f);
+  }
+  for (; n < N; n += 8) {
+    float v[8];
+    load8_f32<T>(src + (int64_t)n * in, v);
+    dst[(int64_t)n * n8] = scaled_f16x8(v, f);
+  }
 }
 
 // Scalar path for any shape: thread (c, r) sums column c over rows r, r+4, ...
@@ -284,61 +373,45 @@ __global__ void __launch_bounds__(256) to_f16_kernel(const T* __restrict__ X, in
   }
 }
 
-// xs[k][n][j] = fp16(X[n][j] * xinv[k][j]).  CTA (x, k): lane l of every
-// warp owns the eight columns 8 (32 x + l) .. + 7 (a warp covers 512
-// contiguous bytes of a row), keeps their xinv factors in registers, and
-// the CTA's eight warps walk the rows.
-template <typename T>
-__global__ void __launch_bounds__(256) x_over_s_kernel(const T* __restrict__ X, int N, int in,
-                                                       const float* __restrict__ xinv,
-                                                       uint4* __restrict__ xs) {
-  pdl_wait();
-  pdl_trigger();
-  const int k = blockIdx.y;
-  const int j8 = blockIdx.x * 32 + (threadIdx.x & 31);
-  const int n8 = in / 8;
-  if (j8 >= n8) return;
-  float f[8];
-  load8_f32<float>(xinv + (int64_t)k * in + j8 * 8, f);
-  uint4* dst = xs + (int64_t)k * N * n8 + j8;
-  for (int n = threadIdx.x >> 5; n < N; n += 8) {
-    float v[8];
-    load8_f32<T>(X + (int64_t)n * in + j8 * 8, v);
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      __half2 h = __floats2half2_rn(v[2 * q] * f[2 * q], v[2 * q + 1] * f[2 * q + 1]);
-      w[q] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    dst[(int64_t)n * n8] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
 unsigned grid_for(int64_t work);
 
 template <typename T>
 cudaError_t stats_dispatch(const void* X, int64_t N, int64_t in, double* sx, uint32_t* xmax,
-                           const void* W, int64_t nW, uint32_t* wmax, const CentreArgs& ca,
-                           cudaStream_t s) {
+                           const CentreArgs& ca, cudaStream_t s) {
   const bool vec = (in % 8 == 0) && ((reinterpret_cast<uintptr_t>(X) & 15) == 0);
-  const bool wvec = W != nullptr && nW % 8 == 0 && ((reinterpret_cast<uintptr_t>(W) & 15) == 0);
-  if (vec && (W == nullptr || wvec)) {
+  if (vec) {
     const int nx = (int)((in + kStatCols - 1) / kStatCols);
-    // max|W| blocks: eight 16-byte loads in flight per thread; at most four
-    // CTAs per SM, so that they and the statistics CTAs are resident at once
-    // (no second wave)
-    const int nw =
-        W != nullptr ? (int)std::max<int64_t>(1, std::min<int64_t>((nW / 8 + 2047) / 2048,
-                                                                   device_sm_count() * 4))
-                     : 0;
-    stats_vec_kernel<T><<<(unsigned)(nx + nw), 256, 0, s>>>(
-        static_cast<const T*>(X), N, in, sx, xmax, static_cast<const T*>(W), nW, wmax, nx, ca);
+    stats_vec_kernel<T><<<(unsigned)nx, 256, 0, s>>>(static_cast<const T*>(X), N, in, sx, xmax,
+                                                     ca);
   } else {
-    if (xmax != nullptr || W != nullptr || ca.grid != 0) return cudaErrorInvalidValue;
+    if (xmax != nullptr || ca.grid != 0) return cudaErrorInvalidValue;
     stats_scalar_kernel<T><<<(unsigned)((in + kScalarCols - 1) / kScalarCols), 256, 0, s>>>(
         static_cast<const T*>(X), N, in, sx);
   }
   return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t wmax_xs_dispatch(const void* W, int64_t nW, uint32_t* wmax, const void* X, int64_t N,
+                             int64_t in, int grid, const double* u, const double* minmax,
+                             const uint32_t* xmax_bits, float* s32, double* qk, int32_t* pow2_s,
+                             void* xs, cudaStream_t s) {
+  if (nW % 8 != 0 || (reinterpret_cast<uintptr_t>(W) & 15) != 0) return cudaErrorInvalidValue;
+  // max|W| CTAs: eight 16-byte loads in flight per thread, at most three
+  // per SM (five fit), so that copy CTAs find room beside them
+  const int nw = (int)std::max<int64_t>(
+      1, std::min<int64_t>((nW / 8 + 2047) / 2048, (int64_t)device_sm_count() * 3));
+  int64_t ncopy = 0;
+  if (xs != nullptr) {
+    if (in % 8 != 0 || (reinterpret_cast<uintptr_t>(X) & 15) != 0 || N > (1 << 24) ||
+        in > (1 << 24) || grid < 1 || grid > kMaxGrid)
+      return cudaErrorInvalidValue;
+    ncopy = ((in + 255) / 256) * (int64_t)(grid + 1);
+  }
+  if (nw + ncopy > INT_MAX) return cudaErrorInvalidValue;
+  return launch_pdl(wmax_xs_kernel<T>, (unsigned)(nw + ncopy), 256, 0, s, static_cast<const T*>(W),
+                    nW, wmax, nw, static_cast<const T*>(X), (int)N, (int)in, grid, u, minmax,
+                    xmax_bits, s32, qk, pow2_s, static_cast<uint4*>(xs));
 }
 
 unsigned grid_for(int64_t work) {
@@ -350,12 +423,28 @@ unsigned grid_for(int64_t work) {
 }  // namespace
 
 cudaError_t launch_channel_stats(const void* X, int dt, int64_t N, int64_t in, double* sx,
-                                 uint32_t* xmax, const void* W, int64_t nW, uint32_t* wmax,
-                                 const CentreArgs& ca, cudaStream_t s) {
+                                 uint32_t* xmax, const CentreArgs& ca, cudaStream_t s) {
   switch (dt) {
-    case kDtF32: return stats_dispatch<float>(X, N, in, sx, xmax, W, nW, wmax, ca, s);
-    case kDtF16: return stats_dispatch<__half>(X, N, in, sx, xmax, W, nW, wmax, ca, s);
-    default: return stats_dispatch<__nv_bfloat16>(X, N, in, sx, xmax, W, nW, wmax, ca, s);
+    case kDtF32: return stats_dispatch<float>(X, N, in, sx, xmax, ca, s);
+    case kDtF16: return stats_dispatch<__half>(X, N, in, sx, xmax, ca, s);
+    default: return stats_dispatch<__nv_bfloat16>(X, N, in, sx, xmax, ca, s);
+  }
+}
+
+cudaError_t launch_wmax_xs(const void* W, int dt, int64_t nW, uint32_t* wmax, const void* X,
+                           int64_t N, int64_t in, int grid, const double* u,
+                           const double* minmax, const uint32_t* xmax_bits, float* s32,
+                           double* qk, int32_t* pow2_s, void* xs, cudaStream_t s) {
+  switch (dt) {
+    case kDtF32:
+      return wmax_xs_dispatch<float>(W, nW, wmax, X, N, in, grid, u, minmax, xmax_bits, s32, qk,
+                                     pow2_s, xs, s);
+    case kDtF16:
+      return wmax_xs_dispatch<__half>(W, nW, wmax, X, N, in, grid, u, minmax, xmax_bits, s32, qk,
+                                      pow2_s, xs, s);
+    default:
+      return wmax_xs_dispatch<__nv_bfloat16>(W, nW, wmax, X, N, in, grid, u, minmax, xmax_bits,
+                                             s32, qk, pow2_s, xs, s);
   }
 }
 
@@ -374,26 +463,6 @@ cudaError_t launch_absmax(const void* p, int dt, int64_t n, uint32_t* out, cudaS
                                                         vec, out);
   }
   return cudaGetLastError();
-}
-
-cudaError_t launch_x_over_s(const void* X, int dt, int64_t N, int64_t in, int n_alpha,
-                            const float* xinv, void* xs, cudaStream_t s) {
-  if (in % 8 != 0 || (reinterpret_cast<uintptr_t>(X) & 15) != 0 || N > (1 << 24) ||
-      in > (1 << 24) || n_alpha > 65535)
-    return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)((in / 8 + 31) / 32), (unsigned)n_alpha);
-  uint4* d = static_cast<uint4*>(xs);
-  switch (dt) {
-    case kDtF32:
-      return launch_pdl(x_over_s_kernel<float>, grid, 256, 0, s, static_cast<const float*>(X),
-                        (int)N, (int)in, xinv, d);
-    case kDtF16:
-      return launch_pdl(x_over_s_kernel<__half>, grid, 256, 0, s, static_cast<const __half*>(X),
-                        (int)N, (int)in, xinv, d);
-    default:
-      return launch_pdl(x_over_s_kernel<__nv_bfloat16>, grid, 256, 0, s,
-                        static_cast<const __nv_bfloat16*>(X), (int)N, (int)in, xinv, d);
-  }
 }
 
 cudaError_t launch_to_f16(const void* X, int dt, int64_t n, const uint32_t* xmax_bits, void* dst,
