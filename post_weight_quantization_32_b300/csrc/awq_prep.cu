@@ -115,9 +115,38 @@ __global__ void __launch_bounds__(kTabCols) scale_table_xs_kernel(
 }
 
 // One CTA: per-alpha fixed-order sums, strict argmin, copy of the kept scales.
-// With parts > 0 (the finish of a row-split search) err_k is instead
+// err_k = unscale[k] * sum_t partials[k][t] / denom, the tiles added in
+// order; with parts > 0 (the finish of a row-split search) err_k is instead
 // sum_{p < parts} partials[p][k] / denom, added in part order, and unscale
 // is not read.
+//
+// One thread per alpha: the SM's float64 pipe takes a warp instruction
+// about every 19 cycles however few lanes are active, so the sums and the
+// division run as few warp instructions as possible (for up to 32 alphas,
+// the lanes of warp 0, which then also takes the argmin by shuffles).
+__device__ __forceinline__ double alpha_error(const double* __restrict__ partials,
+                                              const double* __restrict__ unscale, int k,
+                                              int n_alpha, int n_tiles, int parts, double denom) {
+  double s = 0.0;
+  if (parts > 0) {
+    for (int q = 0; q < parts; ++q) s += __ldcg(partials + (int64_t)q * n_alpha + k);
+    return s / denom;
+  }
+  const double* row = partials + (int64_t)k * n_tiles;
+  for (int t = 0; t < n_tiles; ++t) s += row[t];
+  return s * unscale[k] / denom;
+}
+
+// Strict-< keep over (key, index) pairs: the smaller error, then the smaller index.
+__device__ __forceinline__ void keep_smaller(unsigned long long& bk, int& best,
+                                             unsigned long long ok, int ob) {
+  if (ob >= 0 && (best < 0 || ok < bk || (ok == bk && ob < best))) {
+    bk = ok;
+    best = ob;
+  }
+}
+
+constexpr int kStageDoubles = 4096;  // partial sums staged in shared memory (32 KB)
 __global__ void __launch_bounds__(1024) reduce_argmin_kernel(const double* __restrict__ partials,
                                                             const double* __restrict__ unscale,
                                                             int n_alpha, int n_tiles, double denom,
@@ -129,59 +158,73 @@ __global__ void __launch_bounds__(1024) reduce_argmin_kernel(const double* __res
   pdl_wait();
   pdl_trigger();
   __shared__ int best_sh;
-  __shared__ double err_sh[kMaxGrid + 1];
+  __shared__ double stage[kStageDoubles];
+  extern __shared__ double err_sh[];  // [n_alpha] (more than 32 alphas)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (parts > 0) {
+  // the first index of the smallest error under strict <, starting from
+  // +inf, on total-order keys of the errors (integer compares): NaN is never
+  // kept, -0 counts as +0
+  const unsigned long long kinf = f64_key(INFINITY);
+  auto key_of = [](double e) {
+    return f64_is_nan(e) ? ~0ull : f64_key(f64_drop_sign_of_zero(e));
+  };
+  // tiles mode: the partial sums staged in shared memory by every thread in
+  // one coalesced pass (one load round trip), then summed per alpha there
+  const int64_t n_part = (int64_t)n_alpha * n_tiles;
+  const bool staged = parts == 0 && n_part <= kStageDoubles;
+  if (staged) {
+    for (int i = threadIdx.x; i < n_part; i += blockDim.x) stage[i] = __ldcg(partials + i);
+    __syncthreads();
+  }
+  const double* psrc = staged ? stage : partials;
+  if (n_alpha <= 32) {
+    if (warp == 0) {
+      unsigned long long bk = kinf;
+      int best = -1;
+      if (lane < n_alpha) {
+        const double e = alpha_error(psrc, unscale, lane, n_alpha, n_tiles, parts, denom);
+        err[lane] = e;
+        const unsigned long long k = key_of(e);
+        if (k < kinf) {
+          bk = k;
+          best = lane;
+        }
+      }
+      for (int o = 16; o > 0; o >>= 1)
+        keep_smaller(bk, best, __shfl_xor_sync(0xffffffffu, bk, o),
+                     __shfl_xor_sync(0xffffffffu, best, o));
+      if (lane == 0) {
+        if (best < 0) set_status(dev_status, ST_NONFINITE);
+        *best_out = best;
+        best_sh = best;
+      }
+    }
+  } else {
     for (int k = threadIdx.x; k < n_alpha; k += blockDim.x) {
-      double s = 0.0;
-      for (int q = 0; q < parts; ++q) s += partials[(int64_t)q * n_alpha + k];
-      const double e = s / denom;
+      const double e = alpha_error(psrc, unscale, k, n_alpha, n_tiles, parts, denom);
       err[k] = e;
       err_sh[k] = e;
     }
-  } else {
-    for (int k = warp; k < n_alpha; k += blockDim.x >> 5) {
-      double s = 0.0;
-      for (int t = lane; t < n_tiles; t += 32) s += __ldcg(partials + (int64_t)k * n_tiles + t);
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    __syncthreads();
+    if (warp == 0) {
+      // each lane scans its own alphas in order, then lanes merge
+      int best = -1;
+      unsigned long long bk = kinf;
+      for (int k = lane; k < n_alpha; k += 32) {
+        const unsigned long long ek = key_of(err_sh[k]);
+        if (ek < bk) {
+          bk = ek;
+          best = k;
+        }
+      }
+      for (int o = 16; o > 0; o >>= 1)
+        keep_smaller(bk, best, __shfl_xor_sync(0xffffffffu, bk, o),
+                     __shfl_xor_sync(0xffffffffu, best, o));
       if (lane == 0) {
-        const double e = s * unscale[k] / denom;
-        err[k] = e;
-        err_sh[k] = e;
+        if (best < 0) set_status(dev_status, ST_NONFINITE);
+        *best_out = best;
+        best_sh = best;
       }
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // first index of the smallest error under strict <, starting from +inf:
-    // each lane scans its own alphas in order, then lanes merge preferring
-    // the smaller error and, on equal errors, the smaller index.  The
-    // comparisons run on total-order keys of the errors (integer compares;
-    // float64 ones are slow here): NaN is never kept, -0 counts as +0.
-    const unsigned long long kinf = f64_key(INFINITY);
-    int best = -1;
-    unsigned long long bk = kinf;
-    for (int k = lane; k < n_alpha; k += 32) {
-      const double e = err_sh[k];
-      if (f64_is_nan(e)) continue;
-      const unsigned long long ek = f64_key(f64_drop_sign_of_zero(e));
-      if (ek < bk) {
-        bk = ek;
-        best = k;
-      }
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      const int ob = __shfl_xor_sync(0xffffffffu, best, o);
-      if (ob >= 0 && (best < 0 || ok < bk || (ok == bk && ob < best))) {
-        bk = ok;
-        best = ob;
-      }
-    }
-    if (lane == 0) {
-      if (best < 0) set_status(dev_status, ST_NONFINITE);
-      *best_out = best;
-      best_sh = best;
     }
   }
   __syncthreads();
@@ -302,16 +345,19 @@ cudaError_t launch_reduce_argmin(const double* partials, const double* unscale, 
                                  int n_tiles, double denom, const float* s32, int64_t in,
                                  double* err, int32_t* best, float* s_best, int32_t* dev_status,
                                  cudaStream_t s) {
-  return launch_pdl(reduce_argmin_kernel, 1, 1024, 0, s, partials, unscale, n_alpha, n_tiles, denom,
-                    s32, in, err, best, s_best, dev_status, 0);
+  if (n_alpha < 1 || n_alpha > kMaxGrid + 1) return cudaErrorInvalidValue;
+  return launch_pdl(reduce_argmin_kernel, 1, 1024, n_alpha > 32 ? (size_t)n_alpha * sizeof(double) : 0,
+                    s, partials, unscale, n_alpha, n_tiles, denom, s32, in, err, best, s_best,
+                    dev_status, 0);
 }
 
 cudaError_t launch_search_finish(const double* sums, int parts, int n_alpha, double denom,
                                  const float* s_table, int64_t in, double* err, int32_t* best,
                                  float* s_best, int32_t* dev_status, cudaStream_t s) {
   if (n_alpha < 1 || n_alpha > kMaxGrid + 1 || parts < 1) return cudaErrorInvalidValue;
-  return launch_pdl(reduce_argmin_kernel, 1, 1024, 0, s, sums, static_cast<const double*>(nullptr),
-                    n_alpha, 0, denom, s_table, in, err, best, s_best, dev_status, parts);
+  return launch_pdl(reduce_argmin_kernel, 1, 1024, n_alpha > 32 ? (size_t)n_alpha * sizeof(double) : 0,
+                    s, sums, static_cast<const double*>(nullptr), n_alpha, 0, denom, s_table, in,
+                    err, best, s_best, dev_status, parts);
 }
 
 }  // namespace awq
