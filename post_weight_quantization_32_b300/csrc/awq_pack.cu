@@ -296,8 +296,10 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_fast_kernel
     const T* __restrict__ W, int64_t out, int64_t in, const float* __restrict__ s, QParams qp,
     int lpg, uint32_t* __restrict__ qweight, int64_t nwords, float* __restrict__ scales,
     uint8_t* __restrict__ zeros, int32_t* dev_status) {
-  pdl_wait();
+  // W is an input of the call, so the first rows' copies start before the
+  // launch that forms s has finished; s is read only after pdl_wait
   pdl_trigger();
+  bool waited = false;
   constexpr int kChunks = pack_chunks<T>();
   constexpr int kPerWord = 32 / B;  // codes per 32-bit word
   constexpr uint32_t kMaxq = (1u << B) - 1u;
@@ -313,16 +315,6 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_fast_kernel
   for (int64_t seg = blockIdx.y; seg < segs; seg += gridDim.y) {
     const int64_t c0 = seg * kPackSeg + lane * 32;
     const bool live = c0 < in;  // in is a multiple of the group, so all 32 columns are live
-    // the segment's scales, shared by every warp of the CTA: [i][lane] holds
-    // s[c0 + 4i .. c0 + 4i + 3] of that lane, so a warp's reads of one i are
-    // 32 consecutive 16-byte words
-    if (warp == 0) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        s_seg[i][lane] = live ? __ldg(reinterpret_cast<const float4*>(s + c0) + i)
-                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    }
-    __syncthreads();
     const int64_t r0 = (int64_t)blockIdx.x * 8 + warp;
     // copies of row r0 + i * rstep into ring stage i % kPackStages (one group per row)
     auto issue = [&](int64_t i) {
@@ -337,6 +329,20 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_fast_kernel
     };
 #pragma unroll
     for (int i = 0; i < kPackStages - 1; ++i) issue(i);
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
+    // the segment's scales, shared by every warp of the CTA: [i][lane] holds
+    // s[c0 + 4i .. c0 + 4i + 3] of that lane, so a warp's reads of one i are
+    // 32 consecutive 16-byte words
+    if (warp == 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        s_seg[i][lane] = live ? __ldg(reinterpret_cast<const float4*>(s + c0) + i)
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    __syncthreads();
     for (int64_t i = 0; r0 + i * rstep < out; ++i) {
       issue(i + kPackStages - 1);
       cp_async_wait<kPackStages - 1>();
@@ -458,6 +464,7 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_fast_kernel
     cp_async_wait<0>();  // no copy may still target the ring when it is reused
     __syncthreads();     // nor any warp still read the segment's scales
   }
+  if (!waited) pdl_wait();
 }
 
 // General path (any group size): one warp per (row, group), lanes strided
