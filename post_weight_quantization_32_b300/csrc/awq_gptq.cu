@@ -133,6 +133,10 @@ constexpr int kCB = 32;  // Cholesky / inverse block
 
 // Factor the diagonal block A[k0:k0+b, k0:k0+b] = L L^T in place (lower).
 // A non-positive pivot sets the status (the matrix is not positive definite).
+// Right-looking, one thread per entry: at step j the pivot is taken, column
+// j is divided by it and the trailing lower triangle loses L[r][j] L[c][j].
+// Every entry sees the same subtractions in the same order (t = 0, 1, ...)
+// as a column-by-column (left-looking) factorisation.
 __global__ void __launch_bounds__(kCB * kCB) chol_diag_kernel(float* __restrict__ A, int64_t n,
                                                              int64_t k0, int b,
                                                              int32_t* dev_status) {
@@ -143,9 +147,8 @@ __global__ void __launch_bounds__(kCB * kCB) chol_diag_kernel(float* __restrict_
   if (r < b && c < b) L[r][c] = A[(k0 + r) * n + k0 + c];
   __syncthreads();
   for (int j = 0; j < b; ++j) {
-    if (threadIdx.x == 0) {
+    if (r == j && c == j) {
       float d = L[j][j];
-      for (int t = 0; t < j; ++t) d -= L[j][t] * L[j][t];
       if (!(d > 0.0f)) {
         set_status(dev_status, ST_NONFINITE);
         d = 1e-30f;
@@ -153,11 +156,9 @@ __global__ void __launch_bounds__(kCB * kCB) chol_diag_kernel(float* __restrict_
       L[j][j] = sqrtf(d);
     }
     __syncthreads();
-    if (c == 0 && r > j && r < b) {
-      float v = L[r][j];
-      for (int t = 0; t < j; ++t) v -= L[r][t] * L[j][t];
-      L[r][j] = v / L[j][j];
-    }
+    if (c == j && r > j && r < b) L[r][j] = L[r][j] / L[j][j];
+    __syncthreads();
+    if (c > j && r >= c && r < b) L[r][c] -= L[r][j] * L[c][j];
     __syncthreads();
   }
   if (r < b && c < b) A[(k0 + r) * n + k0 + c] = c <= r ? L[r][c] : 0.0f;
@@ -169,8 +170,14 @@ __global__ void __launch_bounds__(128) chol_panel_kernel(float* __restrict__ A, 
   pdl_wait();
   pdl_trigger();
   __shared__ float L[kCB][kCB + 1];
-  for (int i = threadIdx.x; i < b * b; i += blockDim.x)
-    L[i / b][i % b] = A[(k0 + i / b) * n + k0 + i % b];
+  {  // thread t loads column t % 32 of rows t / 32, t / 32 + 4, ...: all loads in flight
+    const int c = (int)threadIdx.x % kCB, r0 = (int)threadIdx.x / kCB;
+#pragma unroll
+    for (int k = 0; k < kCB / 4; ++k) {
+      const int r = r0 + 4 * k;
+      if (r < b && c < b) L[r][c] = A[(k0 + r) * n + k0 + c];
+    }
+  }
   __syncthreads();
   const int64_t row = k0 + b + blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (row >= n) return;
@@ -180,7 +187,8 @@ __global__ void __launch_bounds__(128) chol_panel_kernel(float* __restrict__ A, 
   for (int j = 0; j < kCB; ++j) {
     if (j < b) {
       float v = a[j];
-      for (int t = 0; t < j; ++t) v -= x[t] * L[j][t];
+#pragma unroll
+      for (int t = 0; t < j; ++t) v -= x[t] * L[j][t];  // both loops unrolled: x stays in registers
       x[j] = v / L[j][j];
       a[j] = x[j];
     }
@@ -196,8 +204,9 @@ __global__ void __launch_bounds__(kCB) tri_inv_diag_kernel(const float* __restri
   pdl_wait();
   pdl_trigger();
   __shared__ float L[kCB][kCB + 1];
-  for (int i = threadIdx.x; i < b * b; i += blockDim.x)
-    L[i / b][i % b] = M[(i0 + i / b) * n + i0 + i % b];
+#pragma unroll
+  for (int r = 0; r < kCB; ++r)  // thread c loads column c: all loads in flight
+    if (r < b && (int)threadIdx.x < b) L[r][threadIdx.x] = M[(i0 + r) * n + i0 + threadIdx.x];
   __syncthreads();
   const int c = threadIdx.x;
   if (c >= b) return;
@@ -206,7 +215,8 @@ __global__ void __launch_bounds__(kCB) tri_inv_diag_kernel(const float* __restri
   for (int r = 0; r < kCB; ++r) {
     if (r < b) {
       float v = r == c ? 1.0f : 0.0f;
-      for (int t = 0; t < r; ++t) v -= L[r][t] * y[t];
+#pragma unroll
+      for (int t = 0; t < r; ++t) v -= L[r][t] * y[t];  // both loops unrolled: y stays in registers
       y[r] = v / L[r][r];
       Y[(i0 + r) * n + i0 + c] = y[r];
     }
@@ -242,67 +252,132 @@ __global__ void __launch_bounds__(256) scale_weights_kernel(const T* __restrict_
 }
 
 // ------------------------------------------------------------ the sweep
-constexpr int kSB = 128;       // columns per sweep block
-constexpr int kSRows = 128;    // rows per CTA of the in-block kernel
+constexpr int kSB = 128;                  // columns per sweep block
+constexpr int kSLanes = 8;                // threads per row
+constexpr int kSOwn = kSB / kSLanes;      // columns a thread holds (16)
+constexpr int kSRows = 32;                // rows per CTA (256 threads)
 
-// One thread per row runs columns b0 .. b0+bw-1 in order.  Shared memory:
-// U[b0:b0+bw, b0:b0+bw] and the CTA's rows of the weight block, [col][row].
+// Eight threads per row run columns b0 .. b0+bw-1 in order; thread q of a
+// row holds columns q, q + 8, q + 16, ... of the block in registers.  For
+// column i every thread of the row takes the column's current value from
+// its holder (a shuffle) and forms the same code and scaled error, and
+// each thread takes that error off the columns it holds beyond i (the
+// updates of a column arrive in column order, as in a one-thread sweep).
+// At a group's first column the group is fitted on the corrected weights
+// (extremes over the row's eight threads).  Codes and errors are staged in
+// shared memory and stored row by row.  Shared memory: U[b0:b0+bw,
+// b0:b0+bw], then the codes [32][128] and errors [32][128] of the CTA.
 // Writes the storage codes, the group steps and zero points, and
 // Err[row][i - b0] = (w - w_hat) / U[i][i].
-__global__ void __launch_bounds__(kSRows) sweep_block_kernel(
+__global__ void __launch_bounds__(kSRows * kSLanes, 2) sweep_block_kernel(
     float* __restrict__ Ws, const float* __restrict__ U, int64_t out, int64_t in, int64_t b0,
     int bw, int group, int bits, int sym, uint8_t* __restrict__ codes, float* __restrict__ scales,
     uint8_t* __restrict__ zeros, float* __restrict__ Err) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ float sm[];
-  float* Ub = sm;                   // [kSB][kSB]
-  float* wb = sm + kSB * kSB;       // [kSB][kSRows]
-  for (int i = threadIdx.x; i < bw * bw; i += blockDim.x)
-    Ub[(i / bw) * kSB + i % bw] = U[(b0 + i / bw) * in + b0 + i % bw];
-  const int64_t row = (int64_t)blockIdx.x * kSRows + threadIdx.x;
+  float* Ub = sm;                                                    // [kSB][kSB]
+  float* est = sm + kSB * kSB;                                       // [kSRows][kSB]
+  uint8_t* cst = reinterpret_cast<uint8_t*>(est + kSRows * kSB);     // [kSRows][kSB]
+  {  // thread t loads columns 4 (t % 32) .. + 3 of rows t / 32, t / 32 + 8, ...: all in flight
+    const int c4 = 4 * ((int)threadIdx.x % 32), r0 = (int)threadIdx.x / 32;
+#pragma unroll
+    for (int k = 0; k < kSB / 8; ++k) {
+      const int r = r0 + 8 * k;
+      if (r < bw) {
+        const float* src = U + (b0 + r) * in + b0 + c4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (c4 + e < bw) Ub[r * kSB + c4 + e] = src[e];
+      }
+    }
+  }
+  const int rl = (int)threadIdx.x / kSLanes, q = (int)threadIdx.x % kSLanes;
+  const int lane = (int)threadIdx.x & 31, base = lane & ~(kSLanes - 1);
+  const int64_t row = (int64_t)blockIdx.x * kSRows + rl;
   const bool live = row < out;
-  if (live)
-    for (int j = 0; j < bw; ++j) wb[j * kSRows + threadIdx.x] = Ws[row * in + b0 + j];
+  float w[kSOwn];
+#pragma unroll
+  for (int k = 0; k < kSOwn; ++k) {
+    const int j = q + kSLanes * k;
+    w[k] = (live && j < bw) ? Ws[row * in + b0 + j] : 0.0f;
+  }
   __syncthreads();
-  if (!live) return;
   const float Lf = (float)((1 << (bits - 1)) - 1), maxqf = (float)((1 << bits) - 1);
   const int64_t ng = in / group;
   float scale = 1.0f, zero = 0.0f;
-  for (int i = 0; i < bw; ++i) {
-    const int64_t col = b0 + i;
-    if (col % group == 0) {  // fit the group on the corrected weights
-      float m = 0.0f, lo = 0.0f, hi = 0.0f;
-      for (int j = i; j < i + group && j < bw; ++j) {
-        const float v = wb[j * kSRows + threadIdx.x];
-        m = fmaxf(m, fabsf(v));
-        lo = fminf(lo, v);
-        hi = fmaxf(hi, v);
+  constexpr unsigned FULL = 0xffffffffu;
+#pragma unroll
+  for (int ki = 0; ki < kSOwn; ++ki) {
+#pragma unroll
+    for (int o = 0; o < kSLanes; ++o) {
+      const int i = kSLanes * ki + o;
+      if (i < bw) {
+        const int64_t col = b0 + i;
+        if (col % group == 0) {  // fit the group on the corrected weights
+          float m = 0.0f, lo = 0.0f, hi = 0.0f;
+#pragma unroll
+          for (int k = ki; k < kSOwn; ++k) {
+            const int j = q + kSLanes * k;
+            if (j >= i && j < i + group && j < bw) {
+              m = fmaxf(m, fabsf(w[k]));
+              lo = fminf(lo, w[k]);
+              hi = fmaxf(hi, w[k]);
+            }
+          }
+#pragma unroll
+          for (int x = 1; x < kSLanes; x <<= 1) {
+            m = fmaxf(m, __shfl_xor_sync(FULL, m, x));
+            lo = fminf(lo, __shfl_xor_sync(FULL, lo, x));
+            hi = fmaxf(hi, __shfl_xor_sync(FULL, hi, x));
+          }
+          if (sym) {
+            scale = fmaxf(__fdiv_rn(m, Lf), 1e-8f);
+            zero = 0.0f;
+          } else {
+            scale = fmaxf(__fdiv_rn(__fsub_rn(hi, lo), maxqf), 1e-8f);
+            zero = rintf(__fdiv_rn(-lo, scale));
+          }
+          if (live && q == 0) {
+            scales[row * ng + col / group] = scale;
+            zeros[row * ng + col / group] = (uint8_t)(sym ? (1 << (bits - 1)) : (int)zero);
+          }
+        }
+        const float wi = __shfl_sync(FULL, w[ki], base | o);
+        float qv, what;
+        uint8_t code;
+        if (sym) {
+          qv = fminf(fmaxf(rintf(__fdiv_rn(wi, scale)), -Lf - 1.0f), Lf);
+          what = __fmul_rn(qv, scale);
+          code = (uint8_t)((int)qv + (1 << (bits - 1)));
+        } else {
+          qv = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(wi, scale)), zero), 0.0f), maxqf);
+          what = __fmul_rn(scale, __fsub_rn(qv, zero));
+          code = (uint8_t)qv;
+        }
+        const float err = (wi - what) / Ub[i * kSB + i];
+        if (q == o) {
+          est[rl * kSB + i] = err;
+          cst[rl * kSB + i] = code;
+        }
+        const float* ur = Ub + i * kSB + q;
+#pragma unroll
+        for (int k = ki; k < kSOwn; ++k) {
+          const int j = q + kSLanes * k;
+          if ((k > ki || q > o) && j < bw) w[k] -= err * ur[kSLanes * k];
+        }
       }
-      if (sym) {
-        scale = fmaxf(__fdiv_rn(m, Lf), 1e-8f);
-        zero = 0.0f;
-      } else {
-        scale = fmaxf(__fdiv_rn(__fsub_rn(hi, lo), maxqf), 1e-8f);
-        zero = rintf(__fdiv_rn(-lo, scale));
-      }
-      scales[row * ng + col / group] = scale;
-      zeros[row * ng + col / group] = (uint8_t)(sym ? (1 << (bits - 1)) : (int)zero);
     }
-    const float w = wb[i * kSRows + threadIdx.x];
-    float q, what;
-    if (sym) {
-      q = fminf(fmaxf(rintf(__fdiv_rn(w, scale)), -Lf - 1.0f), Lf);
-      what = __fmul_rn(q, scale);
-      codes[row * in + col] = (uint8_t)((int)q + (1 << (bits - 1)));
-    } else {
-      q = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(w, scale)), zero), 0.0f), maxqf);
-      what = __fmul_rn(scale, __fsub_rn(q, zero));
-      codes[row * in + col] = (uint8_t)q;
+  }
+  __syncthreads();
+  // the CTA's codes and errors, row by row
+  for (int idx = threadIdx.x; idx < kSRows * bw; idx += blockDim.x) {
+    const int r = idx / bw, i = idx % bw;
+    const int64_t gr = (int64_t)blockIdx.x * kSRows + r;
+    if (gr < out) {
+      codes[gr * in + b0 + i] = cst[r * kSB + i];
+      Err[gr * kSB + i] = est[r * kSB + i];
     }
-    const float err = (w - what) / Ub[i * kSB + i];
-    Err[row * kSB + i] = err;
-    for (int j = i + 1; j < bw; ++j) wb[j * kSRows + threadIdx.x] -= err * Ub[i * kSB + j];
   }
 }
 
@@ -426,12 +501,12 @@ cudaError_t launch_gptq(const void* W, const void* X, int dt, int64_t out, int64
   AWQ_TRY(launch_pdl(reverse_kernel, grid_for_elems(in * in), 256, 0, st, Y, A, in));
   const float* U = A;
   // 6: the sweep
-  const size_t smem = (size_t)(kSB * kSB + kSB * kSRows) * 4;
+  const size_t smem = (size_t)(kSB * kSB + kSB * kSRows) * 4 + (size_t)kSB * kSRows;
   AWQ_TRY(cudaFuncSetAttribute(sweep_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem));
   for (int64_t b0 = 0; b0 < in; b0 += kSB) {
     const int bw = (int)std::min<int64_t>(kSB, in - b0);
-    AWQ_TRY(launch_pdl(sweep_block_kernel, (unsigned)((out + kSRows - 1) / kSRows), kSRows, smem,
+    AWQ_TRY(launch_pdl(sweep_block_kernel, (unsigned)((out + kSRows - 1) / kSRows), kSRows * kSLanes, smem,
                        st, Ws, U, out, in, b0, bw, group, bits, sym, codes, scales, zeros, Err));
     const int64_t rest = in - b0 - bw;
     if (rest > 0)
