@@ -129,7 +129,9 @@ __global__ void __launch_bounds__(1024) damp_kernel(float* __restrict__ A, int64
 }
 
 // ------------------------------------------------------- blocked Cholesky
-constexpr int kCB = 32;  // Cholesky / inverse block
+constexpr int kCB = 64;  // Cholesky / inverse block
+constexpr int kDiagThreads = 1024;
+constexpr int kDiagPer = kCB * kCB / kDiagThreads;  // entries of the diagonal block per thread
 
 // Factor the diagonal block A[k0:k0+b, k0:k0+b] = L L^T in place (lower).
 // A non-positive pivot sets the status (the matrix is not positive definite).
@@ -137,17 +139,24 @@ constexpr int kCB = 32;  // Cholesky / inverse block
 // j is divided by it and the trailing lower triangle loses L[r][j] L[c][j].
 // Every entry sees the same subtractions in the same order (t = 0, 1, ...)
 // as a column-by-column (left-looking) factorisation.
-__global__ void __launch_bounds__(kCB * kCB) chol_diag_kernel(float* __restrict__ A, int64_t n,
-                                                             int64_t k0, int b,
-                                                             int32_t* dev_status) {
+__global__ void __launch_bounds__(kDiagThreads) chol_diag_kernel(float* __restrict__ A, int64_t n,
+                                                                 int64_t k0, int b,
+                                                                 int32_t* dev_status) {
   pdl_wait();
   pdl_trigger();
   __shared__ float L[kCB][kCB + 1];
-  const int r = threadIdx.x / kCB, c = threadIdx.x % kCB;
-  if (r < b && c < b) L[r][c] = A[(k0 + r) * n + k0 + c];
+  // thread t holds entries t, t + kDiagThreads, ... of the block (row-major)
+  int r[kDiagPer], c[kDiagPer];
+#pragma unroll
+  for (int e = 0; e < kDiagPer; ++e) {
+    const int idx = (int)threadIdx.x + kDiagThreads * e;
+    r[e] = idx / kCB;
+    c[e] = idx % kCB;
+    if (r[e] < b && c[e] < b) L[r[e]][c[e]] = A[(k0 + r[e]) * n + k0 + c[e]];
+  }
   __syncthreads();
   for (int j = 0; j < b; ++j) {
-    if (r == j && c == j) {
+    if (threadIdx.x == 0) {
       float d = L[j][j];
       if (!(d > 0.0f)) {
         set_status(dev_status, ST_NONFINITE);
@@ -156,12 +165,18 @@ __global__ void __launch_bounds__(kCB * kCB) chol_diag_kernel(float* __restrict_
       L[j][j] = sqrtf(d);
     }
     __syncthreads();
-    if (c == j && r > j && r < b) L[r][j] = L[r][j] / L[j][j];
+#pragma unroll
+    for (int e = 0; e < kDiagPer; ++e)
+      if (c[e] == j && r[e] > j && r[e] < b) L[r[e]][j] = L[r[e]][j] / L[j][j];
     __syncthreads();
-    if (c > j && r >= c && r < b) L[r][c] -= L[r][j] * L[c][j];
+#pragma unroll
+    for (int e = 0; e < kDiagPer; ++e)
+      if (c[e] > j && r[e] >= c[e] && r[e] < b) L[r[e]][c[e]] -= L[r[e]][j] * L[c[e]][j];
     __syncthreads();
   }
-  if (r < b && c < b) A[(k0 + r) * n + k0 + c] = c <= r ? L[r][c] : 0.0f;
+#pragma unroll
+  for (int e = 0; e < kDiagPer; ++e)
+    if (r[e] < b && c[e] < b) A[(k0 + r[e]) * n + k0 + c[e]] = c[e] <= r[e] ? L[r[e]][c[e]] : 0.0f;
 }
 
 // Rows i >= k0 + b: solve x L11^T = A[i, k0:k0+b] (one thread per row).
@@ -170,11 +185,11 @@ __global__ void __launch_bounds__(128) chol_panel_kernel(float* __restrict__ A, 
   pdl_wait();
   pdl_trigger();
   __shared__ float L[kCB][kCB + 1];
-  {  // thread t loads column t % 32 of rows t / 32, t / 32 + 4, ...: all loads in flight
+  {  // thread t loads column t % kCB of rows t / kCB, t / kCB + 2, ...: all loads in flight
     const int c = (int)threadIdx.x % kCB, r0 = (int)threadIdx.x / kCB;
 #pragma unroll
-    for (int k = 0; k < kCB / 4; ++k) {
-      const int r = r0 + 4 * k;
+    for (int k = 0; k < kCB / 2; ++k) {
+      const int r = r0 + 2 * k;
       if (r < b && c < b) L[r][c] = A[(k0 + r) * n + k0 + c];
     }
   }
@@ -477,7 +492,7 @@ cudaError_t launch_gptq(const void* W, const void* X, int dt, int64_t out, int64
   // 3: A = M M^T
   for (int64_t k0 = 0; k0 < in; k0 += kCB) {
     const int b = (int)std::min<int64_t>(kCB, in - k0);
-    AWQ_TRY(launch_pdl(chol_diag_kernel, 1, kCB * kCB, 0, st, A, in, k0, b, dev_status));
+    AWQ_TRY(launch_pdl(chol_diag_kernel, 1, kDiagThreads, 0, st, A, in, k0, b, dev_status));
     const int64_t rest = in - k0 - b;
     if (rest > 0) {
       AWQ_TRY(launch_pdl(chol_panel_kernel, (unsigned)((rest + 127) / 128), 128, 0, st, A, in, k0,
