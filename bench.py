@@ -356,9 +356,12 @@ def main():
     e2e_v = job_throughput(n_alpha, world, r["e2e_ms"])
     achieved = flops / (r["search_ms"] * 1e-3) / 1e12
     cpu_t, cpu_n = run_oracle_sample(cfg, oracle_sample_size(cfg, args.cpu_sample))
-    # statistics (with max|W| and the centring), alpha table, search, argmin, pack;
-    # a bf16 or fp32 X adds its fp16 copy
-    launches_per_step = 5 + (0 if cfg.dtype == "f16" else 1)
+    # statistics, max|W| (with the s table and the X / s copies where the
+    # search reads X pre-divided), the table of scalings, search, argmin,
+    # pack; without the pre-divided mode a bf16 or fp32 X adds its fp16 copy
+    xs_mode = (cfg.dtype in ("f16", "bf16") and cfg.N > 128 and cfg.group in (8, 16, 32, 64, 128)
+               and cfg.n_alpha * cfg.N * cfg.in_ * 2 <= 64 * 2 ** 20)
+    launches_per_step = 6 + (0 if xs_mode or cfg.dtype == "f16" else 1)
     line = {
         "metric": METRIC, "value": value, "unit": "layer-alpha-evals/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
@@ -421,12 +424,19 @@ def run_next_rows(args, cfg, tflops_peak, hbm_peak, peak_kind):
 
     t = timed(lambda: awq.awq_clip_search(Wd, Xd, s_best, cfg.bits, g, cfg.sym, 20, steps_c,
                                           check=False))
-    fl = 2.0 * out * n_in * g * (steps_c + 1) + 2.0 * n_in * g * N     # quadratic forms + Gram
+    if cfg.dtype in ("f16", "bf16") and g == 128 and 32 <= N <= 256:
+        # tensor cores: every factor's group errors times X / s, 2 N in out flops a factor
+        fl = 2.0 * N * n_in * out * (steps_c + 1)
+        clip_roof = {"bound": "tensor", "achieved": fl / t / 1e12, "peak": tflops_peak,
+                     "unit": "TFLOP/s", "frac": fl / t / 1e12 / tflops_peak, "peak_kind": peak_kind}
+    else:
+        fl = 2.0 * out * n_in * g * (steps_c + 1) + 2.0 * n_in * g * N  # quadratic forms + Gram
+        clip_roof = {"bound": "alu", "achieved": fl / t / 1e12, "peak": fp32_peak,
+                     "unit": "TFLOP/s", "frac": fl / t / 1e12 / fp32_peak,
+                     "peak_kind": "fp32 FMA lanes x max clock"}
     rows.append({"row": "clip_search", "metric": "group-factor-evals/s",
                  "value": out * (n_in // g) * (steps_c + 1) / t, "ms": t * 1e3,
-                 "roofline": {"bound": "alu", "achieved": fl / t / 1e12, "peak": fp32_peak,
-                              "unit": "TFLOP/s", "frac": fl / t / 1e12 / fp32_peak,
-                              "peak_kind": "fp32 FMA lanes x max clock"}})
+                 "roofline": clip_roof})
 
     t = timed(lambda: awq.awq_output_power(Wd, Xd, check=False))
     fl = 2.0 * N * n_in * out

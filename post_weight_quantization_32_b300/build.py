@@ -39,11 +39,11 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-# The search kernels split their registers between warpgroups with
-# setmaxnreg (128 threads x 48 + 256 threads x 200 + 128 threads x 56); that
-# split must fit in what the block is launched with, so every search kernel
-# has to be compiled to the full 128 registers a thread that its launch
-# bounds allow.
+# The search and tensor-core clipping kernels split their registers between
+# warpgroups with setmaxnreg (128 threads x 48 + 256 threads x 200 + 128
+# threads x 56 or 64); that split must fit in what the block is launched
+# with, so every such kernel has to be compiled to the full 128 registers a
+# thread that its launch bounds allow.
 SEARCH_KERNEL_REGS = 128
 
 
@@ -55,7 +55,7 @@ def _check_registers(src: str, text: str) -> None:
             current = m.group(1)
             continue
         m = re.search(r"Used (\d+) registers", line)
-        if m and current and "awq_search_kernel" in current:
+        if m and current and ("awq_search_kernel" in current or "clip_mma_kernel" in current):
             if int(m.group(1)) != SEARCH_KERNEL_REGS:
                 raise RuntimeError("%s: %s compiled to %s registers, the register split needs %d"
                                    % (os.path.basename(src), current, m.group(1), SEARCH_KERNEL_REGS))

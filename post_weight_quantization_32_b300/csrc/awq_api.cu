@@ -2,6 +2,7 @@
 // workspace layout, and the order of launches on the caller's stream.
 // Every entry point is an NVTX range named after it (header-only NVTX: a
 // no-op unless a profiler attaches), so timelines group the launches by call.
+#include <algorithm>
 #include <nvtx3/nvToolsExt.h>
 
 #include "awq.h"
@@ -347,7 +348,11 @@ int awq_quantize_pack_clipped(const void* W, int dtype, int64_t out, int64_t in,
 size_t awq_clip_search_workspace_bytes(int64_t in, int64_t N, int group) {
   if (in < 1 || N < 1 || (group != 32 && group != 64 && group != 128) || in % group != 0)
     return 0;
-  return align_up((size_t)clip_splits(N) * in * group * sizeof(float), 256);
+  // the Gram matrices of the FMA path, or what the tensor-core path needs
+  // (16-bit inputs, group 128, at most 256 tokens), whichever is larger
+  const size_t gram = align_up((size_t)clip_splits(N) * in * group * sizeof(float), 256);
+  const size_t mma = clip_mma_eligible(kDtF16, in, N, group) ? clip_mma_workspace_bytes(in, N) : 0;
+  return std::max(gram, mma);
 }
 
 int awq_clip_search(const void* W, const void* X, int dtype, int64_t out, int64_t in, int64_t N,
@@ -366,6 +371,11 @@ int awq_clip_search(const void* W, const void* X, int dtype, int64_t out, int64_
     return AWQ_ERR_INVALID_ARG;
   ClipFactors cf{};
   for (int i = 0; i <= max_shrink_steps; ++i) cf.c[i] = (float)(1.0 - (double)i / n_grid);
+  if (clip_mma_eligible(dtype, in, N, group) && out <= (1 << 24) &&
+      (reinterpret_cast<uintptr_t>(W) & 15) == 0 && (reinterpret_cast<uintptr_t>(X) & 15) == 0)
+    return cuda_status(launch_clip_search_mma(W, X, dtype, out, in, N, s, bits, sym ? 1 : 0,
+                                              max_shrink_steps + 1, cf, workspace, clip, errs,
+                                              dev_status, (cudaStream_t)stream));
   return cuda_status(launch_clip_search(W, X, dtype, out, in, N, s, bits, group, sym ? 1 : 0,
                                         max_shrink_steps + 1, cf, static_cast<float*>(workspace),
                                         clip, errs, dev_status, (cudaStream_t)stream));

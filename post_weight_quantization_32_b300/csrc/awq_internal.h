@@ -200,6 +200,14 @@ int clip_splits(int64_t N);
 // group's share of the row's output error for each of the nc factors of cf,
 // and clip[row][group] = the first factor with the smallest share; errs
 // ([out][in/group][nc], may be null) receives the shares.
+// The tensor-core clipping search (awq_clip_mma.cu): 16-bit W and X, group
+// 128, 32 to 256 tokens.  workspace: clip_mma_workspace_bytes(in, N).
+bool clip_mma_eligible(int dt, int64_t in, int64_t N, int group);
+size_t clip_mma_workspace_bytes(int64_t in, int64_t N);
+cudaError_t launch_clip_search_mma(const void* W, const void* X, int dt, int64_t out, int64_t in,
+                                   int64_t N, const float* s, int bits, int sym, int nf,
+                                   const ClipFactors& cf, void* workspace, float* clip, float* errs,
+                                   int32_t* dev_status, cudaStream_t stream);
 cudaError_t launch_clip_search(const void* W, const void* X, int dt, int64_t out, int64_t in,
                                int64_t N, const float* s, int bits, int group, int sym, int nc,
                                const ClipFactors& cf, float* H, float* clip, float* errs,

@@ -177,9 +177,13 @@ def test_clip_search_rejects_bad_arguments_on_host(lib):
     lib.awq_clip_search.restype = i32
     lib.awq_clip_search.argtypes = [vp, vp, i32, i64, i64, i64, vp, i32, i32, i32, i32, i32, vp, sz,
                                     vp, vp, vp, vp]
-    # Gram matrices: one g x g float block per group and token split of 256
-    assert lib.awq_clip_search_workspace_bytes(4096, 256, 128) == 4096 * 128 * 4
+    # Gram matrices (one g x g float block per group and token split of 256),
+    # or, for group 128 and at most 256 tokens, the tensor-core path's s * 2^e
+    # and 2^m / s rows, control words and fp16 copy of X / s if larger
+    assert lib.awq_clip_search_workspace_bytes(4096, 256, 128) == 2 * 4096 * 4 + 256 + 256 * 4096 * 2
+    assert lib.awq_clip_search_workspace_bytes(4096, 64, 128) == 4096 * 128 * 4
     assert lib.awq_clip_search_workspace_bytes(4096, 2048, 128) == 8 * 4096 * 128 * 4
+    assert lib.awq_clip_search_workspace_bytes(4096, 256, 64) == 4096 * 64 * 4
     assert lib.awq_clip_search_workspace_bytes(4096, 256, 256) == 0     # group not handled
     assert lib.awq_clip_search_workspace_bytes(100, 256, 32) == 0       # group does not divide in
     f = 1 << 20
