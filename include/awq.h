@@ -161,11 +161,16 @@ int awq_search(const void* W, const void* X, int dtype,
  *   workspace, workspace_bytes >= awq_output_power_workspace_bytes(dtype,
  *                               out, in, N) (256-byte aligned)
  *   power  [1] double (written)
- * X W^T is a plain GEMM (cuBLAS on the tensor cores: 16-bit operands with
- * float32 accumulation, float32 operands emulated to float32 accuracy)
- * written to the workspace as float32; its squares are summed in float64 in
- * a fixed order, so repeated calls give identical results.  dev_status is
- * not written (a NaN or infinite product shows in power).
+ * 16-bit W and X (in a multiple of 8, 16-byte aligned) take one tcgen05
+ * kernel: 128-row tiles of W against tiles of tokens, accumulated over all
+ * of `in` in tensor memory (float32), each entry squared as it leaves it and
+ * never stored; rows are summed in float64 and the tiles' sums added in a
+ * fixed order.  Other calls form X W^T as a plain GEMM (cuBLAS: float32
+ * operands emulated to float32 accuracy) in the workspace and sum its
+ * squares in float64 in a fixed order.  Either way repeated calls give
+ * identical results, and a NaN or infinite product shows in power.
+ * dev_status (may be NULL) is set to AWQ_ERR_TIMEOUT when a wait inside the
+ * tensor-core kernel runs past its limit.
  */
 size_t awq_output_power_workspace_bytes(int dtype, int64_t out, int64_t in, int64_t N);
 

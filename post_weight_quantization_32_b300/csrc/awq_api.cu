@@ -292,7 +292,6 @@ int awq_output_power(const void* W, const void* X, int dtype, int64_t out, int64
                      void* workspace, size_t workspace_bytes, double* power, int32_t* dev_status,
                      awq_stream_t stream) {
   const Range range("awq_output_power");
-  (void)dev_status;  // no device-side errors: a NaN or infinite product shows in *power
   if (!W || !X || !workspace || !power || !dtype_ok(dtype)) return AWQ_ERR_INVALID_ARG;
   if (out < 1 || in < 1 || N < 1) return AWQ_ERR_INVALID_ARG;
   if (workspace_bytes < awq_output_power_workspace_bytes(dtype, out, in, N) ||
@@ -300,6 +299,9 @@ int awq_output_power(const void* W, const void* X, int dtype, int64_t out, int64
     return AWQ_ERR_INVALID_ARG;
   if (out >= (1ll << 31) || N >= (1ll << 31) || in >= (1ll << 31)) return AWQ_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
+  if (power_mma_eligible(dtype, out, in, N, W, X) &&
+      workspace_bytes >= power_mma_workspace_bytes(out, N))
+    return cuda_status(launch_power_mma(W, X, dtype, out, in, N, workspace, power, dev_status, s));
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
   // D = X W^T ([N][out] float32, a plain GEMM), then mean(D^2) in float64
   float* D = reinterpret_cast<float*>(wsb);

@@ -39,9 +39,7 @@
 // rounded quotient; either neighbour is half a step away, so only that
 // entry's error changes sign, far below the fp16 rounding of the operands.
 #include <algorithm>
-#include <mutex>
 
-#include <cudaTypedefs.h>
 
 #include "awq_device.cuh"
 #include "awq_internal.h"
@@ -493,33 +491,6 @@ __global__ void __launch_bounds__(256) clip_xcopy_kernel(const T* __restrict__ X
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 clip_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult q;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-bool clip_map(CUtensorMap* m, CUtensorMapDataType t, const void* ptr, uint64_t cols, uint64_t rows,
-              uint32_t box_rows) {
-  auto enc = clip_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kCKB, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, t, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 // With fewer than 32 tokens a share is a sum of few squared dot products,
@@ -569,8 +540,9 @@ cudaError_t launch_clip_search_mma(const void* W, const void* X, int dt, int64_t
   CUtensorMap mw, mx;
   const CUtensorMapDataType wt =
       dt == kDtF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!clip_map(&mw, wt, W, (uint64_t)in, (uint64_t)out, kCRows) ||
-      !clip_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xs, (uint64_t)in, (uint64_t)N, (uint32_t)T))
+  if (!tensor_map_sw128(&mw, wt, W, (uint64_t)in, (uint64_t)out, (uint64_t)in * 2, kCKB, kCRows) ||
+      !tensor_map_sw128(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xs, (uint64_t)in, (uint64_t)N,
+                        (uint64_t)in * 2, kCKB, (uint32_t)T))
     return cudaErrorInvalidValue;
   ClipMmaArgs a{};
   a.out = (int)out;

@@ -1,6 +1,7 @@
 // Host-side interfaces between the C ABI (awq_api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -14,6 +15,13 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// 2-D tensor map of a row-major matrix [rows][cols] (row_bytes apart) with
+// box_cols x box_rows boxes in the 128-byte swizzled layout of a K-major
+// MMA operand; out-of-range elements read as zero.  False when the driver's
+// encoder is missing or rejects the arguments.
+bool tensor_map_sw128(CUtensorMap* m, CUtensorMapDataType t, const void* ptr, uint64_t cols,
+                      uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);
 
 // Launch with the programmatic-stream-serialization attribute: the kernel
 // may begin while the previous kernel in the stream is still running, and
@@ -239,6 +247,15 @@ cudaError_t blas_gemm(cudaStream_t s, int m, int n, int k, float alpha, const vo
                       int ta, const void* B, int64_t ldb, int tb, float beta, float* C, int64_t ldc,
                       int dt);
 
+// mean((X W^T)^2) by tcgen05 with the square sum in the epilogue (16-bit
+// W and X, in a multiple of 8, 16-byte aligned operands).  workspace:
+// power_mma_workspace_bytes(out, N), 256-byte aligned; its first 256 bytes
+// are zeroed by the launch.
+bool power_mma_eligible(int dt, int64_t out, int64_t in, int64_t N, const void* W, const void* X);
+size_t power_mma_workspace_bytes(int64_t out, int64_t N);
+cudaError_t launch_power_mma(const void* W, const void* X, int dt, int64_t out, int64_t in,
+                             int64_t N, void* workspace, double* power, int32_t* dev_status,
+                             cudaStream_t stream);
 // ---- output power (awq_prep.cu)
 // *power = sum over the n floats of D of D^2 (float64, a fixed order: the
 // grid's threads' strided sums, each CTA's tree, then the CTAs in order) /

@@ -93,7 +93,7 @@ constexpr int kMaxJobGroups = 4;  // groups a 64-column job can touch when they 
 // must not exceed the 512 * 128 = 65536 registers the block is launched
 // with (the build checks that every search kernel is compiled to 128
 // registers).
-constexpr uint32_t kRegsCtl = 48, kRegsProd = 200, kRegsEpi = 56;
+constexpr uint32_t kRegsCtl = 56, kRegsProd = 200, kRegsEpi = 56;
 constexpr uint32_t kLaunchRegs = 128;
 static_assert(128 * kRegsCtl + 256 * kRegsProd + 128 * kRegsEpi <= kThreads * kLaunchRegs,
               "register split");
@@ -325,35 +325,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     setmaxnreg_dec<kRegsCtl>();
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
       // ---------------------------------------------------------- W loader
-      uint32_t wc0 = 0, wc1 = 0;  // W blocks loaded into each warpgroup's bank
+      // (the whole warp runs the loop, the elected lane issues the copies)
+      uint32_t m0 = 0, ph0 = 0, m1 = 0, ph1 = 0;  // next stage of each bank and its phase
+      uint32_t wc0 = 0, wc1 = 0;                  // W blocks loaded into each bank
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
         const int rt = u / units_per_rt;
         const int ag = (u % units_per_rt) / p.n_tt;
         for (int kb = 0; kb < p.n_kb; ++kb) {
           const int b = (kb / KBJ) & 1;
-          const uint32_t m = b ? wc1 : wc0;
-          const uint32_t st = b * hw + m % hw, ph = (m / hw) & 1;
-          if (!mbar_wait(smem_addr(&c.w_empty[st]), ph ^ 1, abort, lim, p.diag, 1, m | (b << 30))) {
-            ok = false;
-            break;
+          const uint32_t st = b ? hw + m1 : m0, ph = b ? ph1 : ph0;
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&c.w_empty[st]), ph ^ 1, abort, lim,
+                                                 p.diag, 1, (b ? wc1 : wc0) | (b << 30)));
+          if (!ok) break;
+          if (elect_one()) {
+            const uint32_t bar = smem_addr(&c.w_full[st]);
+            mbar_arrive_expect_tx(bar, W_TILE + S_BYTES);
+            const uint32_t dst = w_ring + st * W_STAGE;
+            if (sizeof(WT) == 4) {
+              tma_load_2d(dst, &tmW, bar, kb * kKB, rt * kRows);
+              tma_load_2d(dst + W_TILE / 2, &tmW, bar, kb * kKB + 32, rt * kRows);
+            } else {
+              tma_load_2d(dst, &tmW, bar, kb * kKB, rt * kRows);
+            }
+            if (XS)
+              tma_load_2d(dst + W_TILE, &tmS, bar, kb * kKB, ag);
+            else
+              tma_load_3d(dst + W_TILE, &tmS, bar, kb * kKB, ag * p.a_per, 0);
           }
-          const uint32_t bar = smem_addr(&c.w_full[st]);
-          mbar_arrive_expect_tx(bar, W_TILE + S_BYTES);
-          const uint32_t dst = w_ring + st * W_STAGE;
-          if (sizeof(WT) == 4) {
-            tma_load_2d(dst, &tmW, bar, kb * kKB, rt * kRows);
-            tma_load_2d(dst + W_TILE / 2, &tmW, bar, kb * kKB + 32, rt * kRows);
+          __syncwarp();
+          if (b) {
+            ++wc1;
+            if (++m1 == hw) {
+              m1 = 0;
+              ph1 ^= 1;
+            }
           } else {
-            tma_load_2d(dst, &tmW, bar, kb * kKB, rt * kRows);
+            ++wc0;
+            if (++m0 == hw) {
+              m0 = 0;
+              ph0 ^= 1;
+            }
           }
-          if (XS)
-            tma_load_2d(dst + W_TILE, &tmS, bar, kb * kKB, ag);
-          else
-            tma_load_3d(dst + W_TILE, &tmS, bar, kb * kKB, ag * p.a_per, 0);
-          if (b) ++wc1; else ++wc0;
         }
       }
       int never_set = 0;  // drain: wait for the loads still in flight
@@ -362,86 +377,114 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t m = wc > hw ? wc - hw : 0; m < wc; ++m)
           mbar_wait(smem_addr(&c.w_full[b * hw + m % hw]), (m / hw) & 1, &never_set, lim);
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ---------------------------------------------------------- X loader
-      uint32_t seq = 0;
+      const uint32_t SX = (uint32_t)p.sx;
+      uint32_t seq = 0, st = 0, ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
         const int tt = (u % units_per_rt) % p.n_tt;
         const int ag = (u % units_per_rt) / p.n_tt;
         for (int kb = 0; kb < p.n_kb; ++kb) {
-          const uint32_t st = seq % p.sx, ph = (seq / p.sx) & 1;
-          if (!mbar_wait(smem_addr(&c.x_empty[st]), ph ^ 1, abort, lim, p.diag, 3, seq)) {
-            ok = false;
-            break;
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&c.x_empty[st]), ph ^ 1, abort, lim,
+                                                 p.diag, 3, seq));
+          if (!ok) break;
+          if (elect_one()) {
+            const uint32_t bar = smem_addr(&c.x_full[st]);
+            mbar_arrive_expect_tx(bar, X_STAGE);
+            if (XS)
+              tma_load_3d(x_ring + st * X_STAGE, &tmX, bar, kb * kKB, tt * p.T, ag);
+            else
+              tma_load_2d(x_ring + st * X_STAGE, &tmX, bar, kb * kKB, tt * p.T);
           }
-          const uint32_t bar = smem_addr(&c.x_full[st]);
-          mbar_arrive_expect_tx(bar, X_STAGE);
-          if (XS)
-            tma_load_3d(x_ring + st * X_STAGE, &tmX, bar, kb * kKB, tt * p.T, ag);
-          else
-            tma_load_2d(x_ring + st * X_STAGE, &tmX, bar, kb * kKB, tt * p.T);
+          __syncwarp();
           ++seq;
+          if (++st == SX) {
+            st = 0;
+            ph ^= 1;
+          }
         }
       }
       int never_set = 0;
-      for (uint32_t i = seq > (uint32_t)p.sx ? seq - p.sx : 0; i < seq; ++i)
-        mbar_wait(smem_addr(&c.x_full[i % p.sx]), (i / p.sx) & 1, &never_set, lim);
-    } else if (warp == 2 && lane == 0) {
+      for (uint32_t i = seq > SX ? seq - SX : 0; i < seq; ++i)
+        mbar_wait(smem_addr(&c.x_full[i % SX]), (i / SX) & 1, &never_set, lim);
+    } else if (warp == 2) {
       // ---------------------------------------------------------- MMA issuer
+      // The whole warp runs the loop (the elected lane issues) and the ring
+      // positions advance by counting, with no division in the loop.
       const uint32_t idesc = idesc_f16_f32(kRows, (uint32_t)p.T);
-      uint32_t xseq = 0, useq = 0;
-      uint32_t dc0 = 0, dc1 = 0;  // dW slots consumed from each warpgroup's bank
+      const uint32_t SX = (uint32_t)p.sx;
+      uint32_t x_st = 0, x_ph = 0;       // X stage and phase of the next unit's first block
+      uint32_t d0 = 0, dp0 = 0, d1 = 0, dp1 = 0;  // next dW slot and phase of each bank
+      uint32_t useq = 0;
       bool ok = true;
-      if (p.test_timeout) ok = mbar_wait(smem_addr(&c.never), 0, abort, lim, p.diag, 5, 0);
+      if (p.test_timeout)
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&c.never), 0, abort, lim, p.diag, 5, 0));
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
         const int ag = (u % units_per_rt) / p.n_tt;
         const int na = min(p.a_per, p.n_alpha - ag * p.a_per);
         if (useq > 0) {
-          if (!mbar_wait(smem_addr(&c.acc_empty), (useq - 1) & 1, abort, lim, p.diag, 6, useq)) {
-            ok = false;
-            break;
-          }
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&c.acc_empty), (useq - 1) & 1, abort,
+                                                 lim, p.diag, 6, useq));
+          if (!ok) break;
           tc_fence_after();
         }
         for (int kg = 0; ok && kg < n_kg; ++kg) {
           const int b = kg & 1;
           for (int a = 0; ok && a < na; ++a) {
+            uint32_t xs = x_st, xph = x_ph;
             for (int kbi = 0; kbi < KBJ; ++kbi) {
-              const uint32_t xq = xseq + kg * KBJ + kbi;
-              const uint32_t xs = xq % p.sx;
-              if (a == 0 &&
-                  !mbar_wait(smem_addr(&c.x_full[xs]), (xq / p.sx) & 1, abort, lim, p.diag, 7, xq)) {
-                ok = false;
-                break;
+              if (a == 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&c.x_full[xs]), xph, abort, lim,
+                                                       p.diag, 7, xs));
+                if (!ok) break;
               }
-              const uint32_t n = b ? dc1 : dc0;
-              const uint32_t ds = b * kBankSlots + n % kBankSlots;
-              if (!mbar_wait(smem_addr(&c.d_full[ds]), (n / kBankSlots) & 1, abort, lim, p.diag, 8,
-                             n | (b << 30))) {
-                ok = false;
-                break;
-              }
+              const uint32_t slot = b ? d1 : d0, sph = b ? dp1 : dp0;
+              const uint32_t ds = b * kBankSlots + slot;
+              ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&c.d_full[ds]), sph, abort, lim,
+                                                     p.diag, 8, slot | (b << 30)));
+              if (!ok) break;
               tc_fence_after();
               const uint32_t d_t = tmem + (uint32_t)(a * p.T);
               const uint32_t a_t = tmem + kSlotCol0 + ds * 32u;
               const uint64_t bdesc = smem_desc_sw128(x_ring + xs * X_STAGE);
 #pragma unroll
               for (int k = 0; k < kKB / 16; ++k)
-                umma_ts(d_t, a_t + 8u * k, bdesc + (uint64_t)(2 * k), idesc,
-                        (kg | kbi | k) != 0 ? 1u : 0u);
-              umma_commit(smem_addr(&c.d_empty[ds]));
-              if (a == na - 1) umma_commit(smem_addr(&c.x_empty[xs]));
-              if (b) ++dc1; else ++dc0;
+                umma_ts_elect(d_t, a_t + 8u * k, bdesc + (uint64_t)(2 * k), idesc,
+                              (kg | kbi | k) != 0 ? 1u : 0u);
+              umma_commit_elect(smem_addr(&c.d_empty[ds]));
+              if (a == na - 1) umma_commit_elect(smem_addr(&c.x_empty[xs]));
+              if (b) {
+                if (++d1 == (uint32_t)kBankSlots) {
+                  d1 = 0;
+                  dp1 ^= 1;
+                }
+              } else {
+                if (++d0 == (uint32_t)kBankSlots) {
+                  d0 = 0;
+                  dp0 ^= 1;
+                }
+              }
+              if (++xs == SX) {
+                xs = 0;
+                xph ^= 1;
+              }
+            }
+          }
+          // the next job's X blocks follow this job's KBJ blocks in the ring
+#pragma unroll
+          for (int kbi = 0; kbi < KBJ; ++kbi) {
+            if (++x_st == SX) {
+              x_st = 0;
+              x_ph ^= 1;
             }
           }
         }
         if (!ok) break;
-        xseq += p.n_kb;
-        umma_commit(smem_addr(&c.acc_full));
+        umma_commit_elect(smem_addr(&c.acc_full));
         ++useq;
       }
-      umma_commit(smem_addr(&c.drain));
+      umma_commit_elect(smem_addr(&c.drain));
       int never_set = 0;
       mbar_wait(smem_addr(&c.drain), 0, &never_set, lim);
     }
@@ -810,6 +853,11 @@ int max_dyn_smem() {
 }
 
 }  // namespace
+
+bool tensor_map_sw128(CUtensorMap* m, CUtensorMapDataType t, const void* ptr, uint64_t cols,
+                      uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
+  return make_map(m, t, ptr, cols, rows, row_bytes, box_cols, box_rows);
+}
 
 bool search_wide_group(int64_t group, int64_t in) {
   return in % 8 == 0 && group > 0 && in % group == 0 && (group % 256 == 0 || group == in);

@@ -230,15 +230,45 @@ def test_search_wide_groups_match_oracle(awq, case):
     check_pack(awq, W, res.s32[b], bits, n_in if group is None else group, sym)
 
 
+# 16-bit layers take the tensor-core kernel (token tiles of 32, 64, 128 or
+# 256; two K blocks a ring stage below 256): (256, 512, 64) 64-token tiles;
+# (300, 1032, 300) ragged rows, tokens and K (1032 = 16 blocks of 64 + 8, the
+# last stage's second block all zeros); (2048, 2048, 1024) 256 units, more
+# than one a CTA, so both accumulators alternate; (9600, 136, 250) 128-token
+# tiles; (19000, 64, 256) 256-token tiles, one K block; (130, 264, 17) a
+# 32-token tile for 17 tokens; (1, 64, 1) one row and one token.  float32
+# takes the GEMM route.
 @pytest.mark.parametrize("dtype,shape", [("f16", (256, 512, 64)), ("bf16", (300, 1032, 300)),
+                                         ("f16", (2048, 2048, 1024)), ("f16", (9600, 136, 250)),
+                                         ("bf16", (19000, 64, 256)), ("bf16", (130, 264, 17)),
                                          ("f32", (96, 256, 17)), ("bf16", (1, 64, 1))])
 def test_output_power_matches_oracle(awq, dtype, shape):
     out, n_in, N = shape
     W, X = make_random_layer(out, n_in, N, dtype=dtype, seed=out * 3 + N,
                              n_outlier=max(1, n_in // 64))
-    p = float(awq.awq_output_power(*_dev(W, X)).item())
+    Wd, Xd = _dev(W, X)
+    p = awq.awq_output_power(Wd, Xd)
     ref = O.output_power(_np_w(W), _np_x(X))
-    assert abs(p - ref) <= ERR_RTOL * ref, (p, ref)
+    assert abs(float(p.item()) - ref) <= ERR_RTOL * ref, (float(p.item()), ref)
+    # a fixed summation order: a second call gives the same bits
+    assert torch.equal(awq.awq_output_power(Wd, Xd).view(torch.int64), p.view(torch.int64))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_output_power_routes_agree(awq, dtype):
+    """X two bytes off a 16-byte boundary cannot be read by TMA: the call
+    takes the GEMM route instead, and the two routes agree."""
+    W, X = make_random_layer(384, 1024, 200, dtype=dtype, seed=5, n_outlier=16)
+    Wd, Xd = _dev(W, X)
+    buf = torch.empty(Xd.numel() + 1, dtype=Xd.dtype, device=Xd.device)
+    Xm = buf[1:].view(Xd.shape)
+    Xm.copy_(Xd)
+    assert Xm.data_ptr() % 16 != 0
+    p_tc = float(awq.awq_output_power(Wd, Xd).item())
+    p_gemm = float(awq.awq_output_power(Wd, Xm).item())
+    ref = O.output_power(_np_w(W), _np_x(X))
+    assert abs(p_tc - ref) <= ERR_RTOL * ref and abs(p_gemm - ref) <= ERR_RTOL * ref
+    assert abs(p_tc - p_gemm) <= 1e-4 * ref, (p_tc, p_gemm)
 
 
 def test_sweep_matches_oracle(awq):
