@@ -88,15 +88,6 @@ struct ClipMmaArgs {
   uint64_t wait_limit_ns;
 };
 
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -184,29 +175,35 @@ __global__ void __launch_bounds__(kCThreads, 1)
 
   if (warp < 4) {
     setmaxnreg_dec<kCRegsCtl>();
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
       // ---------------------------------------------------------- loader
+      // (the whole warp runs the loop, the elected lane issues the copies)
       uint32_t wq = 0, xq = 0;
       bool ok = true;
       for (int it = i0; ok && it < i1; ++it) {
         const int rt = it / p.ngroups, g = it % p.ngroups;
         for (int kb = 0; ok && kb < 2; ++kb) {
           const uint32_t ws = wq % kCSW, wph = (wq / kCSW) & 1;
-          if (!mbar_wait(smem_addr(&c.w_empty[ws]), wph ^ 1, abort, lim, p.diag, 21, wq)) {
-            ok = false;
-            break;
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&c.w_empty[ws]), wph ^ 1, abort, lim,
+                                                 p.diag, 21, wq));
+          if (!ok) break;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(smem_addr(&c.w_full[ws]), kCW_TILE);
+            tma_load_2d(w_ring + ws * kCW_TILE, &tmW, smem_addr(&c.w_full[ws]),
+                        g * kCG + kb * kCKB, rt * kCRows);
           }
-          mbar_arrive_expect_tx(smem_addr(&c.w_full[ws]), kCW_TILE);
-          tma_load_2d(w_ring + ws * kCW_TILE, &tmW, smem_addr(&c.w_full[ws]), g * kCG + kb * kCKB,
-                      rt * kCRows);
+          __syncwarp();
           ++wq;
           const uint32_t xs = xq % kCSX, xph = (xq / kCSX) & 1;
-          if (!mbar_wait(smem_addr(&c.x_empty[xs]), xph ^ 1, abort, lim, p.diag, 22, xq)) {
-            ok = false;
-            break;
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&c.x_empty[xs]), xph ^ 1, abort, lim,
+                                                 p.diag, 22, xq));
+          if (!ok) break;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(smem_addr(&c.x_full[xs]), X_STAGE);
+            tma_load_2d(x_ring + xs * X_STAGE, &tmX, smem_addr(&c.x_full[xs]),
+                        g * kCG + kb * kCKB, 0);
           }
-          mbar_arrive_expect_tx(smem_addr(&c.x_full[xs]), X_STAGE);
-          tma_load_2d(x_ring + xs * X_STAGE, &tmX, smem_addr(&c.x_full[xs]), g * kCG + kb * kCKB, 0);
+          __syncwarp();
           ++xq;
         }
       }
@@ -215,7 +212,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
         mbar_wait(smem_addr(&c.w_full[m % kCSW]), (m / kCSW) & 1, &never_set, lim);
       for (uint32_t m = xq > kCSX ? xq - kCSX : 0; m < xq; ++m)
         mbar_wait(smem_addr(&c.x_full[m % kCSX]), (m / kCSX) & 1, &never_set, lim);
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
       const uint32_t idesc = idesc_f16_f32(kCRows, (uint32_t)p.T);
       uint32_t xq = 0, fq = 0;  // X blocks and factors consumed
@@ -224,16 +221,19 @@ __global__ void __launch_bounds__(kCThreads, 1)
         uint32_t xs[2];
         for (int kb = 0; ok && kb < 2; ++kb) {
           xs[kb] = (xq + kb) % kCSX;
-          ok = mbar_wait(smem_addr(&c.x_full[xs[kb]]), ((xq + kb) / kCSX) & 1, abort, lim, p.diag,
-                         23, xq + kb);
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&c.x_full[xs[kb]]),
+                                                 ((xq + kb) / kCSX) & 1, abort, lim, p.diag, 23,
+                                                 xq + kb));
         }
         if (!ok) break;
         for (int f = 0; ok && f < nf; ++f) {
           const uint32_t sl = fq % kCSlots, acc = fq & 1;
-          ok = mbar_wait(smem_addr(&c.d_full[sl]), (fq / kCSlots) & 1, abort, lim, p.diag, 24, fq);
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&c.d_full[sl]), (fq / kCSlots) & 1,
+                                                 abort, lim, p.diag, 24, fq));
           if (ok && fq >= 2)
-            ok = mbar_wait(smem_addr(&c.acc_empty[acc]), ((fq - 2) / 2) & 1, abort, lim, p.diag,
-                           25, fq);
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&c.acc_empty[acc]),
+                                                   ((fq - 2) / 2) & 1, abort, lim, p.diag, 25,
+                                                   fq));
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_t = tmem + acc * 256u;
@@ -243,19 +243,19 @@ __global__ void __launch_bounds__(kCThreads, 1)
             const uint64_t bdesc = smem_desc_sw128(x_ring + xs[kb] * X_STAGE);
 #pragma unroll
             for (int k = 0; k < kCKB / 16; ++k)
-              umma_ss(d_t, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
-                      (kb | k) != 0 ? 1u : 0u);
+              umma_ss_elect(d_t, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
+                            (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit(smem_addr(&c.d_empty[sl]));
-          umma_commit(smem_addr(&c.acc_full[acc]));
+          umma_commit_elect(smem_addr(&c.d_empty[sl]));
+          umma_commit_elect(smem_addr(&c.acc_full[acc]));
           ++fq;
         }
         if (!ok) break;
-        umma_commit(smem_addr(&c.x_empty[xs[0]]));
-        umma_commit(smem_addr(&c.x_empty[xs[1]]));
+        umma_commit_elect(smem_addr(&c.x_empty[xs[0]]));
+        umma_commit_elect(smem_addr(&c.x_empty[xs[1]]));
         xq += 2;
       }
-      umma_commit(smem_addr(&c.drain));
+      umma_commit_elect(smem_addr(&c.drain));
       int never_set = 0;
       mbar_wait(smem_addr(&c.drain), 0, &never_set, lim);
     }
