@@ -324,6 +324,217 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (threadIdx.x == 0 && c.abort) set_status(p.status, ST_TIMEOUT);
 }
 
+// ---- split-K form, for layers with fewer 128 x NT tiles than SMs ----------
+// The KS CTAs of a cluster share one tile (128 W rows x NT tokens): CTA r
+// accumulates K blocks [r n_kb / KS, (r + 1) n_kb / KS) in tensor memory and
+// stages its float32 accumulator in its own shared memory (over the drained
+// ring) as [NT / 4][128 rows][4 tokens], so that a row's four consecutive
+// tokens are one 16-byte vector and a warp's vectors are contiguous.  After a cluster barrier CTA r forms,
+// for tokens [r NT / KS, (r + 1) NT / KS), the sum of the KS partial
+// products in rank order, squares it and sums its rows; every output entry
+// is formed in one fixed order.  Each CTA writes one float64 partial and a
+// one-CTA launch adds them in order.  Wide tiles read W once per NT tokens
+// from shared memory, where 64-token tiles were bound by shared-memory
+// bandwidth (each 64-column block written by TMA and read by the MMA).
+struct SplitArgs {
+  int n_kb;          // K blocks of the layer
+  int n_tt;          // token tiles
+  double* partials;  // [grid]
+  uint32_t* diag;
+  int32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+template <int NT> struct SplitTile {
+  static constexpr uint32_t kX = (uint32_t)NT * 128u;
+  static constexpr uint32_t kStage = kPWTile + kX;
+  static constexpr int kStages =
+      (int)(kPRingBudget / kStage) < kPMaxStages ? (int)(kPRingBudget / kStage) : kPMaxStages;
+  static constexpr size_t kSmem = kPCtrl + 1024 + (size_t)kStages * kStage;
+  static_assert((size_t)NT * 128 * 4 <= (size_t)kStages * kStage, "staging must fit the ring");
+};
+
+template <bool BF16, int NT, int KS>
+__global__ void __launch_bounds__(kPThreads, 1)
+    power_split_kernel(const __grid_constant__ CUtensorMap tmW,
+                       const __grid_constant__ CUtensorMap tmX, const SplitArgs p) {
+  using Tile = SplitTile<NT>;
+  constexpr uint32_t S = (uint32_t)Tile::kStages;
+  extern __shared__ uint8_t psmem_raw[];
+  const uint32_t raw = smem_addr(psmem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  PowCtrl& c = *reinterpret_cast<PowCtrl*>(psmem_raw + (base - raw));
+  const uint32_t ring = base + kPCtrl;
+  float* staged = reinterpret_cast<float*>(psmem_raw + (base - raw) + kPCtrl);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int tile = blockIdx.x / KS;
+  const int rt = tile / p.n_tt, tt = tile - (tile / p.n_tt) * p.n_tt;
+  const int kb0 = (int)((int64_t)rank * p.n_kb / KS);
+  const int kb1 = (int)((int64_t)(rank + 1) * p.n_kb / KS);
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    for (uint32_t i = 0; i < S; ++i) {
+      mbar_init(smem_addr(&c.full[i]), 1);
+      mbar_init(smem_addr(&c.empty[i]), 1);
+    }
+    mbar_init(smem_addr(&c.acc_full[0]), 1);
+    mbar_init(smem_addr(&c.drain), 1);
+    c.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(&c.tmem_base), NT);
+    tmem_relinquish();
+  }
+  if (warp == 1 && lane == 0) {
+    tma_prefetch_map(&tmW);
+    tma_prefetch_map(&tmX);
+  }
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();  // W and X may come from earlier kernels
+  const uint32_t tmem = c.tmem_base;
+  volatile int* abort = &c.abort;
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- loader
+    uint32_t q = 0, st = 0, ph = 0;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&c.empty[st]), ph ^ 1, abort, lim, p.diag,
+                                             45, q)))
+        break;
+      const uint32_t dst = ring + st * Tile::kStage;
+      tma_stage_elect(smem_addr(&c.full[st]), Tile::kStage, dst, dst + kPWTile, &tmW, &tmX,
+                      kb * kPKB, rt * kPRows, tt * NT);
+      ++q;
+      if (++st == S) {
+        st = 0;
+        ph ^= 1;
+      }
+    }
+    int never_set = 0;  // drain the copies still in flight
+    for (uint32_t m = q > S ? q - S : 0; m < q; ++m)
+      mbar_wait(smem_addr(&c.full[m % S]), (m / S) & 1, &never_set, lim);
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc = idesc_16bit(kPRows, (uint32_t)NT, BF16);
+    uint32_t q = 0, st = 0, ph = 0;
+    bool ok = true;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(smem_addr(&c.full[st]), ph, abort, lim, p.diag, 46, q));
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t adesc = smem_desc_sw128(ring + st * Tile::kStage);
+      const uint64_t bdesc = smem_desc_sw128(ring + st * Tile::kStage + kPWTile);
+#pragma unroll
+      for (int k = 0; k < kPKB / 16; ++k)
+        umma_ss_elect(tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
+                      (kb > kb0 || k > 0) ? 1u : 0u);
+      umma_commit_elect(smem_addr(&c.empty[st]));
+      ++q;
+      if (++st == S) {
+        st = 0;
+        ph ^= 1;
+      }
+    }
+    if (ok) umma_commit_elect(smem_addr(&c.acc_full[0]));
+    umma_commit_elect(smem_addr(&c.drain));
+    int never_set = 0;
+    mbar_wait(smem_addr(&c.drain), 0, &never_set, lim);
+  } else {
+    // ------------------------------------------- epilogue: stage the product
+    const int qd = warp & 3;
+    const int row = qd * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(qd * 32) << 16;
+    const bool ok = mbar_wait(smem_addr(&c.acc_full[0]), 0, abort, lim, p.diag, 47, 0);
+    if (epi_all(ok)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int cc = 0; cc < NT; cc += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_addr + (uint32_t)cc, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4*>(staged + ((cc + i) / 4 * 128 + row) * 4) =
+              make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                          __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+      }
+      tc_fence_before();
+    }
+  }
+  cluster_sync_all();  // every CTA's partial product is staged
+  if (warp >= 2) {
+    // ------------------------ this CTA's token slice, summed over the cluster
+    constexpr int SL = NT / KS;
+    const int e = warp - 2;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t loc = smem_addr(staged) + (uint32_t)(((int)rank * SL / 4 * 128 + row) * 16);
+    uint32_t src[KS];
+#pragma unroll
+    for (int r = 0; r < KS; ++r) src[r] = map_shared_rank(loc, (uint32_t)r);
+    double rs = 0.0;
+#pragma unroll 1
+    for (int c0 = 0; c0 < SL; c0 += 16) {
+      float4 v[4][KS];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int r = 0; r < KS; ++r)
+          v[i][r] = ld_shared_cluster_f32x4(src[r] + (uint32_t)(((c0 / 4 + i) * 128) * 16));
+      float s16 = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);  // the partial products in rank order
+#pragma unroll
+        for (int r = 0; r < KS; ++r) {
+          t.x += v[i][r].x;
+          t.y += v[i][r].y;
+          t.z += v[i][r].z;
+          t.w += v[i][r].w;
+        }
+        s16 = fmaf(t.x, t.x, s16);
+        s16 = fmaf(t.y, t.y, s16);
+        s16 = fmaf(t.z, t.z, s16);
+        s16 = fmaf(t.w, t.w, s16);
+      }
+      rs += (double)s16;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+    if (lane == 0) c.red[e] = rs;
+    epi_sync();
+    if (e == 0 && lane == 0)
+      p.partials[blockIdx.x] = ((c.red[0] + c.red[1]) + c.red[2]) + c.red[3];
+  }
+  cluster_sync_all();  // the other CTAs are done reading this one's staging
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, NT);
+  }
+  if (threadIdx.x == 0 && c.abort) set_status(p.status, ST_TIMEOUT);
+}
+
+// power = (sum of the n partials in a fixed order) / denom; one CTA.
+__global__ void __launch_bounds__(256) power_finish_kernel(const double* __restrict__ partials,
+                                                           int n, double denom,
+                                                           double* __restrict__ power) {
+  pdl_wait();
+  __shared__ double red[256];
+  double s = 0.0;
+  for (int i = threadIdx.x; i < n; i += 256) s += partials[i];
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *power = red[0] / denom;
+}
+
 // Tokens a tile: the largest of 256, 128 and 64 that still gives every SM a
 // unit (fewer tokens a tile re-read W from L2 more often), halved while the
 // tile would still hold all N tokens, down to 32.
@@ -367,6 +578,46 @@ cudaError_t launch_power_dt(int nt, const CUtensorMap& mw, const CUtensorMap& mx
   }
 }
 
+// Split-K plan: 256-token tiles (N > 128) or 128-token tiles (64 < N <= 128),
+// KS = 4 or 2 when that many CTAs per tile still fit one a SM and each
+// keeps at least four K blocks; ks = 0 leaves the layer to the persistent
+// kernel.
+void split_plan(int64_t out, int64_t in, int64_t N, int sms, int& nt, int& ks) {
+  nt = 0;
+  ks = 0;
+  if (N <= 64) return;
+  nt = N > 128 ? 256 : 128;
+  const int64_t tiles = ((out + kPRows - 1) / kPRows) * ((N + nt - 1) / nt);
+  const int64_t n_kb = (in + kPKB - 1) / kPKB;
+  for (int cand : {4, 2}) {
+    if (tiles * cand <= sms && n_kb >= 4 * cand) {
+      ks = cand;
+      return;
+    }
+  }
+}
+
+template <bool BF16, int NT, int KS>
+cudaError_t launch_split_tile(const CUtensorMap& mw, const CUtensorMap& mx, const SplitArgs& a,
+                              int grid, cudaStream_t stream) {
+  auto k = power_split_kernel<BF16, NT, KS>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SplitTile<NT>::kSmem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl_cluster(k, dim3((unsigned)grid), (unsigned)KS, dim3(kPThreads),
+                            SplitTile<NT>::kSmem, stream, mw, mx, a);
+}
+
+template <bool BF16>
+cudaError_t launch_split_dt(int nt, int ks, const CUtensorMap& mw, const CUtensorMap& mx,
+                            const SplitArgs& a, int grid, cudaStream_t stream) {
+  if (nt == 256)
+    return ks == 4 ? launch_split_tile<BF16, 256, 4>(mw, mx, a, grid, stream)
+                   : launch_split_tile<BF16, 256, 2>(mw, mx, a, grid, stream);
+  return ks == 4 ? launch_split_tile<BF16, 128, 4>(mw, mx, a, grid, stream)
+                 : launch_split_tile<BF16, 128, 2>(mw, mx, a, grid, stream);
+}
+
 }  // namespace
 
 bool power_mma_eligible(int dt, int64_t out, int64_t in, int64_t N, const void* W, const void* X) {
@@ -376,7 +627,10 @@ bool power_mma_eligible(int dt, int64_t out, int64_t in, int64_t N, const void* 
 }
 
 size_t power_mma_workspace_bytes(int64_t out, int64_t N) {
-  return 256 + (size_t)power_units(out, N, 32) * 8;  // the smallest tile gives the most units
+  // the partials: one per unit of the persistent kernel (the smallest tile
+  // gives the most), or one per CTA of the split form (at most four per
+  // 128-token tile)
+  return 256 + (size_t)(power_units(out, N, 32) + 4 * power_units(out, N, 128)) * 8;
 }
 
 cudaError_t launch_power_mma(const void* W, const void* X, int dt, int64_t out, int64_t in,
@@ -384,17 +638,43 @@ cudaError_t launch_power_mma(const void* W, const void* X, int dt, int64_t out, 
                              cudaStream_t stream) {
   if (!power_mma_eligible(dt, out, in, N, W, X)) return cudaErrorInvalidValue;
   const int sms = device_sm_count();
+  const CUtensorMapDataType t =
+      dt == kDtF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  {
+    int snt, ks;
+    split_plan(out, in, N, sms, snt, ks);
+    if (ks > 0) {
+      CUtensorMap mw, mx;
+      if (!tensor_map_sw128(&mw, t, W, (uint64_t)in, (uint64_t)out, (uint64_t)in * 2, kPKB,
+                            kPRows) ||
+          !tensor_map_sw128(&mx, t, X, (uint64_t)in, (uint64_t)N, (uint64_t)in * 2, kPKB,
+                            (uint32_t)snt))
+        return cudaErrorInvalidValue;
+      SplitArgs a{};
+      a.n_kb = (int)((in + kPKB - 1) / kPKB);
+      a.n_tt = (int)((N + snt - 1) / snt);
+      const int grid = (int)(((out + kPRows - 1) / kPRows) * a.n_tt * ks);
+      // words 16..19 of the control area: wait diagnostics; partials from byte 256
+      a.partials = reinterpret_cast<double*>(wsb + 256);
+      a.diag = reinterpret_cast<uint32_t*>(wsb) + 16;
+      a.status = dev_status;
+      a.wait_limit_ns = 2000000000ull;
+      cudaError_t e = dt == kDtF16 ? launch_split_dt<false>(snt, ks, mw, mx, a, grid, stream)
+                                   : launch_split_dt<true>(snt, ks, mw, mx, a, grid, stream);
+      if (e != cudaSuccess) return e;
+      return launch_pdl(power_finish_kernel, 1, 256, 0, stream, a.partials, grid,
+                        (double)N * (double)out, power);
+    }
+  }
   const int nt = power_token_tile(out, N, sms);
   const int64_t n_units = power_units(out, N, nt);
   if (n_units >= (1ll << 31)) return cudaErrorInvalidValue;
-  uint8_t* wsb = static_cast<uint8_t*>(workspace);
   // control area (256 bytes): the ticket at word 0, wait diagnostics at
   // words 16..19; the partials from byte 256
   cudaError_t e = cudaMemsetAsync(wsb, 0, 256, stream);
   if (e != cudaSuccess) return e;
   CUtensorMap mw, mx;
-  const CUtensorMapDataType t =
-      dt == kDtF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!tensor_map_sw128(&mw, t, W, (uint64_t)in, (uint64_t)out, (uint64_t)in * 2, kPKB, kPRows) ||
       !tensor_map_sw128(&mx, t, X, (uint64_t)in, (uint64_t)N, (uint64_t)in * 2, kPKB,
                         (uint32_t)nt))
