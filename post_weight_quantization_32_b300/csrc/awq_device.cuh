@@ -302,35 +302,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       : "memory");
 }
 
-// ---------------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster: arrive with release semantics,
-// then wait with acquire semantics (shared-memory writes before it are
-// visible to the whole cluster after it).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
-}
-// The address in CTA `rank`'s shared memory that corresponds to this CTA's
-// shared-memory address `a`.
-__device__ __forceinline__ uint32_t map_shared_rank(uint32_t a, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float4 ld_shared_cluster_f32x4(uint32_t a) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(a)
-               : "memory");
-  return v;
-}
-
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
 // layout (rows of 128 bytes, 8-row groups 1024 bytes apart).  Bits: start
 // address >> 4 at [0,14), leading byte offset >> 4 at [16,30) (unused for
