@@ -320,6 +320,11 @@ __global__ void __launch_bounds__(kSRows * kSLanes, 2) sweep_block_kernel(
   __syncthreads();
   const float Lf = (float)((1 << (bits - 1)) - 1), maxqf = (float)((1 << bits) - 1);
   const int64_t ng = in / group;
+  // group is 32, 64 or 128 and b0 a multiple of kSB (128), so column b0 + i
+  // starts a group exactly when i is a multiple of group: a mask test per
+  // column instead of a 64-bit remainder
+  const int gmask = group - 1;
+  const int64_t g0 = b0 / group;
   float scale = 1.0f, zero = 0.0f;
   constexpr unsigned FULL = 0xffffffffu;
 #pragma unroll
@@ -328,8 +333,7 @@ __global__ void __launch_bounds__(kSRows * kSLanes, 2) sweep_block_kernel(
     for (int o = 0; o < kSLanes; ++o) {
       const int i = kSLanes * ki + o;
       if (i < bw) {
-        const int64_t col = b0 + i;
-        if (col % group == 0) {  // fit the group on the corrected weights
+        if ((i & gmask) == 0) {  // fit the group on the corrected weights
           float m = 0.0f, lo = 0.0f, hi = 0.0f;
 #pragma unroll
           for (int k = ki; k < kSOwn; ++k) {
@@ -354,8 +358,9 @@ __global__ void __launch_bounds__(kSRows * kSLanes, 2) sweep_block_kernel(
             zero = rintf(__fdiv_rn(-lo, scale));
           }
           if (live && q == 0) {
-            scales[row * ng + col / group] = scale;
-            zeros[row * ng + col / group] = (uint8_t)(sym ? (1 << (bits - 1)) : (int)zero);
+            const int64_t gi = row * ng + g0 + i / group;
+            scales[gi] = scale;
+            zeros[gi] = (uint8_t)(sym ? (1 << (bits - 1)) : (int)zero);
           }
         }
         const float wi = __shfl_sync(FULL, w[ki], base | o);
