@@ -495,7 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // tensor memory lanes 32q .. 32q+31
     const int row = q * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-    uint32_t wm = 0, dn = 0;  // this warpgroup's W-block and dW-slot counters
+    // the next W stage of this warpgroup's bank and its phase (counted: the
+    // bank's stages are used in order), and the dW-slot counter
+    uint32_t wsl = 0, wph = 0, dn = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       const int rem = u % units_per_rt;
@@ -508,14 +510,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float clampk = XS ? 1e-8f * __ldg(wa.escale + ag) : 1e-8f;
       for (int kg = wg; ok && kg < n_kg; kg += 2) {
         const uint8_t* stg[KBJ];
+        uint32_t wst[KBJ];
 #pragma unroll
         for (int kbi = 0; kbi < KBJ; ++kbi) {
-          const uint32_t m = wm + kbi;
-          const uint32_t st = wg * hw + m % hw;
+          uint32_t sl = wsl + kbi, ph = wph;  // KBJ <= hw: at most one wrap
+          if (sl >= hw) {
+            sl -= hw;
+            ph ^= 1;
+          }
+          const uint32_t st = wg * hw + sl;
+          wst[kbi] = st;
           stg[kbi] = w_ring_ptr + st * W_STAGE;
           if (ok)
-            ok = mbar_wait(smem_addr(&c.w_full[st]), (m / hw) & 1, abort, lim, p.diag, 10,
-                           m | (wg << 30));
+            ok = mbar_wait(smem_addr(&c.w_full[st]), ph, abort, lim, p.diag, 10, sl | (wg << 30));
         }
         ok = __all_sync(FULL, ok);
         if (!ok) break;
@@ -591,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
               for (int kbi = 0; kbi < KBJ; ++kbi)
-                mbar_arrive(smem_addr(&c.w_empty[wg * hw + (wm + kbi) % hw]));
+                mbar_arrive(smem_addr(&c.w_empty[wst[kbi]]));
           }
           // group steps
           float scl[NG], rcp[NG], chi[NG];
@@ -664,9 +671,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0)
             for (int kbi = 0; kbi < KBJ; ++kbi)
-              mbar_arrive(smem_addr(&c.w_empty[wg * hw + (wm + kbi) % hw]));
+              mbar_arrive(smem_addr(&c.w_empty[wst[kbi]]));
         }
-        wm += KBJ;
+        wsl += KBJ;
+        if (wsl >= hw) {
+          wsl -= hw;
+          wph ^= 1;
+        }
       }
     }
   } else {
