@@ -508,6 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.pow2_s[ag * p.a_per + a] != 0) exact_mask |= 1u << a;
       // the step's lower clamp 1e-8, scaled like t (XS: one alpha per unit)
       const float clampk = XS ? 1e-8f * __ldg(wa.escale + ag) : 1e-8f;
+      // this thread's W row, for the group ranges read from memory (GP, GV)
+      const int64_t grow = (GP || GV) ? min((int64_t)(u / units_per_rt) * kRows + row,
+                                            (int64_t)p.out - 1)
+                                      : 0;
       for (int kg = wg; ok && kg < n_kg; kg += 2) {
         const uint8_t* stg[KBJ];
         uint32_t wst[KBJ];
@@ -536,10 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 4; ++j) r0[g][j] = r1[g][j] = 0.0f;
           if constexpr (GP) {  // the group's extremes over all its jobs (loaded before pass 1
                                // so that the load overlaps it)
-            const int64_t grow =
-                min((int64_t)(u / units_per_rt) * kRows + row, (int64_t)p.out - 1);
             const int64_t gi = ((int64_t)(ag * p.a_per + a) * p.out + grow) * wa.ngroups +
-                               (int64_t)kg * JC / wa.group;
+                               (kg * JC) / wa.group;  // kg * JC < in <= 2^24
             if (SYM) {
               r0[0][0] = __ldg(wa.gext + gi);
             } else {
@@ -554,8 +556,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col0 = kg * JC;
             vg0 = col0 / wa.group;
             vgn = min((col0 + JC - 1) / wa.group, wa.ngroups - 1) - vg0 + 1;
-            const int64_t grow =
-                min((int64_t)(u / units_per_rt) * kRows + row, (int64_t)p.out - 1);
             const int64_t gi0 = ((int64_t)(ag * p.a_per + a) * p.out + grow) * wa.ngroups + vg0;
 #pragma unroll
             for (int i = 0; i < kMaxJobGroups; ++i) {
