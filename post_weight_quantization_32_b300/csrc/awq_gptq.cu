@@ -211,13 +211,15 @@ __global__ void __launch_bounds__(128) chol_panel_kernel(float* __restrict__ A, 
 }
 
 // ------------------------------------------------- blocked lower inverse
-// Y[i0:i0+b, i0:i0+b] = inverse of the lower block M[i0:i0+b, i0:i0+b]:
-// thread c solves M y = e_c by forward substitution.
+// Y[i0:i0+b, i0:i0+b] = inverse of the lower block M[i0:i0+b, i0:i0+b],
+// i0 = blockIdx.x * kCB (every diagonal block in one launch: each needs only
+// its own block of M): thread c solves M y = e_c by forward substitution.
 __global__ void __launch_bounds__(kCB) tri_inv_diag_kernel(const float* __restrict__ M,
-                                                           float* __restrict__ Y, int64_t n,
-                                                           int64_t i0, int b) {
+                                                           float* __restrict__ Y, int64_t n) {
   pdl_wait();
   pdl_trigger();
+  const int64_t i0 = (int64_t)blockIdx.x * kCB;
+  const int b = (int)min((int64_t)kCB, n - i0);
   __shared__ float L[kCB][kCB + 1];
 #pragma unroll
   for (int r = 0; r < kCB; ++r)  // thread c loads column c: all loads in flight
@@ -506,11 +508,14 @@ cudaError_t launch_gptq(const void* W, const void* X, int dt, int64_t out, int64
                     A + (k0 + b) * in + k0, in, 1, 1.0f, A + (k0 + b) * in + k0 + b, in));
     }
   }
-  // 4: Y = M^-1 (Y starts at zero above the diagonal)
+  // 4: Y = M^-1 (Y starts at zero above the diagonal): every diagonal block
+  // inverted in one launch, then each block row's off-diagonal part from the
+  // rows above it
   AWQ_TRY(cudaMemsetAsync(Y, 0, (size_t)in * in * 4, st));
+  AWQ_TRY(launch_pdl(tri_inv_diag_kernel, (unsigned)((in + kCB - 1) / kCB), kCB, 0, st, A, Y,
+                     in));
   for (int64_t i0 = 0; i0 < in; i0 += kCB) {
     const int b = (int)std::min<int64_t>(kCB, in - i0);
-    AWQ_TRY(launch_pdl(tri_inv_diag_kernel, 1, kCB, 0, st, A, Y, in, i0, b));
     if (i0 > 0) {
       AWQ_TRY(sgemm(st, b, (int)i0, (int)i0, 1.0f, A + i0 * in, in, 0, Y, in, 0, 0.0f, T, i0));
       AWQ_TRY(sgemm(st, b, (int)i0, b, -1.0f, Y + i0 * in + i0, in, 0, T, i0, 0, 0.0f,
