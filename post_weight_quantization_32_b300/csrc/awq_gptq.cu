@@ -90,6 +90,21 @@ cudaError_t sgemm(cudaStream_t s, int m, int n, int k, float alpha, const float*
   return blas_gemm(s, m, n, k, alpha, A, lda, ta, B, ldb, tb, beta, C, ldc, kDtF32);
 }
 
+// batch row-major products C_i = alpha A_i B_i + beta C_i (no transposes),
+// operand i at A + i * sa, B + i * sb, C + i * sc; float32 emulated as above
+cudaError_t sgemm_batched(cudaStream_t s, int m, int n, int k, float alpha, const float* A,
+                          int64_t lda, int64_t sa, const float* B, int64_t ldb, int64_t sb,
+                          float beta, float* C, int64_t ldc, int64_t sc, int batch) {
+  if (m <= 0 || n <= 0 || k <= 0 || batch <= 0) return cudaSuccess;
+  cublasHandle_t h = blas_handle();
+  if (h == nullptr || cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+  const cublasStatus_t r = cublasGemmStridedBatchedEx(
+      h, CUBLAS_OP_N, CUBLAS_OP_N, n, m, k, &alpha, B, CUDA_R_32F, (int)ldb, sb, A, CUDA_R_32F,
+      (int)lda, sa, &beta, C, CUDA_R_32F, (int)ldc, sc, batch, CUBLAS_COMPUTE_32F_EMULATED_16BFX9,
+      CUBLAS_GEMM_DEFAULT);
+  return r == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
 // ------------------------------------------------------- inputs and Hessian
 // Xr[t][j] = X[t][in - 1 - j] / s[in - 1 - j] (fp32)
 template <typename T>
@@ -514,7 +529,25 @@ cudaError_t launch_gptq(const void* W, const void* X, int dt, int64_t out, int64
   AWQ_TRY(cudaMemsetAsync(Y, 0, (size_t)in * in * 4, st));
   AWQ_TRY(launch_pdl(tri_inv_diag_kernel, (unsigned)((in + kCB - 1) / kCB), kCB, 0, st, A, Y,
                      in));
-  for (int64_t i0 = 0; i0 < in; i0 += kCB) {
+  const int64_t nblk = (in + kCB - 1) / kCB;
+  if (in % kCB == 0 && (nblk & (nblk - 1)) == 0) {
+    // a power-of-two count of blocks: recursive doubling.  With the inverses
+    // Y_A, Y_C of two neighbouring sz x sz lower triangles and the block B of
+    // M below the first, inv([[A, 0], [B, C]]) = [[Y_A, 0], [-Y_C B Y_A,
+    // Y_C]]; every pair of a level in one batched call (pairs 2 sz (in + 1)
+    // elements apart along the diagonal).  B Y_A goes to the upper triangle
+    // of A's storage, unused until U is written there.
+    for (int64_t sz = kCB; sz < in; sz *= 2) {
+      const int batch = (int)(in / (2 * sz));
+      const int64_t stride = 2 * sz * (in + 1);
+      float* Tb = A + sz;                  // rows [0, sz), columns [sz, 2 sz): scratch
+      AWQ_TRY(sgemm_batched(st, (int)sz, (int)sz, (int)sz, 1.0f, A + sz * in, in, stride, Y, in,
+                            stride, 0.0f, Tb, in, stride, batch));
+      AWQ_TRY(sgemm_batched(st, (int)sz, (int)sz, (int)sz, -1.0f, Y + sz * in + sz, in, stride,
+                            Tb, in, stride, 0.0f, Y + sz * in, in, stride, batch));
+    }
+  }
+  for (int64_t i0 = 0; i0 < in && (in % kCB != 0 || (nblk & (nblk - 1)) != 0); i0 += kCB) {
     const int b = (int)std::min<int64_t>(kCB, in - i0);
     if (i0 > 0) {
       AWQ_TRY(sgemm(st, b, (int)i0, (int)i0, 1.0f, A + i0 * in, in, 0, Y, in, 0, 0.0f, T, i0));

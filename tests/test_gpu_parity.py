@@ -357,11 +357,14 @@ def test_clip_search_matches_oracle(awq, case):
 
 
 GPTQ_CASES = [
-    # (out, in, N, dtype, bits, group, sym, with AWQ scales)
+    # (out, in, N, dtype, bits, group, sym, with AWQ scales).  A power-of-two
+    # count of 64-column blocks (in = 256, 512, 1024) takes the doubling
+    # inverse; 384 and 160 the block-row loop
     (64, 256, 512, "bf16", 4, 128, True, True),
     (48, 384, 300, "f16", 3, 64, False, True),
     (37, 160, 50, "f32", 4, 32, True, False),      # fewer tokens than inputs; partial blocks
     (96, 512, 2048, "bf16", 2, 128, False, True),
+    (64, 1024, 256, "f16", 4, 128, True, True),    # four doubling levels
 ]
 
 
