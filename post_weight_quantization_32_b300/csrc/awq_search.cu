@@ -506,8 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t exact_mask = 0;
       for (int a = 0; a < na; ++a)
         if (p.pow2_s[ag * p.a_per + a] != 0) exact_mask |= 1u << a;
-      // the step's lower clamp 1e-8, scaled like t (XS: one alpha per unit)
-      const float clampk = XS ? 1e-8f * __ldg(wa.escale + ag) : 1e-8f;
+      // XS: t is scaled by 2^e (one alpha per unit), and so are the step's
+      // lower clamp 1e-8 and the group ranges read from memory
+      const float esc = XS ? __ldg(wa.escale + ag) : 1.0f;
+      const float clampk = 1e-8f * esc;
       // this thread's W row, for the group ranges read from memory (GP, GV)
       const int64_t grow = (GP || GV) ? min((int64_t)(u / units_per_rt) * kRows + row,
                                             (int64_t)p.out - 1)
@@ -543,10 +545,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t gi = ((int64_t)(ag * p.a_per + a) * p.out + grow) * wa.ngroups +
                                (kg * JC) / wa.group;  // kg * JC < in <= 2^24
             if (SYM) {
-              r0[0][0] = __ldg(wa.gext + gi);
+              r0[0][0] = __ldg(wa.gext + gi) * esc;
             } else {
-              r0[0][0] = -__ldg(wa.gext + 2 * gi);
-              r1[0][0] = __ldg(wa.gext + 2 * gi + 1);
+              r0[0][0] = -__ldg(wa.gext + 2 * gi) * esc;
+              r1[0][0] = __ldg(wa.gext + 2 * gi + 1) * esc;
             }
           }
           // GV: the extremes of the (at most kMaxJobGroups) groups the job touches
@@ -829,7 +831,9 @@ using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMa
                           const SearchArgs, const WideArgs);
 
 template <typename WT>
-KernelFn pick_xs(int group, int sym) {
+KernelFn pick_xs(int group, int sym, int64_t in) {
+  if (search_wide_group(group, in))
+    return sym ? &awq_search_kernel<WT, 0, true, true> : &awq_search_kernel<WT, 0, false, true>;
   switch (group) {
     case 8: return sym ? &awq_search_kernel<WT, 8, true, true> : &awq_search_kernel<WT, 8, false, true>;
     case 16: return sym ? &awq_search_kernel<WT, 16, true, true> : &awq_search_kernel<WT, 16, false, true>;
@@ -887,10 +891,12 @@ bool search_needs_ranges(int64_t group, int64_t in) {
 
 bool search_xs_eligible(int dt, int64_t in, int64_t N, int group, int grid) {
   // one alpha per unit (more than 128 tokens), a group inside one producer
-  // job (8, 16, 32, 64 or 128 columns), 16-bit W, and
+  // job (8, 16, 32, 64 or 128 columns) or one read from the precomputed
+  // ranges of a wide group (256 k columns or a whole row), 16-bit W, and
   // all n_alpha copies of X / s small enough to stay in L2 during the search
   const int64_t n_alpha = (int64_t)grid + 1;
-  return dt != kDtF32 && N > 128 && in % 8 == 0 && in_job_group(group) &&
+  return dt != kDtF32 && N > 128 && in % 8 == 0 &&
+         (in_job_group(group) || search_wide_group(group, in)) &&
          n_alpha * N * in * 2 <= ((int64_t)64 << 20);
 }
 
@@ -949,7 +955,8 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
   CUtensorMapDataType wt;
   uint32_t wbox;
   const bool xs = ss32 != nullptr;
-  if (xs && (gext != nullptr || pl.a_per != 1 || dt == kDtF32)) return cudaErrorInvalidValue;
+  if (xs && ((gext != nullptr && !search_wide_group(group, in)) || pl.a_per != 1 || dt == kDtF32))
+    return cudaErrorInvalidValue;
   switch (dt) {
     case kDtF32:
       fn = pick_g<float>(group, sym, in, gext != nullptr);
@@ -957,12 +964,12 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
       wbox = 32;
       break;
     case kDtF16:
-      fn = xs ? pick_xs<__half>(group, sym) : pick_g<__half>(group, sym, in, gext != nullptr);
+      fn = xs ? pick_xs<__half>(group, sym, in) : pick_g<__half>(group, sym, in, gext != nullptr);
       wt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
       wbox = 64;
       break;
     default:
-      fn = xs ? pick_xs<__nv_bfloat16>(group, sym)
+      fn = xs ? pick_xs<__nv_bfloat16>(group, sym, in)
               : pick_g<__nv_bfloat16>(group, sym, in, gext != nullptr);
       wt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
       wbox = 64;

@@ -217,6 +217,11 @@ WIDE_GROUP_CASES = [
     (300, 2056, 20, "bf16", 8, None, False, 4),    # ragged last K block
     (128, 1024, 300, "f16", 4, 1024, True, 20),    # two token tiles
     (100, 1536, 24, "bf16", 4, 768, False, 20),    # three 256-column multiples per group
+    # more than 128 tokens and 16-bit: the pre-divided kernel with the stored
+    # ranges scaled by its power of two
+    (256, 1024, 256, "bf16", 4, 256, False, 20),
+    (192, 2048, 200, "f16", 3, None, True, 10),
+    (96, 2056, 160, "bf16", 4, None, False, 6),    # ragged last K block
 ]
 
 
