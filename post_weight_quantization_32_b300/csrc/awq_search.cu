@@ -564,10 +564,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               vlo[i] = vhi[i] = 0.0f;
               if (i < vgn) {
                 if (SYM) {
-                  vhi[i] = __ldg(wa.gext + gi0 + i);
+                  vhi[i] = __ldg(wa.gext + gi0 + i) * esc;
                 } else {
-                  vlo[i] = -__ldg(wa.gext + 2 * (gi0 + i));
-                  vhi[i] = __ldg(wa.gext + 2 * (gi0 + i) + 1);
+                  vlo[i] = -__ldg(wa.gext + 2 * (gi0 + i)) * esc;
+                  vhi[i] = __ldg(wa.gext + 2 * (gi0 + i) + 1) * esc;
                 }
               }
             }
@@ -834,6 +834,8 @@ template <typename WT>
 KernelFn pick_xs(int group, int sym, int64_t in) {
   if (search_wide_group(group, in))
     return sym ? &awq_search_kernel<WT, 0, true, true> : &awq_search_kernel<WT, 0, false, true>;
+  if (search_needs_ranges(group, in))
+    return sym ? &awq_search_kernel<WT, -1, true, true> : &awq_search_kernel<WT, -1, false, true>;
   switch (group) {
     case 8: return sym ? &awq_search_kernel<WT, 8, true, true> : &awq_search_kernel<WT, 8, false, true>;
     case 16: return sym ? &awq_search_kernel<WT, 16, true, true> : &awq_search_kernel<WT, 16, false, true>;
@@ -891,12 +893,12 @@ bool search_needs_ranges(int64_t group, int64_t in) {
 
 bool search_xs_eligible(int dt, int64_t in, int64_t N, int group, int grid) {
   // one alpha per unit (more than 128 tokens), a group inside one producer
-  // job (8, 16, 32, 64 or 128 columns) or one read from the precomputed
-  // ranges of a wide group (256 k columns or a whole row), 16-bit W, and
+  // job (8, 16, 32, 64 or 128 columns) or one read from precomputed ranges
+  // (wider groups, or groups that straddle the jobs), 16-bit W, and
   // all n_alpha copies of X / s small enough to stay in L2 during the search
   const int64_t n_alpha = (int64_t)grid + 1;
   return dt != kDtF32 && N > 128 && in % 8 == 0 &&
-         (in_job_group(group) || search_wide_group(group, in)) &&
+         (in_job_group(group) || search_needs_ranges(group, in)) &&
          n_alpha * N * in * 2 <= ((int64_t)64 << 20);
 }
 
@@ -955,8 +957,7 @@ cudaError_t launch_search(const void* W, const void* Xf16, int dt, int64_t out, 
   CUtensorMapDataType wt;
   uint32_t wbox;
   const bool xs = ss32 != nullptr;
-  if (xs && ((gext != nullptr && !search_wide_group(group, in)) || pl.a_per != 1 || dt == kDtF32))
-    return cudaErrorInvalidValue;
+  if (xs && (pl.a_per != 1 || dt == kDtF32)) return cudaErrorInvalidValue;
   switch (dt) {
     case kDtF32:
       fn = pick_g<float>(group, sym, in, gext != nullptr);

@@ -84,17 +84,16 @@ def test_workspace_query(lib):
 
 def test_workspace_of_the_pre_divided_path(lib):
     full = lambda *a: _ws(lib, *a, fn="awq_search_workspace_bytes")  # noqa: E731
-    # 16-bit, more than 128 tokens, group 128 (or a wide group read from its
+    # 16-bit, more than 128 tokens, group 128 (or a group read from its
     # precomputed ranges), 21 copies of X / s within 64 MiB: the full
     # workspace adds the copies (fp16, N x in each) and the scaled s table
     for dt in (1, 2):
-        for g in (128, 256, 4096):
+        for g in (128, 256, 4096, 96):
             assert full(dt, 4096, 4096, 256, g, 20) >= (
                 _ws(lib, 1, 4096, 4096, 256, g, 20) + 21 * 256 * 4096 * 2 + 21 * 4096 * 4)
-    # not eligible: fp32, 128 tokens or fewer, a group straddling the producer
-    # jobs (96), or copies beyond 64 MiB
+    # not eligible: fp32, 128 tokens or fewer, or copies beyond 64 MiB
     for args in ((0, 4096, 4096, 256, 128, 20), (1, 4096, 4096, 128, 128, 20),
-                 (1, 4096, 4096, 256, 96, 20), (2, 8192, 28672, 1024, 128, 40)):
+                 (1, 4096, 4096, 128, 96, 20), (2, 8192, 28672, 1024, 128, 40)):
         assert full(*args) == _ws(lib, *args)
 
 

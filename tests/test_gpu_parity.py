@@ -192,6 +192,10 @@ SEARCH_CASES = [
     (96, 768, 50, "f16", 4, 48, True, 12),
     (70, 1536, 20, "bf16", 4, 24, False, 8),       # up to four groups in one job
     (33, 240, 9, "f32", 3, 40, True, 5),           # ragged K block
+    # the same with more than 128 tokens and 16-bit: X pre-divided by s, the
+    # stored ranges scaled by the same power of two as t
+    (160, 480, 200, "f16", 4, 96, True, 10),
+    (96, 384, 150, "bf16", 3, 24, False, 8),
 ]
 
 
