@@ -88,12 +88,12 @@ def test_workspace_of_the_pre_divided_path(lib):
     # precomputed ranges), 21 copies of X / s within 64 MiB: the full
     # workspace adds the copies (fp16, N x in each) and the scaled s table
     for dt in (1, 2):
-        for g in (128, 256, 4096, 96):
-            assert full(dt, 4096, 4096, 256, g, 20) >= (
-                _ws(lib, 1, 4096, 4096, 256, g, 20) + 21 * 256 * 4096 * 2 + 21 * 4096 * 4)
+        for n_in, g in ((4096, 128), (4096, 256), (4096, 4096), (3072, 96)):
+            assert full(dt, 4096, n_in, 256, g, 20) >= (
+                _ws(lib, 1, 4096, n_in, 256, g, 20) + 21 * 256 * n_in * 2 + 21 * n_in * 4)
     # not eligible: fp32, 128 tokens or fewer, or copies beyond 64 MiB
     for args in ((0, 4096, 4096, 256, 128, 20), (1, 4096, 4096, 128, 128, 20),
-                 (1, 4096, 4096, 128, 96, 20), (2, 8192, 28672, 1024, 128, 40)):
+                 (1, 4096, 3072, 128, 96, 20), (2, 8192, 28672, 1024, 128, 40)):
         assert full(*args) == _ws(lib, *args)
 
 
