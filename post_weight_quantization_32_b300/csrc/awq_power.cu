@@ -3,30 +3,34 @@
 // relative output error divides ||X W^T - X Wq^T||^2 by ||X W^T||^2; the
 // notebook's "Output MSE vs bit width" reports the same ratio).
 //
-// The product is never stored: each work unit is one 128-row tile of W
-// against one tile of nt tokens of X, accumulated over all of K in tensor
-// memory, and the epilogue squares the accumulator and sums it.  The plain
-// GEMM route (product written as float32, then squared) moved 4 MB out and
-// back and left most SMs idle on short layers; here the only traffic is W
-// and X (once from HBM; the tiles sharing a row tile run side by side and
-// meet in L2).
+// The product is never stored: each tile of 128 W rows against a tile of
+// tokens of X is accumulated in tensor memory and the epilogue squares the
+// accumulator and sums it.  The plain GEMM route (product written as
+// float32, then squared) moved 4 MB out and back and left most SMs idle on
+// short layers; here the only traffic is W and X.  Two forms:
+//   power_split_kernel    layers with fewer 128 x 256 (or 128 x 128) tiles
+//                         than SMs: the four (or two) CTAs of a cluster share
+//                         a tile, each over a share of K, and add their
+//                         partial products over distributed shared memory
+//                         before squaring; a one-CTA launch adds the CTAs'
+//                         float64 partials in order.
+//   power_mma_kernel      the others: persistent CTAs over (128-row, 32- to
+//                         256-token) units, two alternating accumulators, the
+//                         units' partials added in unit order by the last CTA.
 //
-// Roles (192 threads):
-//   warp 0       tensor memory owner; lane 0 issues the TMA loads, one W
-//                block (128 rows x 64 columns) and one X block (nt tokens x
-//                64 columns) per ring stage, 128-byte swizzled, starting
-//                at a K block that differs between row tiles
-//   warp 1       lane 0 issues tcgen05.mma (kind::f16, M = 128, N = nt,
-//                K = 16) from both shared-memory operands into one of two
-//                accumulators of nt columns, so a unit's epilogue overlaps
-//                the next unit's products
+// Roles (192 threads) in both:
+//   warp 0       tensor memory owner and TMA loader: W blocks (128 rows x 64
+//                columns) and X blocks (tokens x 64 columns), 128-byte
+//                swizzled, into a ring of stages
+//   warp 1       tcgen05.mma issuer (kind::f16, M = 128, N = the token tile,
+//                K = 16), both operands from shared memory
 //   warps 2..5   epilogue: thread = row; each warp reads the tensor-memory
-//                lane quarter it may access, squares and sums its row
-//                (float32 over 16 columns, float64 across them), then the
-//                four warps add their sums in a fixed order into the unit's
-//                float64 partial.  The last CTA to finish (a ticket) adds
-//                the partials in unit order: repeated calls give identical
-//                results.
+//                lane quarter it may access and squares and sums its row
+//                (float32 over 16 columns, float64 across them); the four
+//                warps add their sums in a fixed order.
+// The loader and MMA warps run their loops as whole warps, the elected lane
+// issuing, and count their ring positions (no division in a loop).  Every
+// summation order is fixed, so repeated calls give identical results.
 // Rows past `out`, tokens past N and columns past `in` are read by TMA as
 // zeros and add nothing.  Every wait is bounded; a timeout sets the status
 // word to AWQ_ERR_TIMEOUT.

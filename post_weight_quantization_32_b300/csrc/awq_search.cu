@@ -8,13 +8,17 @@
 // Work unit = (128-row tile of W, a group of up to 8 alphas, a token tile of
 // T <= 256 tokens).  One persistent CTA per SM walks a static list of units.
 // Warp roles inside a CTA (512 threads, four warpgroups):
-//   warpgroup 0 (48 registers a thread after setmaxnreg):
+//   warpgroup 0 (56 registers a thread after setmaxnreg):
 //     warp 0    TMA loads of W blocks (128 rows x 64 columns) together with
 //               the matching 64 columns of the s and 2^e/s tables of the
 //               unit's alphas, into one ring stage
 //     warp 1    TMA loads of X blocks (T tokens x 64 columns, fp16)
-//     warp 2    tensor memory owner and the single tcgen05.mma issuer
+//     warp 2    tensor memory owner and the tcgen05.mma issuer
 //     warp 3    idle
+//   Warps 0-2 run their loops as whole warps, the lane elect.sync picks
+//   issuing each copy, MMA and commit, and every role counts its ring
+//   positions: a loop on one lane, or a division by a ring depth per
+//   iteration, cost hundreds of cycles an iteration here.
 //   warpgroups 1 and 2 (200 registers a thread): producers, thread = one W
 //     row.  Per 128-column job (one quantization group for group 128) and
 //     alpha, pass 1 forms t = w * s in registers and the group's range;
