@@ -8,12 +8,12 @@
 // accumulator and sums it.  The plain GEMM route (product written as
 // float32, then squared) moved 4 MB out and back and left most SMs idle on
 // short layers; here the only traffic is W and X.  Two forms:
-//   power_split_kernel    layers with fewer 128 x 256 (or 128 x 128) tiles
-//                         than SMs: the four (or two) CTAs of a cluster share
-//                         a tile, each over a share of K, and add their
-//                         partial products over distributed shared memory
-//                         before squaring; a one-CTA launch adds the CTAs'
-//                         float64 partials in order.
+//   power_split_kernel    layers with few 128 x 128 tiles: the two (or four)
+//                         CTAs of a cluster share a tile, each over a share
+//                         of K, and add their partial products over
+//                         distributed shared memory before squaring; a
+//                         one-CTA launch adds the CTAs' float64 partials in
+//                         order.
 //   power_mma_kernel      the others: persistent CTAs over (128-row, 32- to
 //                         256-token) units, two alternating accumulators, the
 //                         units' partials added in unit order by the last CTA.
@@ -357,18 +357,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (threadIdx.x == 0 && c.abort) set_status(p.status, ST_TIMEOUT);
 }
 
-// ---- split-K form, for layers with fewer 128 x NT tiles than SMs ----------
-// The KS CTAs of a cluster share one tile (128 W rows x NT tokens): CTA r
-// accumulates K blocks [r n_kb / KS, (r + 1) n_kb / KS) in tensor memory and
-// stages its float32 accumulator in its own shared memory (over the drained
-// ring) as [NT / 4][128 rows][4 tokens], so that a row's four consecutive
-// tokens are one 16-byte vector and a warp's vectors are contiguous.  After a cluster barrier CTA r forms,
-// for tokens [r NT / KS, (r + 1) NT / KS), the sum of the KS partial
-// products in rank order, squares it and sums its rows; every output entry
-// is formed in one fixed order.  Each CTA writes one float64 partial and a
-// one-CTA launch adds them in order.  Wide tiles read W once per NT tokens
-// from shared memory, where 64-token tiles were bound by shared-memory
-// bandwidth (each 64-column block written by TMA and read by the MMA).
+// ---- split-K form, for layers with few 128 x NT tiles ---------------------
+// The KS CTAs of a cluster share one tile (128 W rows x NT tokens, NT = 128):
+// CTA r accumulates K blocks [r n_kb / KS, (r + 1) n_kb / KS) in tensor
+// memory and stages its float32 accumulator in its own shared memory (over
+// the drained ring) as [NT / 4][128 rows][4 tokens], so that a row's four
+// consecutive tokens are one 16-byte vector and a warp's vectors are
+// contiguous.  After a cluster barrier CTA r forms, for tokens
+// [r NT / KS, (r + 1) NT / KS), the sum of the KS partial products in rank
+// order, squares it and sums its rows; every output entry is formed in one
+// fixed order.  Each CTA writes one float64 partial and a one-CTA launch adds
+// them in order.  A 128-token tile reads W from shared memory once per 128
+// tokens, where 64-token tiles were bound by shared-memory bandwidth (each
+// 64-column block written by TMA and read by the MMA).
 struct SplitArgs {
   int n_kb;          // K blocks of the layer
   int n_tt;          // token tiles
@@ -611,23 +612,25 @@ cudaError_t launch_power_dt(int nt, const CUtensorMap& mw, const CUtensorMap& mx
   }
 }
 
-// Split-K plan: 256-token tiles (N > 128) or 128-token tiles (64 < N <= 128),
-// KS = 4 or 2 when that many CTAs per tile still fit one a SM and each
-// keeps at least four K blocks; ks = 0 leaves the layer to the persistent
-// kernel.
+// Split-K plan: 128-token tiles (N > 64), four CTAs a tile where the layer
+// would otherwise leave most SMs idle, else two, as long as that many CTAs
+// still fit one a SM and each keeps at least four K blocks; ks = 0 leaves
+// the layer to the persistent kernel.  Measured on the notebook-shaped layer
+// (4096 x 4096, 256 tokens): 128-token tiles split two ways 23.6 us, 256-token
+// tiles split four ways 25.6 us (the cluster reduction reads three remote
+// slices instead of one), two ways 29.7 us.
+constexpr int kSplitNT = 128;
 void split_plan(int64_t out, int64_t in, int64_t N, int sms, int& nt, int& ks) {
   nt = 0;
   ks = 0;
   if (N <= 64) return;
-  nt = N > 128 ? 256 : 128;
+  nt = kSplitNT;
   const int64_t tiles = ((out + kPRows - 1) / kPRows) * ((N + nt - 1) / nt);
   const int64_t n_kb = (in + kPKB - 1) / kPKB;
-  for (int cand : {4, 2}) {
-    if (tiles * cand <= sms && n_kb >= 4 * cand) {
-      ks = cand;
-      return;
-    }
-  }
+  if (tiles * 4 <= sms / 2 && n_kb >= 16)
+    ks = 4;
+  else if (tiles * 2 <= sms && n_kb >= 8)
+    ks = 2;
 }
 
 template <bool BF16, int NT, int KS>
@@ -642,13 +645,10 @@ cudaError_t launch_split_tile(const CUtensorMap& mw, const CUtensorMap& mx, cons
 }
 
 template <bool BF16>
-cudaError_t launch_split_dt(int nt, int ks, const CUtensorMap& mw, const CUtensorMap& mx,
+cudaError_t launch_split_dt(int ks, const CUtensorMap& mw, const CUtensorMap& mx,
                             const SplitArgs& a, int grid, cudaStream_t stream) {
-  if (nt == 256)
-    return ks == 4 ? launch_split_tile<BF16, 256, 4>(mw, mx, a, grid, stream)
-                   : launch_split_tile<BF16, 256, 2>(mw, mx, a, grid, stream);
-  return ks == 4 ? launch_split_tile<BF16, 128, 4>(mw, mx, a, grid, stream)
-                 : launch_split_tile<BF16, 128, 2>(mw, mx, a, grid, stream);
+  return ks == 4 ? launch_split_tile<BF16, kSplitNT, 4>(mw, mx, a, grid, stream)
+                 : launch_split_tile<BF16, kSplitNT, 2>(mw, mx, a, grid, stream);
 }
 
 }  // namespace
@@ -693,8 +693,8 @@ cudaError_t launch_power_mma(const void* W, const void* X, int dt, int64_t out, 
       a.diag = reinterpret_cast<uint32_t*>(wsb) + 16;
       a.status = dev_status;
       a.wait_limit_ns = 2000000000ull;
-      cudaError_t e = dt == kDtF16 ? launch_split_dt<false>(snt, ks, mw, mx, a, grid, stream)
-                                   : launch_split_dt<true>(snt, ks, mw, mx, a, grid, stream);
+      cudaError_t e = dt == kDtF16 ? launch_split_dt<false>(ks, mw, mx, a, grid, stream)
+                                   : launch_split_dt<true>(ks, mw, mx, a, grid, stream);
       if (e != cudaSuccess) return e;
       return launch_pdl(power_finish_kernel, 1, 256, 0, stream, a.partials, grid,
                         (double)N * (double)out, power);

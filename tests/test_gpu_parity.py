@@ -239,18 +239,20 @@ def test_search_wide_groups_match_oracle(awq, case):
     check_pack(awq, W, res.s32[b], bits, n_in if group is None else group, sym)
 
 
-# 16-bit layers take a tensor-core kernel.  Layers with few 128 x 256 (or
-# 128 x 128) tiles split each tile's K range over a cluster of CTAs:
-# (300, 1032, 300) four CTAs a tile, ragged rows, tokens and K (1032 = 16
-# blocks of 64 + 8); (2048, 2048, 1024) two CTAs a tile; (384, 1024, 100)
-# 128-token tiles.  The others take the persistent kernel (token tiles of 32,
-# 64, 128 or 256, two K blocks a ring stage below 256): (256, 512, 64)
-# 64-token tiles; (9600, 136, 250) 128-token tiles; (9600, 512, 600) 225
-# units, more than one a CTA, so both accumulators alternate; (19000, 64,
-# 256) 256-token tiles, one K block; (130, 264, 17) a 32-token tile for 17
-# tokens; (1, 64, 1) one row and one token.  float32 takes the GEMM route.
+# 16-bit layers take a tensor-core kernel.  Layers with few 128-row x
+# 128-token tiles split each tile's K range over a cluster of CTAs: four a
+# tile for (300, 1032, 300) (ragged rows, tokens and K: 1032 = 16 blocks of
+# 64 + 8) and (384, 1024, 100), two a tile for (4096, 512, 256).  The others
+# take the persistent kernel (token tiles of 32, 64, 128 or 256, two K
+# blocks a ring stage below 256): (256, 512, 64) 64-token tiles; (2048,
+# 2048, 1024) 256 units, more than one a CTA, so both accumulators
+# alternate; (9600, 136, 250) 128-token tiles; (9600, 512, 600) 225 units;
+# (19000, 64, 256) 256-token tiles, one K block; (130, 264, 17) a 32-token
+# tile for 17 tokens; (1, 64, 1) one row and one token.  float32 takes the
+# GEMM route.
 @pytest.mark.parametrize("dtype,shape", [("f16", (256, 512, 64)), ("bf16", (300, 1032, 300)),
                                          ("f16", (2048, 2048, 1024)), ("bf16", (384, 1024, 100)),
+                                         ("f16", (4096, 512, 256)),
                                          ("f16", (9600, 136, 250)), ("bf16", (9600, 512, 600)),
                                          ("bf16", (19000, 64, 256)), ("bf16", (130, 264, 17)),
                                          ("f32", (96, 256, 17)), ("bf16", (1, 64, 1))])
