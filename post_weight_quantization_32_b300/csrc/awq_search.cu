@@ -708,13 +708,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int a = 0; a < na; ++a) {
         float acc = 0.0f;
         const uint32_t cb = tmem + lane_addr + (uint32_t)(a * p.T);
-        for (int cc = 0; cc < p.T; cc += 16) {
-          uint32_t v[16];
+        for (int cc = 0; cc < p.T; cc += 32) {  // T is a multiple of 32: two loads, one wait
+          uint32_t v[16], w[16];
           tmem_ld16(cb + (uint32_t)cc, v);
+          tmem_ld16(cb + (uint32_t)cc + 16u, w);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float f = __uint_as_float(v[i]);
+            acc = fmaf(f, f, acc);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float f = __uint_as_float(w[i]);
             acc = fmaf(f, f, acc);
           }
         }
